@@ -1,0 +1,81 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module only draws random numbers; it holds none of the attention
+arithmetic.  Both the CUDA path (through the tests and the benchmark) and the
+fp64 oracle consume what it produces.
+
+Recipe: a CPU ``torch.Generator`` seeded with ``seed``; q, k, v drawn in that
+order as float32 iid N(0, 1) of shape [B, H, S, D]; k multiplied by
+``k_scale`` in float32 (the grouped-query workload stresses the softmax range
+with k_scale = 3); every tensor then rounded once to bf16 (round to nearest
+even).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, asdict
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    S_q: int
+    S_kv: int
+    D: int
+    causal: bool
+    k_scale: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flops(self) -> float:
+        """4 * B * H_q * S_q * S_kv * D, halved when causal (two GEMMs of 2*M*N*K)."""
+        f = 4.0 * self.B * self.H_q * self.S_q * self.S_kv * self.D
+        return f / 2.0 if self.causal else f
+
+    def as_dict(self) -> dict:
+        d = asdict(self)
+        d["scale"] = self.scale
+        return d
+
+
+# The headline workloads: shapes, masks and distributions of the pages'
+# attention-forward microbenchmarks (long-sequence case at S = 16384).
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("single_head_b1_h1_s256_d64", 1, 1, 1, 256, 256, 64, False),
+        Workload("batched_b4_h16_s2048_d128", 4, 16, 16, 2048, 2048, 128, False),
+        Workload("causal_b2_h16_s8192_d128", 2, 16, 16, 8192, 8192, 128, True),
+        Workload("long_b1_h32_s16384_d128", 1, 32, 32, 16384, 16384, 128, False),
+        Workload("long_causal_b1_h32_s16384_d128", 1, 32, 32, 16384, 16384, 128, True),
+        Workload("gqa_b8_hq32_hkv8_s4096_d64_k3", 8, 32, 8, 4096, 4096, 64, True, k_scale=3.0),
+    ]
+}
+
+HEADLINE = "long_b1_h32_s16384_d128"
+
+
+def make_qkv(B: int, H_q: int, H_kv: int, S_q: int, S_kv: int, D: int,
+             k_scale: float = 1.0, seed: int = 0):
+    """q [B,H_q,S_q,D], k and v [B,H_kv,S_kv,D], all bf16 on the CPU."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((B, H_q, S_q, D), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H_kv, S_kv, D), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H_kv, S_kv, D), generator=g, dtype=torch.float32)
+    if k_scale != 1.0:
+        k = k * k_scale
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def make_workload(w: Workload):
+    return make_qkv(w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.D, w.k_scale, w.seed)

@@ -1,0 +1,176 @@
+"""fp64 CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference arm may import this package.  The CUDA product path never touches
+it: the two share no code, header, table or helper.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over output
+rows).  It is the definition written out, following "PipeThreader:
+Software-Defined Pipelining for Efficient DNN Execution", section A2,
+paragraph "FlashAttention-3" and Fig. 7 (acc_s = Q K^T -> Softmax -> P ->
+P V = O), with the readings listed at the top of the C file (scale before
+the mask, top-left causal mask j <= i, grouped heads h // (H_q / H_kv),
+natural-log LSE, [B, H, S, D] layout).
+
+This module only builds the shared library and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_default = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_source(_SRC, _LIB)
+    return _LIB
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc a C file with the oracle's exported functions into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+           "-fno-fast-math", "-ffp-contract=off", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    ci, cd = ctypes.c_int, ctypes.c_double
+    lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p,
+                                    ci, ci, ci, ci, ci, ci, ci, cd]
+    lib.oracle_attn_fwd.restype = ci
+    lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, i64p, ctypes.c_int64,
+                                     f64p, f64p, ci, ci, ci, ci, ci, ci, ci, cd]
+    lib.oracle_attn_rows.restype = ci
+    lib.oracle_attn_probs.argtypes = [u16p, u16p, u16p, f64p, f64p, f64p,
+                                      ci, ci, ci, ci, ci, ci, ci, cd]
+    lib.oracle_attn_probs.restype = ci
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ci
+    return lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 input as a contiguous uint16 bit array.
+
+    Accepts a torch.bfloat16 tensor (any device; copied to the CPU) or a numpy
+    uint16 array of bf16 bit patterns.
+    """
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("numpy inputs must be uint16 bf16 bit patterns")
+        return np.ascontiguousarray(x)
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs must be bfloat16")
+    return x.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _p(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _dims(q, k, v):
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return B, Hq, Hkv, Sq, Skv, D
+
+
+class Oracle:
+    """Handle on one compiled copy of the oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.lib = _bind(path)
+
+    def attn_fwd(self, q, k, v, causal: bool, scale: float):
+        """O [B,H_q,S_q,D] and LSE [B,H_q,S_q], both float64 numpy arrays."""
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        qb, kb, vb = _bits(q), _bits(k), _bits(v)
+        o = np.empty((B, Hq, Sq, D), np.float64)
+        lse = np.empty((B, Hq, Sq), np.float64)
+        rc = self.lib.oracle_attn_fwd(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(o, ctypes.c_double), _p(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_fwd rejected the arguments (rc={rc})")
+        return o, lse
+
+    def attn_rows(self, q, k, v, rows, causal: bool, scale: float):
+        """O and LSE for the flat row indices ``rows`` into [B, H_q, S_q].
+
+        Returns (o_rows [n, D], lse_rows [n]) as float64 numpy arrays.
+        """
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        qb, kb, vb = _bits(q), _bits(k), _bits(v)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        o = np.empty((r.size, D), np.float64)
+        lse = np.empty((r.size,), np.float64)
+        rc = self.lib.oracle_attn_rows(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(r, ctypes.c_int64), r.size, _p(o, ctypes.c_double), _p(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_rows rejected the arguments (rc={rc})")
+        return o, lse
+
+    def attn_probs(self, q, k, v, causal: bool, scale: float):
+        """P [B,H_q,S_q,S_kv], O and LSE as float64 numpy arrays (tiny sizes)."""
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        qb, kb, vb = _bits(q), _bits(k), _bits(v)
+        p = np.empty((B, Hq, Sq, Skv), np.float64)
+        o = np.empty((B, Hq, Sq, D), np.float64)
+        lse = np.empty((B, Hq, Sq), np.float64)
+        rc = self.lib.oracle_attn_probs(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(p, ctypes.c_double), _p(o, ctypes.c_double), _p(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_probs rejected the arguments (rc={rc})")
+        return p, o, lse
+
+    def num_threads(self) -> int:
+        """OpenMP threads the oracle runs on."""
+        return int(self.lib.oracle_num_threads())
+
+
+def default() -> Oracle:
+    """The oracle built from attn_oracle.c (compiled on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float):
+    return default().attn_fwd(q, k, v, causal, scale)
+
+
+def attn_rows(q, k, v, rows, causal: bool, scale: float):
+    return default().attn_rows(q, k, v, rows, causal, scale)
+
+
+def attn_probs(q, k, v, causal: bool, scale: float):
+    return default().attn_probs(q, k, v, causal, scale)
+
+
+def num_threads() -> int:
+    return default().num_threads()
