@@ -1,0 +1,172 @@
+"""GB300 (sm_103a) fused attention forward -- Python binding of libattn_gb300.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/attn.h``.  PyTorch supplies
+device memory and the current CUDA stream.  There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+
+    o, lse = attn_fwd(q, k, v, causal, scale)
+
+q [B, H_q, S_q, D], k and v [B, H_kv, S_kv, D]: contiguous bf16 CUDA tensors,
+D in {64, 128}, H_q a multiple of H_kv.  o is bf16 [B, H_q, S_q, D], lse is
+fp32 [B, H_q, S_q] (natural log).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH, build as _build_lib
+
+__all__ = ["attn_fwd", "attn_fwd_out", "attn_fwd_host", "selftest_qk", "selftest_pv",
+           "device_status", "status_string", "lib_path", "AttnError", "STATUS"]
+
+STATUS = {
+    0: "ATTN_OK",
+    1: "ATTN_ERR_INVALID_ARG",
+    2: "ATTN_ERR_UNSUPPORTED",
+    3: "ATTN_ERR_MISALIGNED",
+    4: "ATTN_ERR_CUDA",
+    5: "ATTN_ERR_TIMEOUT",
+}
+
+# every entry point of include/attn.h and include/attn_selftest.h
+EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
+           "attn_version", "attn_selftest_qk", "attn_selftest_pv"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is not built; run attention_pipelining_gb300._build.build() "
+            "(needs nvcc) -- there is no fallback implementation")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp]
+    lib.attn_fwd.restype = ci
+    lib.attn_fwd_host.argtypes = [vp] * 10 + [ci] * 7 + [cf, vp]
+    lib.attn_fwd_host.restype = ci
+    lib.attn_status_string.argtypes = [ci]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_device_status.argtypes = [ctypes.POINTER(ci), ci]
+    lib.attn_device_status.restype = ci
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = ci
+    lib.attn_selftest_qk.argtypes = [vp, vp, vp, ci, vp]
+    lib.attn_selftest_qk.restype = ci
+    lib.attn_selftest_pv.argtypes = [vp, vp, vp, ci, vp]
+    lib.attn_selftest_pv.restype = ci
+    _lib = lib
+    return lib
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library (nvcc, sm_103a) if needed and load it."""
+    global _lib
+    path = _build_lib(force=force)
+    _lib = None
+    _load()
+    return path
+
+
+def status_string(code: int) -> str:
+    return _load().attn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise AttnError(code, where)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_inputs(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D [B, H, S, D] tensor")
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+
+
+def attn_fwd_out(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Writes O and LSE into caller-allocated ``o`` (bf16) and ``lse`` (fp32)."""
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    _check(_load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+                            _stream_handle(stream)), "attn_fwd")
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, stream=None):
+    """Fused attention forward; returns (o, lse) allocated on q's device."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    attn_fwd_out(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,
+                  causal: bool, scale: float, stream=None) -> None:
+    """Host-buffer entry: copies q/k/v (host, ideally pinned) into the device
+    buffers, runs the kernel, copies o/lse back, all queued on ``stream``."""
+    B, Hq, Sq, D = q_dev.shape
+    Hkv, Skv = k_dev.shape[1], k_dev.shape[2]
+    _check(_load().attn_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                 o_host.data_ptr(), lse_host.data_ptr(), q_dev.data_ptr(),
+                                 k_dev.data_ptr(), v_dev.data_ptr(), o_dev.data_ptr(),
+                                 lse_dev.data_ptr(), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)),
+                                 float(scale), _stream_handle(stream)), "attn_fwd_host")
+
+
+def selftest_qk(q, k):
+    """s = q k^T ([128, D] bf16 each) through TMA + tcgen05, fp32 [128, 128]."""
+    import torch
+    s = torch.empty((128, 128), dtype=torch.float32, device=q.device)
+    _check(_load().attn_selftest_qk(q.data_ptr(), k.data_ptr(), s.data_ptr(), q.shape[1],
+                                    _stream_handle(None)), "attn_selftest_qk")
+    return s
+
+
+def selftest_pv(p, v):
+    """o = p v (p [128, 128] bf16 via tensor memory, v [128, D] bf16), fp32 [128, D]."""
+    import torch
+    o = torch.empty((128, v.shape[1]), dtype=torch.float32, device=v.device)
+    _check(_load().attn_selftest_pv(p.data_ptr(), v.data_ptr(), o.data_ptr(), v.shape[1],
+                                    _stream_handle(None)), "attn_selftest_pv")
+    return o
+
+
+def device_status(reset: bool = True) -> int:
+    """The device-side status word (0, or 5 = a kernel wait timed out)."""
+    st = ctypes.c_int(0)
+    _check(_load().attn_device_status(ctypes.byref(st), int(bool(reset))), "attn_device_status")
+    return st.value

@@ -1,0 +1,47 @@
+// attn_internal.h -- declarations shared by the translation units of the
+// CUDA library (kernel launchers, the C ABI, the self-tests).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+
+namespace attnpipe {
+
+// Everything the fused kernel reads, passed as one __grid_constant__ block.
+struct AttnParams {
+  CUtensorMap tm_q;  // Q as [B*H_q, S_q, D], box {64, 128, 1}, 128-byte swizzle (load)
+  CUtensorMap tm_k;  // K as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
+  CUtensorMap tm_v;  // V as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
+  CUtensorMap tm_o;  // O as [B*H_q, S_q, D], box {64, 32, 1} (store, rows >= S_q dropped)
+  float* lse;        // [B, H_q, S_q]
+  int B, H_q, H_kv, S_q, S_kv, causal;
+  float scale_log2;  // scale * log2(e): the softmax runs in base 2
+  unsigned long long timeout_ns;  // budget of any single wait inside the kernel
+};
+
+// Encodes a 3-D bf16 tensor map over a contiguous [outer, rows, D] array with
+// a {64, box_rows, 1} box and 128-byte swizzle.  Returns false on failure.
+bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t rows,
+                        uint64_t outer, uint32_t box_rows);
+
+// Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(S_q / 256).
+cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream);
+
+// Reads (and optionally clears) the device status word of the current device.
+cudaError_t read_device_status(int* status, bool reset);
+
+// Reads (and optionally clears) the self-test kernels' status word.
+cudaError_t read_selftest_status(int* status, bool reset);
+
+// Self-test launchers (one CTA each).
+cudaError_t launch_selftest_qk(const CUtensorMap& tq, const CUtensorMap& tk, float* s, int D,
+                               cudaStream_t stream);
+cudaError_t launch_selftest_pv(const uint16_t* p, const CUtensorMap& tv, float* o, int D,
+                               cudaStream_t stream);
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+}  // namespace attnpipe

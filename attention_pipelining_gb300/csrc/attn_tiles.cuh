@@ -1,0 +1,78 @@
+// attn_tiles.cuh -- tile-level steps shared by the fused kernel and the
+// self-test kernels: TMA loads of one 128-row bf16 tile and the two
+// tensor-core GEMMs of the attention forward ("PipeThreader: Software-
+// Defined Pipelining for Efficient DNN Execution", section A2, Fig. 7:
+// load_k / load_v, mma_qk, mma_pv).
+//
+// Shared-memory tile layout: a [128 rows x D] bf16 tile is stored as D/64
+// slabs of [128 rows x 64 columns]; each slab is 128 rows of 128 bytes in
+// the 128-byte swizzle (16-byte chunk c of row r sits at chunk c ^ (r % 8)),
+// exactly what one TMA load with 128-byte swizzle and a {64, 128} box writes.
+// Slabs are 16 KB apart and 1024-byte aligned.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace attnpipe {
+
+constexpr int kTileRows = 128;
+constexpr int kSlabBytes = kTileRows * 128;  // one [128 x 64] bf16 slab
+
+template <int D>
+struct TileShape {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kBytes = kTileRows * D * 2;
+};
+
+// Loads rows [row0, row0 + 128) of slice z of a [*, rows, D] tensor map into
+// `dst` (a tile as above); completion is counted on `bar`.  Rows outside the
+// tensor are filled with zeros (and still counted).
+template <int D>
+__device__ __forceinline__ void tma_load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int row0, int z, uint64_t hint) {
+#pragma unroll
+  for (int s = 0; s < TileShape<D>::kSlabs; ++s)
+    tma_load_3d(dst + s * kSlabBytes, map, bar, s * 64, row0, z, hint);
+}
+
+// S[tmem, 128 x 128 fp32] = Q K^T for one 128-row Q tile and one 128-row K
+// tile.  Both operands are K-major (the head dimension is contiguous): per
+// K step of 16 elements the descriptor start advances 32 bytes inside a
+// swizzle row, and moves to the next slab every 64 elements.  Stride between
+// 8-row groups (SBO) is 1024 bytes; the leading offset is unused for
+// swizzled K-major operands.  Issued by one thread.
+template <int D>
+__device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
+    mma_ss(s_tmem, make_smem_desc_sw128(q_smem + off, 16, 1024),
+           make_smem_desc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O[tmem, 128 x D fp32] (+)= P V with P [128 x 128] bf16 in tensor memory
+// (row i in lane i, keys 2c and 2c+1 packed in column c) and V a
+// [128 keys x D] tile used MN-major (D contiguous).  Per K step of 16 keys
+// the descriptor start advances 16 rows = 2048 bytes; the 8-row groups along
+// K are 1024 bytes apart (SBO); the 64-column slabs along N are one slab
+// apart (LBO).  `accumulate` = false overwrites O.  Issued by one thread.
+template <int D>
+__device__ __forceinline__ void issue_pv_gemm(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                              bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
+  // With D = 64 there is a single slab along N and the leading offset is never
+  // used; it is set to the in-slab group stride so no field can point past the tile.
+  constexpr uint32_t lbo = (D == 64) ? 1024 : kSlabBytes;
+#pragma unroll
+  for (int kk = 0; kk < kTileRows / 16; ++kk) {
+    mma_ts(o_tmem, p_tmem + kk * 8, make_smem_desc_sw128(v_smem + kk * 2048, lbo, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+}  // namespace attnpipe

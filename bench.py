@@ -1,0 +1,421 @@
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one fused attention forward over the whole workload (one kernel
+launch), inputs resident in HBM.  Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Metric: attention forward TFLOP/s = 4 * B * H_q * S_q * S_kv * D (halved when
+causal) / time, and its fraction of the measured dense BF16 peak.
+
+Extra keys: ``roofline`` (the kernel against the measured tensor peak),
+``e2e`` (the same metric through the host-buffer C entry point, copies timed),
+``cpu_baseline`` (the fp64 oracle on a bounded sample of the same workload,
+on the host cores), ``clocks`` (nvidia-smi samples during the timed region),
+``gpu_launches``.
+
+Multi-GPU: one process per GPU under torchrun; each rank runs an independent
+replica of the workload (the path has no exchange step), the timed region is
+bracketed by barriers, and the time is the maximum over ranks.
+``--impl reference`` times the fp64 CPU oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, fp32 acc) and % of GB300 dense BF16 peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+KERNEL_SOURCES = ["attention_pipelining_gb300/csrc/attn_fwd_sm103.cu",
+                  "attention_pipelining_gb300/csrc/attn_tiles.cuh",
+                  "attention_pipelining_gb300/csrc/ptx.cuh"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS * 0.9, "fallback"
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [l.strip().split(",") for l in self.out.read().splitlines() if l.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Maximum of a per-rank scalar (time) over all ranks."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def time_oracle_rows(q, k, v, w, rows) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
+    return time.perf_counter() - t0
+
+
+def row_flops(w, rows) -> float:
+    """FLOPs of the sampled rows under the metric's convention (4*S_kv*D per
+    row, causal rows counting only their visible keys)."""
+    import numpy as np
+    i = rows % w.S_q
+    vis = np.minimum(i + 1, w.S_kv) if w.causal else np.full(rows.shape, w.S_kv)
+    return float(4.0 * w.D * vis.sum())
+
+
+def sample_rows(w, n: int, seed: int = 0):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    total = w.B * w.H_q * w.S_q
+    return np.sort(rng.choice(total, size=min(n, total), replace=False)).astype(np.int64)
+
+
+def calibrate_oracle(q, k, v, w, target_s: float):
+    """Row count whose oracle time is about target_s seconds."""
+    n = 64
+    while True:
+        rows = sample_rows(w, n)
+        dt = time_oracle_rows(q, k, v, w, rows)
+        if dt >= 0.5 or n >= w.B * w.H_q * w.S_q:
+            break
+        n *= 4
+    per_row = dt / len(rows)
+    return max(1, int(target_s / per_row))
+
+
+def cpu_baseline(q, k, v, w, target_s: float = 12.0) -> dict:
+    import oracle
+    n = calibrate_oracle(q, k, v, w, target_s)
+    rows = sample_rows(w, n, seed=1)
+    dt = time_oracle_rows(q, k, v, w, rows)
+    return {
+        "value": row_flops(w, rows) / dt / 1e12,
+        "unit": "TFLOP/s",
+        "cores": oracle.num_threads(),
+        "kind": "oracle",
+        "sample": f"{len(rows)} of {w.B * w.H_q * w.S_q} output rows of {w.name} "
+                  f"(random rows, each over its full visible key range), fp64, {dt:.1f} s",
+    }
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    import oracle
+    from attention_pipelining_gb300.synthetic import make_workload
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    oracle.build()
+    q, k, v = make_workload(w)
+    budget = 150.0
+    n = calibrate_oracle(q, k, v, w, budget / max(1, args.steps + args.warmup))
+    for s in range(args.warmup):
+        time_oracle_rows(q, k, v, w, sample_rows(w, n, seed=100 + s))
+    total_t, total_f = 0.0, 0.0
+    for s in range(args.steps):
+        rows = sample_rows(w, n, seed=s)
+        total_t += time_oracle_rows(q, k, v, w, rows)
+        total_f += row_flops(w, rows)
+    value = total_f / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{kk: vv for kk, vv in w.as_dict().items() if kk != "name"},
+                   "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n} random output rows of {w.name} per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import attention_pipelining_gb300 as ap
+    from attention_pipelining_gb300.synthetic import make_workload
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    ap.build()
+    dev = torch.device("cuda", local)
+
+    q_cpu, k_cpu, v_cpu = make_workload(w)
+    q, k, v = q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H_q, w.S_q), dtype=torch.float32, device=dev)
+    in_bytes = (q.numel() + k.numel() + v.numel()) * 2
+    out_bytes = o.numel() * 2 + lse.numel() * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ap.attn_fwd_out(q, k, v, o, lse, w.causal, w.scale, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, world)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+
+    # end to end through the host-buffer entry point: pinned host inputs in,
+    # host outputs back, copies inside the timed region
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    qh, kh, vh = q_cpu.pin_memory(), k_cpu.pin_memory(), v_cpu.pin_memory()
+    oh = torch.empty_like(q_cpu).pin_memory()
+    lh = torch.empty((w.B, w.H_q, w.S_q), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        ap.attn_fwd_host(qh, kh, vh, oh, lh, q, k, v, o, lse, w.causal, w.scale, stream)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+    if rank != 0:
+        return
+    peak, peak_sustained, peak_kind = load_peaks()
+    flops = w.flops
+    value = world * flops * args.steps / t / 1e12
+    per_launch = t_local / args.steps
+    achieved = flops / per_launch / 1e12
+    traffic = load_traffic()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S_q": w.S_q,
+            "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
+            "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
+                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+        },
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_kind": f"{peak_kind} bf16 dense (burst)",
+            "frac_of_sustained": achieved / peak_sustained,
+            "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+            "algorithmic_flops_per_launch": flops,
+            "kernel": "attn_fwd_kernel",
+        },
+        "e2e": {
+            "value": world * flops * e2e_steps / t_e2e / 1e12,
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out_bytes,
+            "steps": e2e_steps,
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(q_cpu, k_cpu, v_cpu, w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    from attention_pipelining_gb300.synthetic import HEADLINE, WORKLOADS
+    ap_ = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap_.add_argument("--gpus", type=int, default=1)
+    ap_.add_argument("--steps", type=int, default=300)
+    ap_.add_argument("--warmup", type=int, default=10)
+    ap_.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap_.add_argument("--e2e-steps", type=int, default=50)
+    ap_.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap_.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap_.parse_args(argv)
+    if args.warmup < 3:
+        ap_.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+    world, _, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

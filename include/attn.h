@@ -1,0 +1,108 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * The operation ("PipeThreader: Software-Defined Pipelining for Efficient DNN
+ * Execution", section A2, paragraph "FlashAttention-3" and Fig. 7): from Q, K
+ * and V, MatMulQK gives acc_s = Q K^T, Softmax turns acc_s into P, MatMulPV
+ * gives O = P V, all fused into one kernel.  This library computes, for each
+ * batch b, query head h and query row i,
+ *
+ *     s_ij   = scale * sum_d Q[b,h,i,d] * K[b,g,j,d]     g = h / (H_q / H_kv)
+ *     A_i    = { j < S_kv }            (non-causal)
+ *              { j < S_kv, j <= i }    (causal: top-left aligned lower triangle)
+ *     O[b,h,i,:] = sum_{j in A_i} exp(s_ij) V[b,g,j,:] / sum_{j in A_i} exp(s_ij)
+ *     LSE[b,h,i] = ln sum_{j in A_i} exp(s_ij)
+ *
+ * The kernel follows the Blackwell warp-role split described in "GPU软件流水线与
+ * Warp Specialization优化技术解析", section 3.1 (Flash Attention forward,
+ * Blackwell): loads and tensor-core GEMMs in their own warps, the softmax of
+ * two query sub-tiles in two warpgroups, the accumulator rescale in a third.
+ *
+ * Layout: Q, O are contiguous row-major [B, H_q, S_q, D] bf16; K, V are
+ * contiguous [B, H_kv, S_kv, D] bf16; LSE is contiguous [B, H_q, S_q] fp32.
+ * Arithmetic: bf16 operands, fp32 accumulation and softmax statistics, the
+ * probabilities P rounded to bf16 before the second GEMM, O rounded to bf16.
+ *
+ * Ownership: every buffer belongs to the caller.  The library allocates no
+ * memory and keeps no per-call state; it caches, per device, only the
+ * architecture check and the kernels' shared-memory attribute.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * rejected call returns a status other than ATTN_OK and touches no memory.
+ * There is no CPU fallback: a device that is not compute capability 10.3
+ * gives ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef void *attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, a size <= 0, H_q % H_kv != 0, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* D not 64 or 128, size beyond the kernel's limits, not sm_103 */
+  ATTN_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  ATTN_ERR_TIMEOUT = 5      /* a kernel wait ran out of time (see attn_device_status) */
+} attn_status_t;
+
+/*
+ * Fused attention forward on device buffers, asynchronous on `stream`.
+ *
+ *   q    [B, H_q, S_q, D]  bf16, device, read
+ *   k    [B, H_kv, S_kv, D] bf16, device, read
+ *   v    [B, H_kv, S_kv, D] bf16, device, read
+ *   o    [B, H_q, S_q, D]  bf16, device, written
+ *   lse  [B, H_q, S_q]     fp32, device, written (natural log)
+ *   D in {64, 128}; H_q a multiple of H_kv; every size >= 1;
+ *   causal 0 or 1; scale finite and >= 0 (the scores are multiplied by it
+ *   before the mask and the softmax; 1/sqrt(D) is the usual choice).
+ *
+ * All pointers must be 16-byte aligned and must not alias o/lse with inputs.
+ * Returns once the kernel is queued; no synchronisation happens inside.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                       float scale, attn_stream_t stream);
+
+/*
+ * The same computation with host inputs and outputs: on `stream`, copies
+ * q/k/v from host memory into the caller's device buffers q_dev/k_dev/v_dev,
+ * runs attn_fwd into o_dev/lse_dev, and copies o/lse back to host memory.
+ * Host buffers should be page-locked for the copies to be asynchronous.
+ * Returns once everything is queued; the host outputs are valid after the
+ * stream is synchronised.  Same argument rules as attn_fwd for the device
+ * buffers; host pointers must be non-null.
+ */
+attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                            void *o_host, float *lse_host, void *q_dev, void *k_dev,
+                            void *v_dev, void *o_dev, float *lse_dev, int B, int H_q, int H_kv,
+                            int S_q, int S_kv, int D, int causal, float scale,
+                            attn_stream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char *attn_status_string(attn_status_t status);
+
+/*
+ * Reads the device-side status word of the current device: ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if a launch since the last reset gave up on a wait (that
+ * launch's outputs are then unspecified).  Synchronises the device.  With
+ * reset != 0 the word is cleared afterwards.
+ */
+attn_status_t attn_device_status(int *status_out, int reset);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

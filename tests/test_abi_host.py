@@ -1,0 +1,101 @@
+"""The C-ABI library: it builds, loads, exports every declared entry point, and
+rejects bad arguments on the host before touching any device (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_pipelining_gb300 as ap
+from attention_pipelining_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ap.build()
+    return ap._load()
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(attn_[a-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_expected_entry_points():
+    names = _declared_functions()
+    assert set(ap.EXPORTS) <= set(names), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_built_for_sm103a_only():
+    assert _build.GENCODE == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = ap.status_string(code)
+        assert isinstance(s, str) and s
+    assert ap.status_string(99) == "unknown status"
+    assert lib.attn_version() >= 100
+
+
+# Fake, never-dereferenced device addresses: validation must reject or accept
+# them without any CUDA call, so these run without a GPU.
+A = 0x10000  # 16-byte aligned
+GOOD = dict(B=1, H_q=4, H_kv=2, S_q=128, S_kv=128, D=128, causal=0, scale=0.125)
+
+
+def _call(lib, q=A, k=A, v=A, o=A, lse=A, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return lib.attn_fwd(q, k, v, o, lse, a["B"], a["H_q"], a["H_kv"], a["S_q"], a["S_kv"], a["D"],
+                        a["causal"], a["scale"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(B=0), 1), (dict(H_q=0), 1), (dict(H_kv=0), 1), (dict(S_q=0), 1), (dict(S_kv=-3), 1),
+    (dict(D=0), 1), (dict(H_q=3, H_kv=2), 1), (dict(causal=2), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-0.5), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2), (dict(B=70000), 2),
+    (dict(q=A + 8), 3), (dict(k=A + 2), 3), (dict(v=A + 4), 3), (dict(o=A + 1), 3), (dict(lse=A + 4), 3),
+])
+def test_validation_rejects_before_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_host_entry_rejects_null_host_buffers(lib):
+    args = [A, A, A, A, A, A, A, A, A, A, 1, 4, 2, 128, 128, 128, 0, ctypes.c_float(0.1), None]
+    for i in range(5):
+        bad = list(args)
+        bad[i] = None
+        assert lib.attn_fwd_host(*bad) == 1
+
+
+def test_selftest_entry_validation(lib):
+    assert lib.attn_selftest_qk(None, A, A, 128, None) == 1
+    assert lib.attn_selftest_qk(A, A, A, 96, None) == 2
+    assert lib.attn_selftest_pv(A, A + 4, A, 64, None) == 3
+
+
+def test_device_status_null(lib):
+    assert lib.attn_device_status(None, 0) == 1
+
+
+def test_binding_raises_without_cuda_tensors():
+    import torch
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        ap.attn_fwd(q, q, q, False, 0.125)

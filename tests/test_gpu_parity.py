@@ -1,0 +1,141 @@
+"""The CUDA path against the fp64 oracle, element by element on small and odd
+shapes, and on sampled rows at the full sizes of the benchmark workloads."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_pipelining_gb300 as ap
+import oracle
+from attention_pipelining_gb300.synthetic import WORKLOADS, make_qkv, make_workload
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ap.build()
+    ap.device_status(reset=True)
+    yield
+    assert ap.device_status(reset=True) == 0, "a kernel wait timed out during the tests"
+
+
+def run_gpu(q, k, v, causal, scale):
+    o, lse = ap.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu()
+
+
+SMALL = [
+    # B, H_q, H_kv, S_q, S_kv, D, causal, k_scale
+    (1, 1, 1, 256, 256, 64, False, 1.0),   # the single-head workload, full size
+    (1, 2, 2, 128, 128, 128, False, 1.0),
+    (1, 2, 2, 128, 128, 128, True, 1.0),
+    (2, 4, 4, 1024, 1024, 128, False, 1.0),
+    (2, 4, 4, 1024, 1024, 128, True, 1.0),
+    (2, 8, 2, 512, 512, 64, True, 3.0),    # grouped heads, K x 3
+    (1, 4, 1, 512, 512, 128, False, 1.0),
+    (3, 2, 1, 130, 130, 128, True, 1.0),
+    (1, 2, 2, 200, 77, 128, True, 1.0),    # S_q > S_kv
+    (1, 2, 2, 200, 77, 128, False, 1.0),
+    (1, 2, 2, 77, 300, 64, True, 1.0),     # S_q < S_kv
+    (1, 2, 2, 77, 300, 64, False, 1.0),
+    (1, 3, 3, 40, 1, 128, False, 1.0),     # a single key
+    (1, 3, 3, 40, 1, 64, True, 1.0),
+]
+ODD_S = [1, 17, 127, 129, 255, 257, 383, 513]
+
+
+def _check(B, Hq, Hkv, Sq, Skv, D, causal, kscale, seed=0):
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, k_scale=kscale, seed=seed)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o64, lse64 = oracle.attn_fwd(q, k, v, causal, scale)
+    return assert_parity(o, lse, o64, lse64, f"{(B, Hq, Hkv, Sq, Skv, D, causal, kscale)}")
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[str(c) for c in SMALL])
+def test_small_shapes(case):
+    _check(*case)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", ODD_S)
+def test_ragged_lengths(S, causal, D):
+    _check(1, 2, 1, S, S, D, causal, 1.0, seed=S)
+
+
+def test_v_ones_gives_ones():
+    q, k, _ = make_qkv(1, 4, 2, 300, 300, 128, seed=3)
+    v = torch.ones((1, 2, 300, 128), dtype=torch.bfloat16)
+    for causal in (False, True):
+        o, _ = run_gpu(q, k, v, causal, 1 / math.sqrt(128))
+        assert np.abs(o.double().numpy() - 1.0).max() <= 1e-2
+
+
+def test_zero_scale_gives_mean_of_v():
+    q, k, v = make_qkv(1, 2, 2, 260, 260, 64, seed=4)
+    for causal in (False, True):
+        o, lse = run_gpu(q, k, v, causal, 0.0)
+        o64, lse64 = oracle.attn_fwd(q, k, v, causal, 0.0)
+        assert_parity(o, lse, o64, lse64, f"scale=0 causal={causal}")
+
+
+def test_deterministic():
+    q, k, v = make_qkv(2, 4, 2, 700, 700, 128, seed=9)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = ap.attn_fwd(q, k, v, True, 0.1)
+    o2, l2 = ap.attn_fwd(q, k, v, True, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_side_stream_and_host_entry():
+    q, k, v = make_qkv(1, 2, 2, 300, 300, 128, seed=5)
+    scale = 1 / math.sqrt(128)
+    o64, lse64 = oracle.attn_fwd(q, k, v, False, scale)
+    s = torch.cuda.Stream()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        o, lse = ap.attn_fwd(qd, kd, vd, False, scale, stream=s)
+    s.synchronize()
+    assert_parity(o, lse, o64, lse64, "side stream")
+    # host buffers in, host buffers out
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((1, 2, 300), dtype=torch.float32).pin_memory()
+    od, ld = torch.empty_like(qd), torch.empty((1, 2, 300), dtype=torch.float32, device="cuda")
+    ap.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, False, scale)
+    torch.cuda.synchronize()
+    assert_parity(oh, lh, o64, lse64, "host entry")
+
+
+def _sample_rows(w, n_heads=6, seed=0):
+    """Flat row indices into [B, H_q, S_q]: tile edges, sequence ends, random rows."""
+    rng = np.random.default_rng(seed)
+    heads = {(0, 0), (w.B - 1, w.H_q - 1)}
+    while len(heads) < min(n_heads, w.B * w.H_q):
+        heads.add((int(rng.integers(w.B)), int(rng.integers(w.H_q))))
+    pos = {0, 1, 127, 128, 255, 256, w.S_q - 1, w.S_q - 2, w.S_q // 2}
+    pos |= set(int(x) for x in rng.integers(0, w.S_q, 24))
+    pos = sorted(p for p in pos if 0 <= p < w.S_q)
+    return np.array([(b * w.H_q + h) * w.S_q + i for (b, h) in sorted(heads) for i in pos], np.int64)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_full_size_sampled_rows(name):
+    """Full-size workloads in the benchmark's launch configuration, checked on
+    sampled rows that the oracle computes one by one."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    rows = _sample_rows(w)
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
+    og = o.reshape(-1, w.D)[torch.from_numpy(rows)]
+    lg = lse.reshape(-1)[torch.from_numpy(rows)]
+    assert_parity(og, lg, o64, lse64, name)
