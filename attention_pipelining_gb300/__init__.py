@@ -32,7 +32,7 @@ STATUS = {
 
 # every entry point of include/attn.h and include/attn_selftest.h
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
-           "attn_version", "attn_selftest_qk", "attn_selftest_pv"]
+           "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace"]
 
 
 class AttnError(RuntimeError):
@@ -72,6 +72,8 @@ def _load():
     lib.attn_selftest_qk.restype = ci
     lib.attn_selftest_pv.argtypes = [vp, vp, vp, ci, vp]
     lib.attn_selftest_pv.restype = ci
+    lib.attn_fwd_trace.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, ci, ci, vp]
+    lib.attn_fwd_trace.restype = ci
     _lib = lib
     return lib
 
@@ -145,6 +147,32 @@ def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
                                  k_dev.data_ptr(), v_dev.data_ptr(), o_dev.data_ptr(),
                                  lse_dev.data_ptr(), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)),
                                  float(scale), _stream_handle(stream)), "attn_fwd_host")
+
+
+TRACE_EVENTS = ["sm0_wake", "sm0_loaded", "sm0_done", "sm1_wake", "sm1_loaded", "sm1_done",
+                "mma_pv0", "mma_s0", "mma_pv1", "mma_s1", "corr0", "corr1", "load_k", "load_v",
+                "epilogue", "end", "mma_pv0_begin", "mma_s0_begin", "mma_pv1_begin", "mma_s1_begin"]
+
+
+def attn_fwd_trace(q, k, v, causal: bool, scale: float, ctas: int = 4, blocks: int | None = None,
+                   stream=None):
+    """Runs the trace instantiation; returns (o, lse, trace) where trace is an
+    int64 CPU tensor [ctas, 16, blocks] of SM clock cycles (0 = no event)."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if blocks is None:
+        blocks = (Skv + 127) // 128
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    tr = torch.zeros((ctas, len(TRACE_EVENTS), blocks), dtype=torch.int64, device=q.device)
+    _check(_load().attn_fwd_trace(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)),
+                                  float(scale), tr.data_ptr(), ctas, blocks,
+                                  _stream_handle(stream)), "attn_fwd_trace")
+    torch.cuda.synchronize(q.device)
+    return o, lse, tr.cpu()
 
 
 def selftest_qk(q, k):

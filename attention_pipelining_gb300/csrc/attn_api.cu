@@ -82,8 +82,8 @@ static attn_status_t validate(const void* q, const void* k, const void* v, const
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  // grid is (H_q, B, ceil(S_q / 256)); y and z are limited to 65535
-  if (B > 65535 || (S_q + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  // grid is (ceil(S_q / 256), H_q, B); y and z are limited to 65535
+  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
   // tensor-map extents must stay below 2^32 per dimension
   if ((int64_t)B * H_q >= (1ll << 31) || (int64_t)B * H_kv >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
@@ -96,11 +96,12 @@ static attn_status_t validate(const void* q, const void* k, const void* v, const
 
 using namespace attnpipe;
 
-extern "C" {
+namespace attnpipe {
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H_q, int H_kv, int S_q, int S_kv, int D, int causal, float scale,
-                       attn_stream_t stream) {
+static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                              float scale, unsigned long long* trace, int trace_ctas,
+                              int trace_blocks, attn_stream_t stream) {
   attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
   st = check_device();
@@ -121,10 +122,34 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.causal = causal;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = kDefaultTimeoutNs;
+  p.trace = trace;
+  p.trace_ctas = trace_ctas;
+  p.trace_blocks = trace_blocks;
   const int n_m_tiles = (S_q + 255) / 256;
   if (launch_attn_fwd(p, D, n_m_tiles, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace attnpipe
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H_q, int H_kv, int S_q, int S_kv, int D, int causal, float scale,
+                       attn_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0,
+                  stream);
+}
+
+attn_status_t attn_fwd_trace(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                             float scale, unsigned long long* trace, int trace_ctas,
+                             int trace_blocks, attn_stream_t stream) {
+  if (!trace || trace_ctas <= 0 || trace_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(trace) & 7u) != 0) return ATTN_ERR_MISALIGNED;
+  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, trace, trace_ctas,
+                  trace_blocks, stream);
 }
 
 attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,

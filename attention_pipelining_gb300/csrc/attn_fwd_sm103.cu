@@ -52,7 +52,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 // Register split across the four warpgroups (setmaxnreg): softmax x2,
 // correction, load/MMA.  The kernel launches with 128 registers per thread
 // (launch bounds 512 x 1), and the split must fit in that pool.
-constexpr int kRegsSoftmax = 168, kRegsCorrection = 88, kRegsLoadMma = 88;
+constexpr int kRegsSoftmax = 160, kRegsCorrection = 88, kRegsLoadMma = 104;
 static_assert((2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma) * 128 <= 65536 &&
                   kRegsCorrection <= 128 && kRegsLoadMma <= 128,
               "setmaxnreg split exceeds the launch register pool");
@@ -101,7 +101,7 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 }  // namespace
 
-template <int D>
+template <int D, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -128,15 +128,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
-  const int m0 = (gridDim.z - 1 - blockIdx.z) * (2 * kBlockM);  // heaviest tiles launch first
+  // grid = (query tiles, H_q, B): the tiles of one head are adjacent in launch
+  // order, so the CTAs resident at once share few heads' K/V in L2; within a
+  // head the longest (causal) tiles launch first.
+  const int m0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBlockM);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
   const int hkv = h / (p.H_q / p.H_kv);
   const int zq = b * p.H_q + h;
   const int zkv = b * p.H_kv + hkv;
   const int kv_end = p.causal ? min(p.S_kv, m0 + 2 * kBlockM) : p.S_kv;
   const int n_blocks = (kv_end + kBlockN - 1) / kBlockN;
   const uint64_t budget = p.timeout_ns;
+  // trace stamps (compiled only into the trace instantiation)
+  const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const bool traced = kTrace && cta_lin < p.trace_ctas;
+  // The stamp is the SM cycle counter; a slot written by several warps keeps
+  // the latest stamp (a barrier completes when its last warp arrives).
+  auto stamp = [&](int ev, int j) {
+    if constexpr (kTrace) {
+      if (traced && j < p.trace_blocks)
+        atomicMax(&p.trace[((size_t)cta_lin * kNumTraceEvents + ev) * p.trace_blocks + j],
+                  (unsigned long long)clock64());
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -180,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int row = m0 + t * kBlockM + r;                  // query row in the sequence
     const int row_first = m0 + t * kBlockM;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const int key_limit = p.causal ? min(p.S_kv, row + 1) : p.S_kv;
     // Two row sums: l_run of the fp32 probabilities (for the LSE), and lp_run
     // of the bf16-rounded probabilities that the PV GEMM actually consumes,
@@ -191,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int j = 0; j < n_blocks; ++j) {
       if (!warp_wait(&s_full[t], j & 1, sAbort, budget)) { ok = false; break; }
       tc_fence_after_sync();
+      if (lane == 0) stamp(t ? kEvSm1Wake : kEvSm0Wake, j);
       uint32_t s[128];
       {
         uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
@@ -207,23 +224,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         reg_after_wait(s2);
         reg_after_wait(s3);
       }
+      if (lane == 0) stamp(t ? kEvSm1Loaded : kEvSm0Loaded, j);
       const int kv0 = j * kBlockN;
       const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > row_first);
       const int lim = key_limit - kv0;  // columns c < lim are visible to this row
-      // row max of the raw scores (8 independent chains)
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
       if (masked) {
+        // keys this row may not see drop out of the max
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], c < lim ? u2f(s[c]) : -INFINITY);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], u2f(s[c]));
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) s[c] = f2u(-INFINITY);
       }
-      const float mblk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m_run, mblk * sl2);
+      // row max of the raw scores (4 independent chains of 3-input max)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
+      }
+      const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      // scale >= 0, so the max of the scaled scores is the scaled max; a row
+      // whose keys are all masked here leaves the running max unchanged
+      const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
       float m_use = m_run;
       float alpha = 1.f;
       if (j == 0) {
@@ -236,32 +257,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         sScale[t * kBlockM + r] = alpha;
         mbar_arrive(&stats[t]);
       }
-      const float neg_m = -m_use;
-      float ls[8], lp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = lp[i] = 0.f;
+      const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+      uint64_t l2[4] = {0, 0, 0, 0};                 // packed fp32 partial sums of p
+      float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = ch * 32 + 2 * i;
-          float p0 = ex2_approx(fmaf(u2f(s[c]), sl2, neg_m));
-          float p1 = ex2_approx(fmaf(u2f(s[c + 1]), sl2, neg_m));
-          if (masked) {
+          // x = s * scale * log2(e) - m, two lanes per instruction
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
+          if (masked) {  // (also covers scale = 0, where -inf * 0 is NaN)
             p0 = (c < lim) ? p0 : 0.f;
             p1 = (c + 1 < lim) ? p1 : 0.f;
           }
-          ls[i & 7] += p0 + p1;
+          l2[i & 3] = f2_add(l2[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
-          lp[i & 7] += u2f(pk[i] << 16) + u2f(pk[i] & 0xffff0000u);
+          add_bf16x2_to_f32(lp[(2 * i) & 7], lp[(2 * i + 1) & 7], pk[i]);
         }
         tmem_st_x16(tS + ch * 16, pk);
       }
-      l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-      lp_run = lp_run * alpha + (((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7])));
+      float la, lb, lc, ld, le, lf, lg, lh;
+      f2_unpack(f2_add(l2[0], l2[1]), la, lb);
+      f2_unpack(f2_add(l2[2], l2[3]), lc, ld);
+      l_run = l_run * alpha + ((la + lb) + (lc + ld));
+      le = (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      lf = (lp[4] + lp[5]) + (lp[6] + lp[7]);
+      (void)lg;
+      (void)lh;
+      lp_run = lp_run * alpha + (le + lf);
       tmem_st_wait();
       tc_fence_before_sync();
+      if (lane == 0) stamp(t ? kEvSm1Done : kEvSm0Done, j);
       mbar_arrive(&p_full[t]);
       m_run = m_use;
     }
@@ -299,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tmem_st_wait();
         }
         tc_fence_before_sync();
+        if (lane == 0) stamp(t ? kEvCorr1 : kEvCorr0, j);
         mbar_arrive(&o_corr[t]);
       }
     }
@@ -306,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!warp_wait(&stats[t], (n_blocks - 1) & 1, sAbort, budget)) { ok = false; break; }
       if (!warp_wait(&pv_done[t], (n_blocks - 1) & 1, sAbort, budget)) { ok = false; break; }
       tc_fence_after_sync();
+      if (lane == 0) stamp(kEvEpilogue, t);
       const float l = sRowSum[t * kBlockM + r];
       const float m = sRowMax[t * kBlockM + r];
       const float inv_l = 1.f / sRowSumP[t * kBlockM + r];
@@ -351,125 +384,109 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     // ------------------------------------------------------------ warpgroup 3
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLoadMma) : "memory");
-    if (warp == 12) {
-      // tensor-core issuer
-      const uint32_t sQ_addr = smem_u32(sQ);
-      const uint32_t sKV_addr = smem_u32(sKV);
-      auto issue_qk = [&](int t, int slot) {
-        issue_qk_gemm<D>(tmem + (t ? C::kTmS1 : C::kTmS0), sQ_addr + t * C::kTileBytes,
-                         sKV_addr + slot * C::kTileBytes);
-      };
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        issue_pv_gemm<D>(tmem + (t ? C::kTmO1 : C::kTmO0), tmem + (t ? C::kTmS1 : C::kTmS0),
-                         sKV_addr + slot * C::kTileBytes, acc);
-      };
+    if (warp == 12 && lane == 0) {
+      // tensor-core issuer: one thread, no warp-wide votes, so it needs as
+      // few issue slots as possible next to the busy softmax warps
+      const uint64_t dq0 = kmajor_tile_desc(smem_u32(sQ));
+      const uint64_t dq1 = kmajor_tile_desc(smem_u32(sQ + C::kTileBytes));
+      const uint64_t dk0 = kmajor_tile_desc(smem_u32(sKV));
+      const uint64_t dv0 = mnmajor_tile_desc<D>(smem_u32(sKV));
+      constexpr uint64_t kStageDesc = C::kTileBytes >> 4;  // start-address step per ring stage
+      const uint32_t tS0 = tmem + C::kTmS0, tS1 = tmem + C::kTmS1;
+      const uint32_t tO0 = tmem + C::kTmO0, tO1 = tmem + C::kTmO1;
       do {
-        if (!warp_wait(&kv_full[0], 0, sAbort, budget)) break;
-        if (!warp_wait(&q_full[0], 0, sAbort, budget)) break;
+        if (!mbar_wait(&kv_full[0], 0, sAbort, budget)) break;
+        if (!mbar_wait(&q_full[0], 0, sAbort, budget)) break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          issue_qk(0, 0);
-          tc_commit(&s_full[0]);
-        }
-        __syncwarp();
-        if (!warp_wait(&q_full[1], 0, sAbort, budget)) break;
+        issue_qk_gemm<D>(tS0, dq0, dk0);
+        tc_commit(&s_full[0]);
+        stamp(kEvMmaS0, 0);
+        if (!mbar_wait(&q_full[1], 0, sAbort, budget)) break;
         tc_fence_after_sync();
-        if (lane == 0) {
-          issue_qk(1, 0);
-          tc_commit(&s_full[1]);
-          tc_commit(&kv_empty[0]);
-        }
-        __syncwarp();
-        bool ok = true;
-        for (int j = 0; j < n_blocks && ok; ++j) {
-          const int iv = 2 * j + 1;
-          const int sv = iv % C::kStages;
-          const int ik = 2 * j + 2;
-          const int sk = ik % C::kStages;
+        issue_qk_gemm<D>(tS1, dq1, dk0);
+        tc_commit(&s_full[1]);
+        tc_commit(&kv_empty[0]);
+        stamp(kEvMmaS1, 0);
+        int sv = 1 % C::kStages, sk = 2 % C::kStages;   // ring stages of V_j and K_{j+1}
+        uint32_t pv_phase = 0, pk_phase = (2 / C::kStages) & 1;
+        for (int j = 0; j < n_blocks; ++j) {
           const bool more = (j + 1) < n_blocks;
-          if (!warp_wait(&kv_full[sv], (iv / C::kStages) & 1, sAbort, budget)) { ok = false; break; }
+          // V_j lives in ring slot 2j+1, K_{j+1} in slot 2j+2
+          const uint32_t v_par = ((2 * j + 1) / C::kStages) & 1;
+          const uint32_t k_par = ((2 * j + 2) / C::kStages) & 1;
+          (void)pv_phase;
+          (void)pk_phase;
+          if (!mbar_wait(&kv_full[sv], v_par, sAbort, budget)) break;
           // sub-tile 0: O_0 += P_0 V_j, then S_0 = Q_0 K_{j+1}^T
-          if (!warp_wait(&p_full[0], j & 1, sAbort, budget)) { ok = false; break; }
-          if (j > 0 && !warp_wait(&o_corr[0], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
+          if (!mbar_wait(&p_full[0], j & 1, sAbort, budget)) break;
+          if (j > 0 && !mbar_wait(&o_corr[0], (j - 1) & 1, sAbort, budget)) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            issue_pv(0, sv, j > 0);
-            tc_commit(&pv_done[0]);
-          }
-          __syncwarp();
+          stamp(kEvMmaPV0Begin, j);
+          const uint64_t dv = dv0 + (uint64_t)sv * kStageDesc;
+          issue_pv_gemm<D>(tO0, tS0, dv, j > 0);
+          tc_commit(&pv_done[0]);
+          stamp(kEvMmaPV0, j);
+          const uint64_t dk = dk0 + (uint64_t)sk * kStageDesc;
           if (more) {
-            if (!warp_wait(&kv_full[sk], (ik / C::kStages) & 1, sAbort, budget)) { ok = false; break; }
+            if (!mbar_wait(&kv_full[sk], k_par, sAbort, budget)) break;
             tc_fence_after_sync();
-            if (lane == 0) {
-              issue_qk(0, sk);
-              tc_commit(&s_full[0]);
-            }
-            __syncwarp();
+            stamp(kEvMmaS0Begin, j + 1);
+            issue_qk_gemm<D>(tS0, dq0, dk);
+            tc_commit(&s_full[0]);
+            stamp(kEvMmaS0, j + 1);
           }
           // sub-tile 1: O_1 += P_1 V_j, then S_1 = Q_1 K_{j+1}^T
-          if (!warp_wait(&p_full[1], j & 1, sAbort, budget)) { ok = false; break; }
-          if (j > 0 && !warp_wait(&o_corr[1], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
+          if (!mbar_wait(&p_full[1], j & 1, sAbort, budget)) break;
+          if (j > 0 && !mbar_wait(&o_corr[1], (j - 1) & 1, sAbort, budget)) break;
           tc_fence_after_sync();
-          if (lane == 0) {
-            issue_pv(1, sv, j > 0);
-            tc_commit(&pv_done[1]);
-            tc_commit(&kv_empty[sv]);
-            if (more) {
-              issue_qk(1, sk);
-              tc_commit(&s_full[1]);
-              tc_commit(&kv_empty[sk]);
-            }
+          stamp(kEvMmaPV1Begin, j);
+          issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
+          tc_commit(&pv_done[1]);
+          tc_commit(&kv_empty[sv]);
+          stamp(kEvMmaPV1, j);
+          if (more) {
+            stamp(kEvMmaS1Begin, j + 1);
+            issue_qk_gemm<D>(tS1, dq1, dk);
+            tc_commit(&s_full[1]);
+            tc_commit(&kv_empty[sk]);
+            stamp(kEvMmaS1, j + 1);
           }
-          __syncwarp();
+          sv = (sv + 2) % C::kStages;
+          sk = (sk + 2) % C::kStages;
         }
       } while (0);
       // let every tensor-core op this thread issued finish before teardown
-      if (lane == 0) {
-        tc_commit(drain);
-        drain_wait(drain, 0, budget);
-      }
-      __syncwarp();
-    } else if (warp == 13) {
-      // TMA producer
+      tc_commit(drain);
+      drain_wait(drain, 0, budget);
+    } else if (warp == 13 && lane == 0) {
+      // TMA producer (one thread)
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      if (lane == 0) {
-        for (int t = 0; t < 2; ++t) {
-          mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
-          tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zq, pol_q);
-        }
+      for (int t = 0; t < 2; ++t) {
+        mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
+        tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zq, pol_q);
       }
-      __syncwarp();
       int issued = 0;
-      bool ok = true;
       for (int idx = 0; idx < 2 * n_blocks; ++idx) {
         const int slot = idx % C::kStages;
         const int round = idx / C::kStages;
-        if (round > 0 && !warp_wait(&kv_empty[slot], (round - 1) & 1, sAbort, budget)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
-          const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
-          tma_load_tile<D>(sKV + slot * C::kTileBytes, map, &kv_full[slot], (idx >> 1) * kBlockN, zkv,
-                           pol_kv);
-        }
-        __syncwarp();
+        if (round > 0 && !mbar_wait(&kv_empty[slot], (round - 1) & 1, sAbort, budget)) break;
+        mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
+        const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
+        tma_load_tile<D>(sKV + slot * C::kTileBytes, map, &kv_full[slot], (idx >> 1) * kBlockN, zkv,
+                         pol_kv);
+        stamp((idx & 1) ? kEvLoadV : kEvLoadK, idx >> 1);
         issued = idx + 1;
       }
-      (void)ok;
-      if (lane == 0) {
-        // every copy this warp issued must land before the CTA exits (on the
-        // normal path these phases completed long ago)
-        drain_wait(&q_full[0], 0, budget);
-        drain_wait(&q_full[1], 0, budget);
-        const int first = issued > C::kStages ? issued - C::kStages : 0;
-        for (int idx = first; idx < issued; ++idx)
-          drain_wait(&kv_full[idx % C::kStages], (idx / C::kStages) & 1, budget);
-      }
-      __syncwarp();
+      // every copy issued must land before the CTA exits (on the normal path
+      // these phases completed long ago)
+      drain_wait(&q_full[0], 0, budget);
+      drain_wait(&q_full[1], 0, budget);
+      const int first = issued > C::kStages ? issued - C::kStages : 0;
+      for (int idx = first; idx < issued; ++idx)
+        drain_wait(&kv_full[idx % C::kStages], (idx / C::kStages) & 1, budget);
     }
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -477,12 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 12) tmem_dealloc(tmem, C::kTmemCols);
+  if (threadIdx.x == 0) stamp(kEvEnd, 0);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_attn_status, 0, (int)ATTN_ERR_TIMEOUT);
 }
 
 namespace {
 
-template <int D>
+template <int D, bool kTrace>
 cudaError_t launch_d(const AttnParams& p, int n_m_tiles, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
@@ -490,21 +508,26 @@ cudaError_t launch_d(const AttnParams& p, int n_m_tiles, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<D>::kSmemBytes);
+    err = cudaFuncSetAttribute(attn_fwd_kernel<D, kTrace>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  dim3 grid(p.H_q, p.B, n_m_tiles);
-  attn_fwd_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  dim3 grid(n_m_tiles, p.H_q, p.B);
+  attn_fwd_kernel<D, kTrace><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream) {
-  if (D == 128) return launch_d<128>(p, n_m_tiles, stream);
-  if (D == 64) return launch_d<64>(p, n_m_tiles, stream);
+  if (p.trace) {
+    if (D == 128) return launch_d<128, true>(p, n_m_tiles, stream);
+    if (D == 64) return launch_d<64, true>(p, n_m_tiles, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (D == 128) return launch_d<128, false>(p, n_m_tiles, stream);
+  if (D == 64) return launch_d<64, false>(p, n_m_tiles, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -20,6 +20,36 @@ struct AttnParams {
   int B, H_q, H_kv, S_q, S_kv, causal;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   unsigned long long timeout_ns;  // budget of any single wait inside the kernel
+  // Timeline trace (the trace instantiation only): globaltimer stamps,
+  // layout [cta][event][block] for CTAs with linear index < trace_ctas.
+  unsigned long long* trace;
+  int trace_ctas;
+  int trace_blocks;
+};
+
+// Events stamped by the trace instantiation, one slot per KV block j.
+enum TraceEvent : int {
+  kEvSm0Wake = 0,   // softmax 0: S_0(j) ready (wait returned)
+  kEvSm0Loaded,     // softmax 0: S_0(j) in registers
+  kEvSm0Done,       // softmax 0: P_0(j) stored, about to signal
+  kEvSm1Wake,
+  kEvSm1Loaded,
+  kEvSm1Done,
+  kEvMmaPV0,        // tensor-core issuer: O_0 += P_0(j) V_j issued
+  kEvMmaS0,         // S_0(j) = Q_0 K_j^T issued
+  kEvMmaPV1,
+  kEvMmaS1,
+  kEvCorr0,         // correction: O_0 ready for block j (j >= 1)
+  kEvCorr1,
+  kEvLoadK,         // producer: K_j load issued
+  kEvLoadV,         // producer: V_j load issued
+  kEvEpilogue,      // correction: epilogue of sub-tile j (j = 0, 1) starts
+  kEvEnd,           // j = 0: CTA teardown
+  kEvMmaPV0Begin,   // tensor-core issuer: waits for PV_0(j) passed, issue begins
+  kEvMmaS0Begin,
+  kEvMmaPV1Begin,
+  kEvMmaS1Begin,
+  kNumTraceEvents
 };
 
 // Encodes a 3-D bf16 tensor map over a contiguous [outer, rows, D] array with
@@ -28,6 +58,7 @@ bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t
                         uint64_t outer, uint32_t box_rows);
 
 // Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(S_q / 256).
+// With p.trace set, the trace instantiation runs instead.
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream);
 
 // Reads (and optionally clears) the device status word of the current device.

@@ -38,39 +38,52 @@ __device__ __forceinline__ void tma_load_tile(uint8_t* dst, const CUtensorMap* m
     tma_load_3d(dst + s * kSlabBytes, map, bar, s * 64, row0, z, hint);
 }
 
-// S[tmem, 128 x 128 fp32] = Q K^T for one 128-row Q tile and one 128-row K
-// tile.  Both operands are K-major (the head dimension is contiguous): per
-// K step of 16 elements the descriptor start advances 32 bytes inside a
-// swizzle row, and moves to the next slab every 64 elements.  Stride between
-// 8-row groups (SBO) is 1024 bytes; the leading offset is unused for
-// swizzled K-major operands.  Issued by one thread.
+// Shared-memory descriptor of the start of a tile, for either operand use.
+// The GEMM helpers below add constant offsets to its start-address field
+// (bits 0-13, address >> 4), which never carries: shared addresses stay
+// below 2^18.
+__device__ __forceinline__ uint64_t kmajor_tile_desc(uint32_t smem_addr) {
+  return make_smem_desc_sw128(smem_addr, 16, 1024);
+}
+
 template <int D>
-__device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ uint64_t mnmajor_tile_desc(uint32_t smem_addr) {
+  // With D = 64 there is a single slab along N and the leading offset is
+  // never used; it is set to the in-slab group stride so no field can point
+  // past the tile.
+  return make_smem_desc_sw128(smem_addr, (D == 64) ? 1024 : kSlabBytes, 1024);
+}
+
+// S[tmem, 128 x 128 fp32] = Q K^T for one 128-row Q tile and one 128-row K
+// tile, given their K-major tile descriptors.  Both operands are K-major (the
+// head dimension is contiguous): per K step of 16 elements the start advances
+// 32 bytes inside a swizzle row, and moves to the next slab every 64
+// elements.  Stride between 8-row groups (SBO) is 1024 bytes; the leading
+// offset is unused for swizzled K-major operands.  Issued by one thread.
+template <int D>
+__device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = make_idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-    mma_ss(s_tmem, make_smem_desc_sw128(q_smem + off, 16, 1024),
-           make_smem_desc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = (uint64_t)(((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4);
+    mma_ss(s_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O[tmem, 128 x D fp32] (+)= P V with P [128 x 128] bf16 in tensor memory
 // (row i in lane i, keys 2c and 2c+1 packed in column c) and V a
-// [128 keys x D] tile used MN-major (D contiguous).  Per K step of 16 keys
-// the descriptor start advances 16 rows = 2048 bytes; the 8-row groups along
-// K are 1024 bytes apart (SBO); the 64-column slabs along N are one slab
-// apart (LBO).  `accumulate` = false overwrites O.  Issued by one thread.
+// [128 keys x D] tile used MN-major (D contiguous), given its MN-major tile
+// descriptor.  Per K step of 16 keys the start advances 16 rows = 2048
+// bytes; the 8-row groups along K are 1024 bytes apart (SBO); the 64-column
+// slabs along N are one slab apart (LBO).  `accumulate` = false overwrites
+// O.  Issued by one thread.
 template <int D>
-__device__ __forceinline__ void issue_pv_gemm(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv_gemm(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               bool accumulate) {
   constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
-  // With D = 64 there is a single slab along N and the leading offset is never
-  // used; it is set to the in-slab group stride so no field can point past the tile.
-  constexpr uint32_t lbo = (D == 64) ? 1024 : kSlabBytes;
 #pragma unroll
   for (int kk = 0; kk < kTileRows / 16; ++kk) {
-    mma_ts(o_tmem, p_tmem + kk * 8, make_smem_desc_sw128(v_smem + kk * 2048, lbo, 1024), idesc,
+    mma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)((kk * 2048) >> 4), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }

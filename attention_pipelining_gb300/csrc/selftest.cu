@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(128, 1)
     tma_load_tile<D>(sK, &tk, &ctl->full, 0, 0, l2_policy_evict_first());
     if (mbar_wait(&ctl->full, 0, abort_flag, kSelftestBudgetNs)) {
       tc_fence_after_sync();
-      issue_qk_gemm<D>(tmem, smem_u32(sQ), smem_u32(sK));
+      issue_qk_gemm<D>(tmem, kmajor_tile_desc(smem_u32(sQ)), kmajor_tile_desc(smem_u32(sK)));
     }
     tc_commit(&ctl->mma_done);
   }
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(128, 1)
   if (threadIdx.x == 0) {
     if (mbar_wait(&ctl->full, 0, abort_flag, kSelftestBudgetNs)) {
       tc_fence_after_sync();
-      issue_pv_gemm<D>(tmem + 128, tmem, smem_u32(sV), false);
+      issue_pv_gemm<D>(tmem + 128, tmem, mnmajor_tile_desc<D>(smem_u32(sV)), false);
     }
     tc_commit(&ctl->mma_done);
   }

@@ -390,6 +390,26 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_trace(args, w):
+    """Timeline of the first CTAs from the trace instantiation (not a bench line)."""
+    import torch
+    import attention_pipelining_gb300 as ap
+    from attention_pipelining_gb300 import trace as tr
+    from attention_pipelining_gb300.synthetic import make_workload
+    ap.build()
+    q, k, v = (t.cuda() for t in make_workload(w))
+    for _ in range(args.warmup):
+        ap.attn_fwd(q, k, v, w.causal, w.scale)
+    torch.cuda.synchronize()
+    n_blocks = (w.S_kv + 127) // 128
+    _, _, t = ap.attn_fwd_trace(q, k, v, w.causal, w.scale, ctas=args.trace, blocks=n_blocks)
+    out = {"workload": w.name, "traced_ctas": args.trace, **tr.summarize(t.numpy(), n_blocks)}
+    if args.trace_out:
+        import numpy as np
+        np.save(args.trace_out, t.numpy())
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     from attention_pipelining_gb300.synthetic import HEADLINE, WORKLOADS
     ap_ = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -401,10 +421,16 @@ def main(argv=None):
     ap_.add_argument("--e2e-steps", type=int, default=50)
     ap_.add_argument("--cpu-seconds", type=float, default=12.0)
     ap_.add_argument("--no-cpu-baseline", action="store_true")
+    ap_.add_argument("--trace", type=int, default=0,
+                     help="print a timeline summary of the first N CTAs instead of a bench line")
+    ap_.add_argument("--trace-out", default="", help="also save the raw trace (.npy)")
     args = ap_.parse_args(argv)
     if args.warmup < 3:
         ap_.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.trace > 0:
+        run_trace(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

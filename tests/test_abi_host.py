@@ -90,6 +90,14 @@ def test_selftest_entry_validation(lib):
     assert lib.attn_selftest_pv(A, A + 4, A, 64, None) == 3
 
 
+def test_trace_entry_validation(lib):
+    base = [A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, ctypes.c_float(0.1)]
+    assert lib.attn_fwd_trace(*base, None, 1, 1, None) == 1
+    assert lib.attn_fwd_trace(*base, A, 0, 1, None) == 1
+    assert lib.attn_fwd_trace(*base, A, 1, 0, None) == 1
+    assert lib.attn_fwd_trace(*base, A + 4, 1, 1, None) == 3
+
+
 def test_device_status_null(lib):
     assert lib.attn_device_status(None, 0) == 1
 

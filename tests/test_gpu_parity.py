@@ -139,3 +139,20 @@ def test_full_size_sampled_rows(name):
     og = o.reshape(-1, w.D)[torch.from_numpy(rows)]
     lg = lse.reshape(-1)[torch.from_numpy(rows)]
     assert_parity(og, lg, o64, lse64, name)
+
+
+def test_trace_instantiation_matches_and_stamps():
+    """The trace instantiation computes the same result and stamps every role."""
+    q, k, v = make_qkv(1, 2, 2, 600, 600, 128, seed=8)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ap.attn_fwd(qd, kd, vd, False, 0.09)
+    o2, lse2, tr = ap.attn_fwd_trace(qd, kd, vd, False, 0.09, ctas=2)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    n = (600 + 127) // 128
+    t = tr.numpy()
+    for ev in ("sm0_wake", "sm0_done", "sm1_wake", "sm1_done", "mma_pv0", "mma_pv1",
+               "mma_s0", "mma_s1", "load_k", "load_v"):
+        e = ap.TRACE_EVENTS.index(ev)
+        assert (t[:, e, :n] > 0).all(), ev
+    sm0w, sm0d = t[:, 0, :n], t[:, 2, :n]
+    assert (sm0d >= sm0w).all() and (np.diff(sm0w, axis=1) > 0).all()
