@@ -33,6 +33,7 @@
 // records ATTN_ERR_TIMEOUT.  No trap, no assert.
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "attn_tiles.cuh"
@@ -228,68 +229,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const int kv0 = j * kBlockN;
       const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > row_first);
       const int lim = key_limit - kv0;  // columns c < lim are visible to this row
-      if (masked) {
-        // keys this row may not see drop out of the max
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) s[c] = f2u(-INFINITY);
-      }
-      // row max of the raw scores (4 independent chains of 3-input max)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
-      }
-      const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      // scale >= 0, so the max of the scaled scores is the scaled max; a row
-      // whose keys are all masked here leaves the running max unchanged
-      const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
       float m_use = m_run;
       float alpha = 1.f;
-      if (j == 0) {
-        m_use = m_new;
-      } else if (m_new - m_run > kRescaleThreshold) {
-        m_use = m_new;
-        alpha = ex2_approx(m_run - m_new);
-      }
-      if (j > 0) {
-        sScale[t * kBlockM + r] = alpha;
-        mbar_arrive(&stats[t]);
-      }
-      const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
-      uint64_t l2[4] = {0, 0, 0, 0};                 // packed fp32 partial sums of p
-      float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint64_t l2[2] = {0, 0};                  // packed fp32 partial sums of p
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};       // partial sums of bf16(p)
+      // The unmasked and masked bodies are separate code paths so the common
+      // (unmasked) one carries no per-element predication.
+      auto body = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
+        if constexpr (kMasked) {
+          // keys this row may not see drop out of the max
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = ch * 32 + 2 * i;
-          // x = s * scale * log2(e) - m, two lanes per instruction
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (masked) {  // (also covers scale = 0, where -inf * 0 is NaN)
-            p0 = (c < lim) ? p0 : 0.f;
-            p1 = (c + 1 < lim) ? p1 : 0.f;
-          }
-          l2[i & 3] = f2_add(l2[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
-          add_bf16x2_to_f32(lp[(2 * i) & 7], lp[(2 * i + 1) & 7], pk[i]);
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = f2u(-INFINITY);
         }
-        tmem_st_x16(tS + ch * 16, pk);
-      }
-      float la, lb, lc, ld, le, lf, lg, lh;
+        // row max of the raw scores (4 independent chains of 3-input max)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
+        }
+        const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // scale >= 0, so the max of the scaled scores is the scaled max; a row
+        // whose keys are all masked here leaves the running max unchanged
+        const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
+        if (j == 0) {
+          m_use = m_new;
+        } else if (m_new - m_run > kRescaleThreshold) {
+          m_use = m_new;
+          alpha = ex2_approx(m_run - m_new);
+        }
+        if (j > 0) {
+          sScale[t * kBlockM + r] = alpha;
+          mbar_arrive(&stats[t]);
+        }
+        const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = ch * 16 + 2 * i;
+            // x = s * scale * log2(e) - m, two lanes per instruction
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if constexpr (kMasked) {  // (also covers scale = 0, where -inf * 0 is NaN)
+              p0 = (c < lim) ? p0 : 0.f;
+              p1 = (c + 1 < lim) ? p1 : 0.f;
+            }
+            l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+            add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);
+          }
+          tmem_st_x8(tS + ch * 8, pk);
+        }
+      };
+      if (masked)
+        body(std::true_type{});
+      else
+        body(std::false_type{});
+      float la, lb;
       f2_unpack(f2_add(l2[0], l2[1]), la, lb);
-      f2_unpack(f2_add(l2[2], l2[3]), lc, ld);
-      l_run = l_run * alpha + ((la + lb) + (lc + ld));
-      le = (lp[0] + lp[1]) + (lp[2] + lp[3]);
-      lf = (lp[4] + lp[5]) + (lp[6] + lp[7]);
-      (void)lg;
-      (void)lh;
-      lp_run = lp_run * alpha + (le + lf);
+      l_run = l_run * alpha + (la + lb);
+      lp_run = lp_run * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
       tmem_st_wait();
       tc_fence_before_sync();
       if (lane == 0) stamp(t ? kEvSm1Done : kEvSm0Done, j);
