@@ -112,31 +112,36 @@ class ClockSampler:
             self.proc.kill()
         self.out.flush()
         self.out.seek(0)
-        rows = [l.strip().split(",") for l in self.out.read().splitlines() if l.strip()]
+        lines = self.out.read().splitlines()
         self.out.close()
         os.unlink(self.out.name)
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
-            except ValueError:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {
-            "sm_mhz": statistics.median(sm) if sm else None,
-            "sm_max_mhz": max(smax) if smax else None,
-            "power_w_max": max(power) if power else None,
-            "samples": len(sm),
-            "reasons": sorted(reasons),
-        }
+        return parse_clock_rows(lines)
+
+
+def parse_clock_rows(lines) -> dict:
+    """Summary of nvidia-smi CSV rows (noheader, nounits) of ClockSampler.QUERY."""
+    sm, smax, reasons, power = [], [], set(), []
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        r = [x.strip() for x in line.split(",")]
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    return {
+        "sm_mhz": statistics.median(sm) if sm else None,
+        "sm_max_mhz": max(smax) if smax else None,
+        "power_w_max": max(power) if power else None,
+        "samples": len(sm),
+        "reasons": sorted(reasons),
+    }
 
 
 def dist_env():
