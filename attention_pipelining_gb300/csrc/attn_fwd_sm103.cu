@@ -69,8 +69,8 @@ struct Cfg {
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   // kv_full[S], kv_empty[S], q_full[2], s_full[2], p_full[2], stats[2],
-  // o_corr[2], pv_done[2], drain[1]
-  static constexpr int kNumBars = 2 * kStages + 13;
+  // pv_done[2], drain[1]
+  static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffScale = kOffBar + kNumBars * 8;   // float [2][128]
   static constexpr int kOffRowSum = kOffScale + 2 * 128 * 4;  // float [2][128], fp32 sum of p
   static constexpr int kOffRowSumP = kOffRowSum + 2 * 128 * 4; // float [2][128], sum of bf16(p)
@@ -117,9 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* s_full = q_full + 2;
   uint64_t* p_full = q_full + 4;
   uint64_t* stats = q_full + 6;
-  uint64_t* o_corr = q_full + 8;
-  uint64_t* pv_done = q_full + 10;
-  uint64_t* drain = q_full + 12;
+  uint64_t* pv_done = q_full + 8;
+  uint64_t* drain = q_full + 10;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
   float* sRowSum = reinterpret_cast<float*>(smem + C::kOffRowSum);
   float* sRowSumP = reinterpret_cast<float*>(smem + C::kOffRowSumP);
@@ -162,9 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int t = 0; t < 2; ++t) {
       mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kBlockM);
+      // p_full[t]: P_t(j) stored by the softmax (128 arrivals) and O_t
+      // rescaled for block j by the correction warpgroup (128 arrivals)
+      mbar_init(&p_full[t], 2 * kBlockM);
       mbar_init(&stats[t], kBlockM);
-      mbar_init(&o_corr[t], kBlockM);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -314,11 +314,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int r = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     bool ok = true;
+    // Block 0 needs no rescale.  For block j >= 1 the softmax's alpha arrives
+    // on stats[t]; it is published after the softmax saw S_t(j), whose commit
+    // follows PV_t(j-1), so O_t already holds every earlier block.
+    mbar_arrive(&p_full[0]);
+    mbar_arrive(&p_full[1]);
     for (int j = 1; j < n_blocks && ok; ++j) {
       for (int t = 0; t < 2; ++t) {
         if (!warp_wait(&stats[t], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
         const float alpha = sScale[t * kBlockM + r];
-        if (!warp_wait(&pv_done[t], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
         tc_fence_after_sync();
         if (__any_sync(kFull, alpha != 1.f)) {
           const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
@@ -336,12 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         tc_fence_before_sync();
         if (lane == 0) stamp(t ? kEvCorr1 : kEvCorr0, j);
-        mbar_arrive(&o_corr[t]);
+        mbar_arrive(&p_full[t]);
       }
     }
     for (int t = 0; t < 2 && ok; ++t) {
       if (!warp_wait(&stats[t], (n_blocks - 1) & 1, sAbort, budget)) { ok = false; break; }
-      if (!warp_wait(&pv_done[t], (n_blocks - 1) & 1, sAbort, budget)) { ok = false; break; }
+      if (!warp_wait(&pv_done[t], 0, sAbort, budget)) { ok = false; break; }
       tc_fence_after_sync();
       if (lane == 0) stamp(kEvEpilogue, t);
       const float l = sRowSum[t * kBlockM + r];
@@ -424,12 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!mbar_wait(&kv_full[sv], v_par, sAbort, budget)) break;
           // sub-tile 0: O_0 += P_0 V_j, then S_0 = Q_0 K_{j+1}^T
           if (!mbar_wait(&p_full[0], j & 1, sAbort, budget)) break;
-          if (j > 0 && !mbar_wait(&o_corr[0], (j - 1) & 1, sAbort, budget)) break;
           tc_fence_after_sync();
           stamp(kEvMmaPV0Begin, j);
           const uint64_t dv = dv0 + (uint64_t)sv * kStageDesc;
           issue_pv_gemm<D>(tO0, tS0, dv, j > 0);
-          tc_commit(&pv_done[0]);
+          if (!more) tc_commit(&pv_done[0]);  // the epilogue waits for the last PV only
           stamp(kEvMmaPV0, j);
           const uint64_t dk = dk0 + (uint64_t)sk * kStageDesc;
           if (more) {
@@ -442,11 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           // sub-tile 1: O_1 += P_1 V_j, then S_1 = Q_1 K_{j+1}^T
           if (!mbar_wait(&p_full[1], j & 1, sAbort, budget)) break;
-          if (j > 0 && !mbar_wait(&o_corr[1], (j - 1) & 1, sAbort, budget)) break;
           tc_fence_after_sync();
           stamp(kEvMmaPV1Begin, j);
           issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
-          tc_commit(&pv_done[1]);
+          if (!more) tc_commit(&pv_done[1]);
           tc_commit(&kv_empty[sv]);
           stamp(kEvMmaPV1, j);
           if (more) {
