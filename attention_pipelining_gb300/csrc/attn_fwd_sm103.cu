@@ -69,8 +69,8 @@ struct Cfg {
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   // kv_full[S], kv_empty[S], q_full[2], s_full[2], p_full[2], stats[2],
-  // pv_done[2], drain[1]
-  static constexpr int kNumBars = 2 * kStages + 11;
+  // pv_done[2], drain[1], fin[2]
+  static constexpr int kNumBars = 2 * kStages + 13;
   static constexpr int kOffScale = kOffBar + kNumBars * 8;   // float [2][128]
   static constexpr int kOffRowSum = kOffScale + 2 * 128 * 4;  // float [2][128], fp32 sum of p
   static constexpr int kOffRowSumP = kOffRowSum + 2 * 128 * 4; // float [2][128], sum of bf16(p)
@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* stats = q_full + 6;
   uint64_t* pv_done = q_full + 8;
   uint64_t* drain = q_full + 10;
+  uint64_t* fin = q_full + 11;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
   float* sRowSum = reinterpret_cast<float*>(smem + C::kOffRowSum);
   float* sRowSumP = reinterpret_cast<float*>(smem + C::kOffRowSumP);
@@ -164,7 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // p_full[t]: P_t(j) stored by the softmax (128 arrivals) and O_t
       // rescaled for block j by the correction warpgroup (128 arrivals)
       mbar_init(&p_full[t], 2 * kBlockM);
+      // stats[t]: one phase per block j >= 1 (the rescale factor alpha);
+      // fin[t]: one phase, the final row sums and max.  Keeping them apart
+      // means a waiter is never two phases behind on either barrier.
       mbar_init(&stats[t], kBlockM);
+      mbar_init(&fin[t], kBlockM);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       sRowSum[t * kBlockM + r] = l_run;
       sRowSumP[t * kBlockM + r] = lp_run;
       sRowMax[t * kBlockM + r] = m_run;
-      mbar_arrive(&stats[t]);
+      mbar_arrive(&fin[t]);
     }
   } else if (wg == 2) {
     // ------------------------------------------------------------ correction + epilogue
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
     }
     for (int t = 0; t < 2 && ok; ++t) {
-      if (!warp_wait(&stats[t], (n_blocks - 1) & 1, sAbort, budget)) { ok = false; break; }
+      if (!warp_wait(&fin[t], 0, sAbort, budget)) { ok = false; break; }
       if (!warp_wait(&pv_done[t], 0, sAbort, budget)) { ok = false; break; }
       tc_fence_after_sync();
       if (lane == 0) stamp(kEvEpilogue, t);
