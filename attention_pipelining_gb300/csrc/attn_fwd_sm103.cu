@@ -422,27 +422,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_commit(&kv_empty[0]);
         stamp(kEvMmaS1, 0);
         int sv = 1 % C::kStages, sk = 2 % C::kStages;   // ring stages of V_j and K_{j+1}
-        uint32_t pv_phase = 0, pk_phase = (2 / C::kStages) & 1;
         for (int j = 0; j < n_blocks; ++j) {
           const bool more = (j + 1) < n_blocks;
-          // V_j lives in ring slot 2j+1, K_{j+1} in slot 2j+2
+          // V_j lives in ring slot 2j+1, K_{j+1} in slot 2j+2.  Both loads were
+          // issued long before; waiting for them here, while the softmax is
+          // still busy, keeps them off the path from "P ready" to the GEMMs.
           const uint32_t v_par = ((2 * j + 1) / C::kStages) & 1;
           const uint32_t k_par = ((2 * j + 2) / C::kStages) & 1;
-          (void)pv_phase;
-          (void)pk_phase;
           if (!mbar_wait(&kv_full[sv], v_par, sAbort, budget)) break;
+          if (more && !mbar_wait(&kv_full[sk], k_par, sAbort, budget)) break;
+          const uint64_t dv = dv0 + (uint64_t)sv * kStageDesc;
+          const uint64_t dk = dk0 + (uint64_t)sk * kStageDesc;
           // sub-tile 0: O_0 += P_0 V_j, then S_0 = Q_0 K_{j+1}^T
           if (!mbar_wait(&p_full[0], j & 1, sAbort, budget)) break;
           tc_fence_after_sync();
           stamp(kEvMmaPV0Begin, j);
-          const uint64_t dv = dv0 + (uint64_t)sv * kStageDesc;
           issue_pv_gemm<D>(tO0, tS0, dv, j > 0);
           if (!more) tc_commit(&pv_done[0]);  // the epilogue waits for the last PV only
           stamp(kEvMmaPV0, j);
-          const uint64_t dk = dk0 + (uint64_t)sk * kStageDesc;
           if (more) {
-            if (!mbar_wait(&kv_full[sk], k_par, sAbort, budget)) break;
-            tc_fence_after_sync();
             stamp(kEvMmaS0Begin, j + 1);
             issue_qk_gemm<D>(tS0, dq0, dk);
             tc_commit(&s_full[0]);
@@ -454,15 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           stamp(kEvMmaPV1Begin, j);
           issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
           if (!more) tc_commit(&pv_done[1]);
-          tc_commit(&kv_empty[sv]);
           stamp(kEvMmaPV1, j);
           if (more) {
             stamp(kEvMmaS1Begin, j + 1);
             issue_qk_gemm<D>(tS1, dq1, dk);
             tc_commit(&s_full[1]);
-            tc_commit(&kv_empty[sk]);
             stamp(kEvMmaS1, j + 1);
           }
+          // release the ring slots last: off the critical path
+          tc_commit(&kv_empty[sv]);
+          if (more) tc_commit(&kv_empty[sk]);
           sv = (sv + 2) % C::kStages;
           sk = (sk + 2) % C::kStages;
         }
