@@ -32,7 +32,8 @@ STATUS = {
 
 # every entry point of include/attn.h and include/attn_selftest.h
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
-           "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace"]
+           "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
+           "attn_fwd_timeout_test"]
 
 
 class AttnError(RuntimeError):
@@ -74,6 +75,9 @@ def _load():
     lib.attn_selftest_pv.restype = ci
     lib.attn_fwd_trace.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, ci, ci, vp]
     lib.attn_fwd_trace.restype = ci
+    lib.attn_fwd_timeout_test.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                                          ctypes.c_ulonglong, vp]
+    lib.attn_fwd_timeout_test.restype = ci
     _lib = lib
     return lib
 
@@ -173,6 +177,24 @@ def attn_fwd_trace(q, k, v, causal: bool, scale: float, ctas: int = 4, blocks: i
                                   _stream_handle(stream)), "attn_fwd_trace")
     torch.cuda.synchronize(q.device)
     return o, lse, tr.cpu()
+
+
+def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,
+                     wait_budget_ns: int = 20_000_000, stream=None):
+    """Test hook: runs the forward with one P-ready signal withheld at KV block
+    ``drop_block`` so the kernel's bounded wait runs out (see attn_testing.h).
+    Returns (o, lse); the device status word then reads ATTN_ERR_TIMEOUT."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(_load().attn_fwd_timeout_test(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)),
+                                         float(scale), int(drop_block), int(wait_budget_ns),
+                                         _stream_handle(stream)), "attn_fwd_timeout_test")
+    return o, lse
 
 
 def selftest_qk(q, k):

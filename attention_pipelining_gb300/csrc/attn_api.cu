@@ -101,7 +101,8 @@ namespace attnpipe {
 static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
                               float scale, unsigned long long* trace, int trace_ctas,
-                              int trace_blocks, attn_stream_t stream) {
+                              int trace_blocks, int fault_drop_block,
+                              unsigned long long timeout_ns, attn_stream_t stream) {
   attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
   st = check_device();
@@ -121,10 +122,11 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.S_kv = S_kv;
   p.causal = causal;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  p.timeout_ns = kDefaultTimeoutNs;
+  p.timeout_ns = timeout_ns;
   p.trace = trace;
   p.trace_ctas = trace_ctas;
   p.trace_blocks = trace_blocks;
+  p.fault_drop_block = fault_drop_block;
   const int n_m_tiles = (S_q + 255) / 256;
   if (launch_attn_fwd(p, D, n_m_tiles, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -138,8 +140,8 @@ extern "C" {
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H_q, int H_kv, int S_q, int S_kv, int D, int causal, float scale,
                        attn_stream_t stream) {
-  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0,
-                  stream);
+  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0, -1,
+                  kDefaultTimeoutNs, stream);
 }
 
 attn_status_t attn_fwd_trace(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -149,7 +151,18 @@ attn_status_t attn_fwd_trace(const void* q, const void* k, const void* v, void* 
   if (!trace || trace_ctas <= 0 || trace_blocks <= 0) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(trace) & 7u) != 0) return ATTN_ERR_MISALIGNED;
   return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, trace, trace_ctas,
-                  trace_blocks, stream);
+                  trace_blocks, -1, kDefaultTimeoutNs, stream);
+}
+
+attn_status_t attn_fwd_timeout_test(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H_q, int H_kv, int S_q, int S_kv,
+                                    int D, int causal, float scale, int drop_block,
+                                    unsigned long long wait_budget_ns, attn_stream_t stream) {
+  if (drop_block < 0) return ATTN_ERR_INVALID_ARG;
+  if (wait_budget_ns < 1000000ull || wait_budget_ns > kDefaultTimeoutNs)
+    return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0,
+                  drop_block, wait_budget_ns, stream);
 }
 
 attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,

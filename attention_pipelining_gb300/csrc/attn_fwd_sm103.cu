@@ -303,7 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tmem_st_wait();
       tc_fence_before_sync();
       if (lane == 0) stamp(t ? kEvSm1Done : kEvSm0Done, j);
-      mbar_arrive(&p_full[t]);
+      bool signal = true;
+      if constexpr (kTrace) signal = !(t == 0 && j == p.fault_drop_block);
+      if (signal) mbar_arrive(&p_full[t]);
       m_run = m_use;
     }
     if (ok) {
@@ -532,7 +534,7 @@ cudaError_t launch_d(const AttnParams& p, int n_m_tiles, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream) {
-  if (p.trace) {
+  if (p.trace || p.fault_drop_block >= 0) {
     if (D == 128) return launch_d<128, true>(p, n_m_tiles, stream);
     if (D == 64) return launch_d<64, true>(p, n_m_tiles, stream);
     return cudaErrorInvalidValue;

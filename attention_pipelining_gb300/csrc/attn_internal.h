@@ -25,6 +25,10 @@ struct AttnParams {
   unsigned long long* trace;
   int trace_ctas;
   int trace_blocks;
+  // Test of the timeout path (diagnostic instantiation only): when >= 0, the
+  // first softmax warpgroup does not signal "P ready" for this KV block, so
+  // the tensor-core issuer's bounded wait runs out.  -1 in normal use.
+  int fault_drop_block;
 };
 
 // Events stamped by the trace instantiation, one slot per KV block j.
@@ -58,7 +62,8 @@ bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t
                         uint64_t outer, uint32_t box_rows);
 
 // Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(S_q / 256).
-// With p.trace set, the trace instantiation runs instead.
+// With p.trace set or p.fault_drop_block >= 0, the diagnostic instantiation
+// (timeline stamps, timeout test) runs instead.
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream);
 
 // Reads (and optionally clears) the device status word of the current device.

@@ -98,6 +98,15 @@ def test_trace_entry_validation(lib):
     assert lib.attn_fwd_trace(*base, A + 4, 1, 1, None) == 3
 
 
+def test_timeout_test_entry_validation(lib):
+    base = [A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, ctypes.c_float(0.1)]
+    assert lib.attn_fwd_timeout_test(*base, -1, 20_000_000, None) == 1     # no block to drop
+    assert lib.attn_fwd_timeout_test(*base, 1, 10, None) == 1              # budget too short
+    assert lib.attn_fwd_timeout_test(*base, 1, 10**10, None) == 1          # budget too long
+    bad = [A, A, A, A, A, 1, 2, 2, 128, 128, 96, 0, ctypes.c_float(0.1)]
+    assert lib.attn_fwd_timeout_test(*bad, 1, 20_000_000, None) == 2
+
+
 def test_device_status_null(lib):
     assert lib.attn_device_status(None, 0) == 1
 

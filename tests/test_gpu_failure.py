@@ -1,0 +1,51 @@
+"""Failure detection on the GPU without a fault: a kernel wait is made to run
+out (one "P ready" signal is withheld, nothing else sets it) with a short wait
+budget; the kernel must return, the device status word must read
+ATTN_ERR_TIMEOUT, and the same CUDA context must keep working."""
+import math
+
+import pytest
+import torch
+
+import attention_pipelining_gb300 as ap
+import oracle
+from attention_pipelining_gb300.synthetic import make_qkv
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ap.build()
+    ap.device_status(reset=True)
+    yield
+    ap.device_status(reset=True)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_wait_runs_out_and_context_survives(D):
+    q, k, v = make_qkv(1, 2, 2, 512, 512, D, seed=21)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    assert ap.device_status(reset=True) == 0
+    ap.fwd_timeout_test(qd, kd, vd, False, scale, drop_block=1, wait_budget_ns=20_000_000)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 5        # ATTN_ERR_TIMEOUT
+    # the context is intact: a normal call right after is correct and clean
+    o, lse = ap.attn_fwd(qd, kd, vd, False, scale)
+    torch.cuda.synchronize()
+    o64, lse64 = oracle.attn_fwd(q, k, v, False, scale)
+    assert_parity(o.cpu(), lse.cpu(), o64, lse64, f"after timeout D={D}")
+    assert ap.device_status(reset=True) == 0
+
+
+def test_withheld_signal_beyond_last_block_is_harmless():
+    """A drop block past the end of every CTA's KV loop changes nothing."""
+    q, k, v = make_qkv(1, 2, 1, 300, 300, 128, seed=22)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = ap.fwd_timeout_test(q.cuda(), k.cuda(), v.cuda(), True, scale, drop_block=50)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    o64, lse64 = oracle.attn_fwd(q, k, v, True, scale)
+    assert_parity(o.cpu(), lse.cpu(), o64, lse64, "drop beyond end")
