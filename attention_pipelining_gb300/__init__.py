@@ -33,7 +33,8 @@ STATUS = {
 # every entry point of include/attn.h and include/attn_selftest.h
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
            "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
-           "attn_fwd_timeout_test"]
+           "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
+           "attn_splitkv_default_splits"]
 
 
 class AttnError(RuntimeError):
@@ -78,6 +79,13 @@ def _load():
     lib.attn_fwd_timeout_test.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                           ctypes.c_ulonglong, vp]
     lib.attn_fwd_timeout_test.restype = ci
+    lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                     ci, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+    lib.attn_fwd_splitkv.restype = ci
+    lib.attn_splitkv_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+    lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_splitkv_default_splits.argtypes = [ci, ci, ci, ci, ci, ci]
+    lib.attn_splitkv_default_splits.restype = ci
     _lib = lib
     return lib
 
@@ -177,6 +185,33 @@ def attn_fwd_trace(q, k, v, causal: bool, scale: float, ctas: int = 4, blocks: i
                                   _stream_handle(stream)), "attn_fwd_trace")
     torch.cuda.synchronize(q.device)
     return o, lse, tr.cpu()
+
+
+def splitkv_default_splits(B, H_q, H_kv, S_q, S_kv, causal) -> int:
+    return int(_load().attn_splitkv_default_splits(B, H_q, H_kv, S_q, S_kv, int(bool(causal))))
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int = 0, workspace=None,
+                     stream=None):
+    """Split-KV forward; returns (o, lse).  ``workspace``: optional uint8 CUDA
+    tensor of at least attn_splitkv_workspace_bytes bytes (allocated if None)."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    splits = num_splits if num_splits > 0 else splitkv_default_splits(B, Hq, Hkv, Sq, Skv, causal)
+    nbytes = int(_load().attn_splitkv_workspace_bytes(B, Hq, Sq, D, splits))
+    if nbytes == 0:
+        raise AttnError(1, "attn_splitkv_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(_load().attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                    B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+                                    int(splits), _stream_handle(stream)), "attn_fwd_splitkv")
+    return o, lse
 
 
 def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,

@@ -82,8 +82,10 @@ static attn_status_t validate(const void* q, const void* k, const void* v, const
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  // grid is (ceil(S_q / 256), H_q, B); y and z are limited to 65535
-  if (B > 65535 || H_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  // grid is (ceil(R / 256) x splits, H_kv, B) with R = (H_q / H_kv) * S_q
+  // rows per K/V head; y and z are limited to 65535, R must fit an int
+  if (B > 65535 || H_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)(H_q / H_kv) * S_q >= (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   // tensor-map extents must stay below 2^32 per dimension
   if ((int64_t)B * H_q >= (1ll << 31) || (int64_t)B * H_kv >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
@@ -98,6 +100,36 @@ using namespace attnpipe;
 
 namespace attnpipe {
 
+// Fills the kernel parameters (tensor maps over the row-group view).
+static attn_status_t make_params(AttnParams* p, const void* q, const void* k, const void* v,
+                                 void* o, float* lse, int B, int H_q, int H_kv, int S_q, int S_kv,
+                                 int D, int causal, float scale) {
+  std::memset(p, 0, sizeof(*p));
+  const int R = (H_q / H_kv) * S_q;
+  if (!encode_bf16_map_3d(&p->tm_q, q, D, R, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p->tm_k, k, D, S_kv, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p->tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p->tm_o, o, D, R, (uint64_t)B * H_kv, 32))
+    return ATTN_ERR_CUDA;
+  p->lse = lse;
+  p->B = B;
+  p->H_q = H_q;
+  p->H_kv = H_kv;
+  p->S_q = S_q;
+  p->S_kv = S_kv;
+  p->causal = causal;
+  p->rows_per_group = R;
+  p->total_rows = (long long)B * H_q * S_q;
+  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p->timeout_ns = kDefaultTimeoutNs;
+  p->kv_splits = 1;
+  p->kv_blocks_per_split = 1 << 30;
+  p->fault_drop_block = -1;
+  return ATTN_OK;
+}
+
+static int n_m_tiles_of(int H_q, int H_kv, int S_q) { return ((H_q / H_kv) * S_q + 255) / 256; }
+
 static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
                               float scale, unsigned long long* trace, int trace_ctas,
@@ -108,27 +140,71 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   st = check_device();
   if (st != ATTN_OK) return st;
   AttnParams p;
-  std::memset(&p, 0, sizeof(p));
-  if (!encode_bf16_map_3d(&p.tm_q, q, D, S_q, (uint64_t)B * H_q, 128) ||
-      !encode_bf16_map_3d(&p.tm_k, k, D, S_kv, (uint64_t)B * H_kv, 128) ||
-      !encode_bf16_map_3d(&p.tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128) ||
-      !encode_bf16_map_3d(&p.tm_o, o, D, S_q, (uint64_t)B * H_q, 32))
-    return ATTN_ERR_CUDA;
-  p.lse = lse;
-  p.B = B;
-  p.H_q = H_q;
-  p.H_kv = H_kv;
-  p.S_q = S_q;
-  p.S_kv = S_kv;
-  p.causal = causal;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  st = make_params(&p, q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
+  if (st != ATTN_OK) return st;
   p.timeout_ns = timeout_ns;
   p.trace = trace;
   p.trace_ctas = trace_ctas;
   p.trace_blocks = trace_blocks;
   p.fault_drop_block = fault_drop_block;
-  const int n_m_tiles = (S_q + 255) / 256;
-  if (launch_attn_fwd(p, D, n_m_tiles, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (launch_attn_fwd(p, D, n_m_tiles_of(H_q, H_kv, S_q), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+// Split count used when the caller passes num_splits <= 0: enough CTAs to
+// fill about two waves of the GPU, each split at least two KV blocks long.
+static int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = (long long)n_m_tiles_of(H_q, H_kv, S_q) * H_kv * B;
+  const int kv_blocks = ((causal ? (S_kv < S_q ? S_kv : S_q) : S_kv) + 127) / 128;
+  long long want = (2LL * sms + tiles - 1) / tiles;
+  long long cap = kv_blocks / 2;
+  if (want > cap) want = cap;
+  if (want > kMaxSplits) want = kMaxSplits;
+  return want < 1 ? 1 : (int)want;
+}
+
+static size_t splitkv_bytes(int B, int H_q, int S_q, int D, int splits) {
+  const size_t rows = (size_t)B * H_q * S_q;
+  const size_t o_bytes = (size_t)splits * rows * D * sizeof(float);
+  const size_t o_pad = (o_bytes + 255) & ~(size_t)255;
+  return o_pad + (size_t)splits * rows * sizeof(float);
+}
+
+static attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  void* workspace, size_t workspace_bytes, int B, int H_q,
+                                  int H_kv, int S_q, int S_kv, int D, int causal, float scale,
+                                  int num_splits, attn_stream_t stream) {
+  attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
+  if (st != ATTN_OK) return st;
+  if (!workspace) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  if (num_splits > kMaxSplits) return ATTN_ERR_UNSUPPORTED;
+  st = check_device();
+  if (st != ATTN_OK) return st;
+  const int splits = num_splits > 0 ? num_splits
+                                    : default_splits(B, H_q, H_kv, S_q, S_kv, causal);
+  if (workspace_bytes < splitkv_bytes(B, H_q, S_q, D, splits)) return ATTN_ERR_INVALID_ARG;
+  AttnParams p;
+  st = make_params(&p, q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
+  if (st != ATTN_OK) return st;
+  const int kv_blocks = (S_kv + 127) / 128;
+  p.kv_splits = splits;
+  p.kv_blocks_per_split = (kv_blocks + splits - 1) / splits;
+  const size_t rows = (size_t)B * H_q * S_q;
+  const size_t o_bytes = (size_t)splits * rows * D * sizeof(float);
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        ((o_bytes + 255) & ~(size_t)255));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_attn_fwd(p, D, n_m_tiles_of(H_q, H_kv, S_q), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_splitkv_combine(p.o_part, p.lse_part, o, lse, (long long)rows, D, splits, s) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -217,6 +293,26 @@ attn_status_t attn_device_status(int* status_out, int reset) {
 }
 
 int attn_version(void) { return 100; }
+
+size_t attn_splitkv_workspace_bytes(int B, int H_q, int S_q, int D, int num_splits) {
+  if (B <= 0 || H_q <= 0 || S_q <= 0 || (D != 64 && D != 128) || num_splits <= 0 ||
+      num_splits > kMaxSplits)
+    return 0;
+  return splitkv_bytes(B, H_q, S_q, D, num_splits);
+}
+
+int attn_splitkv_default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || S_q <= 0 || S_kv <= 0 || H_q % H_kv != 0) return 0;
+  return default_splits(B, H_q, H_kv, S_q, S_kv, causal);
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                               int S_q, int S_kv, int D, int causal, float scale, int num_splits,
+                               attn_stream_t stream) {
+  return splitkv_impl(q, k, v, o, lse, workspace, workspace_bytes, B, H_q, H_kv, S_q, S_kv, D,
+                      causal, scale, num_splits, stream);
+}
 
 attn_status_t attn_selftest_qk(const void* q, const void* k, float* s, int D, attn_stream_t stream) {
   if (!q || !k || !s) return ATTN_ERR_INVALID_ARG;

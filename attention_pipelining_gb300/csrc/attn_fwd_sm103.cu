@@ -129,17 +129,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // grid = (query tiles, H_q, B): the tiles of one head are adjacent in launch
-  // order, so the CTAs resident at once share few heads' K/V in L2; within a
-  // head the longest (causal) tiles launch first.
-  const int m0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBlockM);
-  const int h = blockIdx.y;
+  // grid = (query tiles x KV splits, H_kv, B).  A CTA works on 256 rows of
+  // one row group (the query heads sharing KV head g of batch b, see
+  // AttnParams); the tiles of one group are adjacent in launch order, so the
+  // CTAs resident at once share few K/V heads in L2, and within a group the
+  // longest causal tiles launch first.
+  const int R = p.rows_per_group;
+  const int split = blockIdx.x % p.kv_splits;
+  const int m0 = ((int)(gridDim.x / p.kv_splits) - 1 - (int)(blockIdx.x / p.kv_splits)) * (2 * kBlockM);
   const int b = blockIdx.z;
-  const int hkv = h / (p.H_q / p.H_kv);
-  const int zq = b * p.H_q + h;
-  const int zkv = b * p.H_kv + hkv;
-  const int kv_end = p.causal ? min(p.S_kv, m0 + 2 * kBlockM) : p.S_kv;
-  const int n_blocks = (kv_end + kBlockN - 1) / kBlockN;
+  const int zkv = b * p.H_kv + blockIdx.y;  // row group = K/V head index
+  // keys any row of this tile may see: row rho is query position rho % S_q,
+  // and with the causal mask it sees keys <= its position
+  int kv_end = p.S_kv;
+  if (p.causal) {
+    const int last = min(m0 + 2 * kBlockM, R) - 1;
+    kv_end = min(p.S_kv, (m0 / p.S_q == last / p.S_q) ? last % p.S_q + 1 : p.S_q);
+  }
+  const int n_total = (kv_end + kBlockN - 1) / kBlockN;
+  const int jb = split * p.kv_blocks_per_split;  // first KV block of this CTA
+  const int n_blocks = min(n_total - jb, p.kv_blocks_per_split);
+  if (n_blocks <= 0) {
+    // split-KV only: no key of this split is visible to any row of the tile,
+    // so its partial result is empty (weight 0 in the merge)
+    for (int idx = threadIdx.x; idx < 2 * kBlockM; idx += kThreads) {
+      const int rho = m0 + idx;
+      if (rho < R) {
+        const size_t row = (size_t)split * p.total_rows + (size_t)zkv * R + rho;
+        p.lse_part[row] = -INFINITY;
+        float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    return;
+  }
   const uint64_t budget = p.timeout_ns;
   // trace stamps (compiled only into the trace instantiation)
   const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
@@ -198,11 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int t = wg;
     const int r = (warp & 3) * 32 + lane;                 // row within the sub-tile
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::kTmS1 : C::kTmS0);
-    const int row = m0 + t * kBlockM + r;                  // query row in the sequence
-    const int row_first = m0 + t * kBlockM;
+    const int rho = m0 + t * kBlockM + r;                  // row in the row group
+    const int pos = rho % p.S_q;                           // its query position
+    // smallest query position in this sub-tile (0 if it spans two heads)
+    const int sub_first = m0 + t * kBlockM;
+    const int min_pos = (sub_first / p.S_q == (sub_first + kBlockM - 1) / p.S_q) ? sub_first % p.S_q : 0;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    const int key_limit = p.causal ? min(p.S_kv, row + 1) : p.S_kv;
+    const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
     // Two row sums: l_run of the fp32 probabilities (for the LSE), and lp_run
     // of the bf16-rounded probabilities that the PV GEMM actually consumes,
     // so O is normalised by the same weights it was accumulated with.
@@ -231,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         reg_after_wait(s3);
       }
       if (lane == 0) stamp(t ? kEvSm1Loaded : kEvSm0Loaded, j);
-      const int kv0 = j * kBlockN;
-      const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > row_first);
+      const int kv0 = (jb + j) * kBlockN;
+      const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > min_pos);
       const int lim = key_limit - kv0;  // columns c < lim are visible to this row
       float m_use = m_run;
       float alpha = 1.f;
@@ -357,8 +383,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (lane == 0) stamp(kEvEpilogue, t);
       const float l = sRowSum[t * kBlockM + r];
       const float m = sRowMax[t * kBlockM + r];
-      const float inv_l = 1.f / sRowSumP[t * kBlockM + r];
+      const float lp = sRowSumP[t * kBlockM + r];
+      // a row with no visible key (possible only within one KV split) has
+      // l = 0: its partial result is O = 0, LSE = -inf
+      const bool empty = !(lp > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / lp;
+      const float lse_row = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
       const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
+      const int rho = m0 + t * kBlockM + r;
+      if (p.o_part != nullptr) {
+        // split-KV partial: fp32 O normalised within the split, and its LSE.
+        // The tensor-memory loads are warp-wide; only the stores depend on
+        // whether the row exists.
+        const size_t row = (size_t)split * p.total_rows + (size_t)zkv * R + rho;
+        float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + ch * 32, o);
+          tmem_ld_wait();
+          reg_after_wait(o);
+          if (rho < R) {
+#pragma unroll
+            for (int qd = 0; qd < 8; ++qd)
+              dst[ch * 8 + qd] = make_float4(u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
+                                             u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
+          }
+        }
+        if (rho < R) p.lse_part[row] = lse_row;
+        continue;
+      }
       uint8_t* stage = sQ + t * C::kTileBytes;  // Q_t is no longer read: reuse it
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -379,17 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           *reinterpret_cast<uint4*>(stage + half * C::kHalfBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = val;
         }
       }
-      const int grow = m0 + t * kBlockM + r;
-      if (grow < p.S_q) {
-        p.lse[(size_t)zq * p.S_q + grow] = (m + log2f(l)) * 0.69314718055994530942f;
-      }
+      if (rho < R) p.lse[(size_t)zkv * R + rho] = lse_row;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
         for (int hf = 0; hf < C::kHalves; ++hf) {
           tma_store_3d(&p.tm_o, stage + hf * C::kHalfBytes + q4 * 32 * 128, hf * 64,
-                       m0 + t * kBlockM + q4 * 32, zq);
+                       m0 + t * kBlockM + q4 * 32, zkv);
         }
         tma_store_commit();
       }
@@ -477,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t pol_kv = l2_policy_evict_last();
       for (int t = 0; t < 2; ++t) {
         mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
-        tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zq, pol_q);
+        tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zkv, pol_q);
       }
       int issued = 0;
       for (int idx = 0; idx < 2 * n_blocks; ++idx) {
@@ -486,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (round > 0 && !mbar_wait(&kv_empty[slot], (round - 1) & 1, sAbort, budget)) break;
         mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
         const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
-        tma_load_tile<D>(sKV + slot * C::kTileBytes, map, &kv_full[slot], (idx >> 1) * kBlockN, zkv,
-                         pol_kv);
+        tma_load_tile<D>(sKV + slot * C::kTileBytes, map, &kv_full[slot],
+                         (jb + (idx >> 1)) * kBlockN, zkv, pol_kv);
         stamp((idx & 1) ? kEvLoadV : kEvLoadK, idx >> 1);
         issued = idx + 1;
       }
@@ -526,7 +577,7 @@ cudaError_t launch_d(const AttnParams& p, int n_m_tiles, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  dim3 grid(n_m_tiles, p.H_q, p.B);
+  dim3 grid(n_m_tiles * p.kv_splits, p.H_kv, p.B);
   attn_fwd_kernel<D, kTrace><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

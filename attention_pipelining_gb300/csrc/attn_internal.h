@@ -12,12 +12,26 @@ namespace attnpipe {
 
 // Everything the fused kernel reads, passed as one __grid_constant__ block.
 struct AttnParams {
-  CUtensorMap tm_q;  // Q as [B*H_q, S_q, D], box {64, 128, 1}, 128-byte swizzle (load)
+  // Row groups: the H_q / H_kv query heads that share a KV head form one
+  // group of R = (H_q / H_kv) * S_q rows (row rho = head-in-group * S_q +
+  // position); a group's rows are contiguous in the [B, H_q, S_q, D] layout.
+  CUtensorMap tm_q;  // Q as [B*H_kv, R, D], box {64, 128, 1}, 128-byte swizzle (load)
   CUtensorMap tm_k;  // K as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
   CUtensorMap tm_v;  // V as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
-  CUtensorMap tm_o;  // O as [B*H_q, S_q, D], box {64, 32, 1} (store, rows >= S_q dropped)
+  CUtensorMap tm_o;  // O as [B*H_kv, R, D], box {64, 32, 1} (store, rows >= R dropped)
   float* lse;        // [B, H_q, S_q]
   int B, H_q, H_kv, S_q, S_kv, causal;
+  int rows_per_group;       // R
+  long long total_rows;     // B * H_q * S_q
+  // Split KV: CTA x-index = query tile * kv_splits + split; split s covers KV
+  // blocks [s * kv_blocks_per_split, (s + 1) * kv_blocks_per_split).  With
+  // kv_splits > 1 the CTA writes a partial result instead of O and LSE:
+  // o_part [kv_splits, total_rows, D] fp32 (normalised within the split) and
+  // lse_part [kv_splits, total_rows] fp32 (-inf for a row with no key in it).
+  int kv_splits;
+  int kv_blocks_per_split;
+  float* o_part;
+  float* lse_part;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   unsigned long long timeout_ns;  // budget of any single wait inside the kernel
   // Timeline trace (the trace instantiation only): globaltimer stamps,
@@ -61,10 +75,14 @@ enum TraceEvent : int {
 bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t rows,
                         uint64_t outer, uint32_t box_rows);
 
-// Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(S_q / 256).
+// Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(R / 256).
 // With p.trace set or p.fault_drop_block >= 0, the diagnostic instantiation
 // (timeline stamps, timeout test) runs instead.
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream);
+
+// Queues the merge of split-KV partial results into O (bf16) and LSE.
+cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                                   long long rows, int D, int splits, cudaStream_t stream);
 
 // Reads (and optionally clears) the device status word of the current device.
 cudaError_t read_device_status(int* status, bool reset);
@@ -79,5 +97,6 @@ cudaError_t launch_selftest_pv(const uint16_t* p, const CUtensorMap& tv, float* 
                                cudaStream_t stream);
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxSplits = 128;  // most KV splits of the split-KV forward
 
 }  // namespace attnpipe

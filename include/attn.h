@@ -35,6 +35,7 @@
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -86,6 +87,40 @@ attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *
                             void *v_dev, void *o_dev, float *lse_dev, int B, int H_q, int H_kv,
                             int S_q, int S_kv, int D, int causal, float scale,
                             attn_stream_t stream);
+
+/*
+ * Split-KV ("FlashDecoding") forward: the same result as attn_fwd, computed
+ * with the KV axis cut into `num_splits` ranges that run as separate CTAs,
+ * followed by a merge of their partial results, L = ln sum_s exp(L_s),
+ * O = sum_s exp(L_s - L) O_s.  The FlashDecoding microbenchmark of
+ * "PipeThreader: Software-Defined Pipelining for Efficient DNN Execution",
+ * section A4, is this operator at decoding shapes (S_q = 1): there a single
+ * query row per head leaves the GPU idle unless the keys are split.
+ *
+ *   workspace        caller-owned device scratch, 256-byte aligned, of at
+ *                    least attn_splitkv_workspace_bytes(B, H_q, S_q, D, s)
+ *                    bytes for the split count s actually used; it holds the
+ *                    partial O (fp32) and LSE of every split
+ *   num_splits       1..128, or <= 0 for attn_splitkv_default_splits(...)
+ *
+ * Other arguments, layouts and errors as attn_fwd; additionally
+ * ATTN_ERR_INVALID_ARG for a null or too small workspace,
+ * ATTN_ERR_MISALIGNED for a workspace not 256-byte aligned,
+ * ATTN_ERR_UNSUPPORTED for num_splits > 128.  Two kernels are queued on
+ * `stream`; the workspace must not be shared with concurrent calls.
+ */
+attn_status_t attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                               void *workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                               int S_q, int S_kv, int D, int causal, float scale, int num_splits,
+                               attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_splitkv needs for `num_splits` splits (0 if the
+ * arguments are invalid). */
+size_t attn_splitkv_workspace_bytes(int B, int H_q, int S_q, int D, int num_splits);
+
+/* The split count attn_fwd_splitkv uses when given num_splits <= 0 for these
+ * sizes on the current device (0 if the arguments are invalid). */
+int attn_splitkv_default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal);
 
 /* Static English description of a status code (never NULL). */
 const char *attn_status_string(attn_status_t status);

@@ -107,6 +107,19 @@ def test_timeout_test_entry_validation(lib):
     assert lib.attn_fwd_timeout_test(*bad, 1, 20_000_000, None) == 2
 
 
+def test_splitkv_entry_validation(lib):
+    ws = A
+    base = [A, A, A, A, A]
+    dims = [1, 4, 2, 1, 4096, 128, 0, ctypes.c_float(0.1)]
+    assert lib.attn_fwd_splitkv(*base, None, 1 << 20, *dims, 4, None) == 1        # no workspace
+    assert lib.attn_fwd_splitkv(*base, ws + 16, 1 << 20, *dims, 4, None) == 3     # not 256-aligned
+    assert lib.attn_fwd_splitkv(*base, ws, 1 << 20, *dims, 129, None) == 2        # too many splits
+    assert lib.attn_splitkv_workspace_bytes(1, 4, 1, 128, 4) == 4 * 4 * (128 * 4) + 4 * 4 * 4 + (
+        (256 - (4 * 4 * 128 * 4) % 256) % 256)
+    assert lib.attn_splitkv_workspace_bytes(1, 4, 1, 96, 4) == 0
+    assert lib.attn_splitkv_default_splits(1, 3, 2, 1, 100, 0) == 0
+
+
 def test_device_status_null(lib):
     assert lib.attn_device_status(None, 0) == 1
 
