@@ -34,7 +34,8 @@ STATUS = {
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
            "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
            "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
-           "attn_splitkv_default_splits"]
+           "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
+           "attn_splitkv_noalloc_capacity"]
 
 
 class AttnError(RuntimeError):
@@ -86,6 +87,11 @@ def _load():
     lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_splitkv_default_splits.argtypes = [ci, ci, ci, ci, ci, ci]
     lib.attn_splitkv_default_splits.restype = ci
+    lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                             ci, vp]
+    lib.attn_fwd_splitkv_noalloc.restype = ci
+    lib.attn_splitkv_noalloc_capacity.argtypes = []
+    lib.attn_splitkv_noalloc_capacity.restype = ctypes.c_size_t
     _lib = lib
     return lib
 

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
 
-SOURCES = ["attn_fwd_sm103.cu", "attn_api.cu", "selftest.cu", "attn_combine.cu"]
+SOURCES = ["attn_fwd_sm103.cu", "attn_api.cu", "selftest.cu", "attn_combine.cu",
+           "attn_noalloc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

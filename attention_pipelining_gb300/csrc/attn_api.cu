@@ -71,8 +71,8 @@ bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t
   return r == CUDA_SUCCESS;
 }
 
-// Pure argument checks (no CUDA calls), shared by both entry points.
-static attn_status_t validate(const void* q, const void* k, const void* v, const void* o,
+// Pure argument checks (no CUDA calls), shared by the entry points.
+attn_status_t validate(const void* q, const void* k, const void* v, const void* o,
                               const void* lse, int B, int H_q, int H_kv, int S_q, int S_kv, int D,
                               int causal, float scale) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -155,7 +155,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
 
 // Split count used when the caller passes num_splits <= 0: enough CTAs to
 // fill about two waves of the GPU, each split at least two KV blocks long.
-static int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
+int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
   int sms = 152;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -169,14 +169,14 @@ static int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causa
   return want < 1 ? 1 : (int)want;
 }
 
-static size_t splitkv_bytes(int B, int H_q, int S_q, int D, int splits) {
+size_t splitkv_bytes(int B, int H_q, int S_q, int D, int splits) {
   const size_t rows = (size_t)B * H_q * S_q;
   const size_t o_bytes = (size_t)splits * rows * D * sizeof(float);
   const size_t o_pad = (o_bytes + 255) & ~(size_t)255;
   return o_pad + (size_t)splits * rows * sizeof(float);
 }
 
-static attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                                   void* workspace, size_t workspace_bytes, int B, int H_q,
                                   int H_kv, int S_q, int S_kv, int D, int causal, float scale,
                                   int num_splits, attn_stream_t stream) {

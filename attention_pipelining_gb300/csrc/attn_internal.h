@@ -96,6 +96,17 @@ cudaError_t launch_selftest_qk(const CUtensorMap& tq, const CUtensorMap& tk, flo
 cudaError_t launch_selftest_pv(const uint16_t* p, const CUtensorMap& tv, float* o, int D,
                                cudaStream_t stream);
 
+// Host-side pieces of the C ABI (attn_api.cu) used by more than one file.
+attn_status_t validate(const void* q, const void* k, const void* v, const void* o, const void* lse,
+                       int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                       float scale);
+int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal);
+size_t splitkv_bytes(int B, int H_q, int S_q, int D, int splits);
+attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                           int S_q, int S_kv, int D, int causal, float scale, int num_splits,
+                           attn_stream_t stream);
+
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxSplits = 128;  // most KV splits of the split-KV forward
 

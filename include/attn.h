@@ -122,6 +122,41 @@ size_t attn_splitkv_workspace_bytes(int B, int H_q, int S_q, int D, int num_spli
  * sizes on the current device (0 if the arguments are invalid). */
 int attn_splitkv_default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal);
 
+/*
+ * attn_fwd_splitkv without a caller workspace, for callers that cannot
+ * allocate device memory: an engine that gives all device memory to its own
+ * pool at start-up and allows no further allocations, a plugin loaded into a
+ * program that exposes no allocator to it, or a latency-critical path where
+ * an allocation call could block on the device.  The paper has no
+ * counterpart of this entry point; it is an interface convenience.
+ *
+ * The partial results go to a scratch array of fixed size,
+ * attn_splitkv_noalloc_capacity() = 16 MiB, that is part of the library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits.  A call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).  The first call on a device looks up the array's device
+ * address once (cudaGetSymbolAddress with that device current) and caches
+ * it; make that first call before any stream capture.
+ *
+ * All calls on a device share the one array, which keeps the last call's
+ * contents; every partial a call reads is written by that same call, so
+ * nothing needs clearing.  Calls whose GPU work overlaps (different streams
+ * without ordering) race on the array: order them, e.g. on one stream.
+ *
+ * Same arguments and results as attn_fwd_splitkv minus the workspace; a call
+ * whose partial results would exceed the array (see
+ * attn_splitkv_workspace_bytes for the split count used) returns
+ * ATTN_ERR_UNSUPPORTED without launching anything: use attn_fwd_splitkv with
+ * a workspace, or fewer splits.
+ */
+attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
+                                       float *lse, int B, int H_q, int H_kv, int S_q, int S_kv,
+                                       int D, int causal, float scale, int num_splits,
+                                       attn_stream_t stream);
+
+/* Bytes of the built-in scratch array attn_fwd_splitkv_noalloc uses. */
+size_t attn_splitkv_noalloc_capacity(void);
+
 /* Static English description of a status code (never NULL). */
 const char *attn_status_string(attn_status_t status);
 
