@@ -147,6 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     kv_end = min(p.S_kv, (m0 / p.S_q == last / p.S_q) ? last % p.S_q + 1 : p.S_q);
   }
   const int n_total = (kv_end + kBlockN - 1) / kBlockN;
+  // sub-tile 1 holds rows m0 + 128 .. m0 + 255; when none of them exists
+  // (short row groups, e.g. one decoding token per head, or a ragged last
+  // tile) every role skips it and the tile costs half
+  const bool has_sub1 = (m0 + kBlockM) < R;
   const int jb = split * p.kv_blocks_per_split;  // first KV block of this CTA
   const int n_blocks = min(n_total - jb, p.kv_blocks_per_split);
   if (n_blocks <= 0) {
@@ -217,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (wg < 2) {
     // ------------------------------------------------------------ softmax
+    // (warpgroup 1 has nothing to do when the tile has no sub-tile 1)
+    if (wg == 0 || has_sub1) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax) : "memory");
     const int t = wg;
     const int r = (warp & 3) * 32 + lane;                 // row within the sub-tile
@@ -340,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       sRowMax[t * kBlockM + r] = m_run;
       mbar_arrive(&fin[t]);
     }
+    }
   } else if (wg == 2) {
     // ------------------------------------------------------------ correction + epilogue
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsCorrection) : "memory");
@@ -350,10 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // Block 0 needs no rescale.  For block j >= 1 the softmax's alpha arrives
     // on stats[t]; it is published after the softmax saw S_t(j), whose commit
     // follows PV_t(j-1), so O_t already holds every earlier block.
+    const int n_sub = has_sub1 ? 2 : 1;
     mbar_arrive(&p_full[0]);
-    mbar_arrive(&p_full[1]);
+    if (has_sub1) mbar_arrive(&p_full[1]);
     for (int j = 1; j < n_blocks && ok; ++j) {
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < n_sub; ++t) {
         if (!warp_wait(&stats[t], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
         const float alpha = sScale[t * kBlockM + r];
         tc_fence_after_sync();
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         mbar_arrive(&p_full[t]);
       }
     }
-    for (int t = 0; t < 2 && ok; ++t) {
+    for (int t = 0; t < n_sub && ok; ++t) {
       if (!warp_wait(&fin[t], 0, sAbort, budget)) { ok = false; break; }
       if (!warp_wait(&pv_done[t], 0, sAbort, budget)) { ok = false; break; }
       tc_fence_after_sync();
@@ -468,12 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         issue_qk_gemm<D>(tS0, dq0, dk0);
         tc_commit(&s_full[0]);
         stamp(kEvMmaS0, 0);
-        if (!mbar_wait(&q_full[1], 0, sAbort, budget)) break;
-        tc_fence_after_sync();
-        issue_qk_gemm<D>(tS1, dq1, dk0);
-        tc_commit(&s_full[1]);
+        if (has_sub1) {
+          if (!mbar_wait(&q_full[1], 0, sAbort, budget)) break;
+          tc_fence_after_sync();
+          issue_qk_gemm<D>(tS1, dq1, dk0);
+          tc_commit(&s_full[1]);
+          stamp(kEvMmaS1, 0);
+        }
         tc_commit(&kv_empty[0]);
-        stamp(kEvMmaS1, 0);
         int sv = 1 % C::kStages, sk = 2 % C::kStages;   // ring stages of V_j and K_{j+1}
         for (int j = 0; j < n_blocks; ++j) {
           const bool more = (j + 1) < n_blocks;
@@ -500,17 +510,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             stamp(kEvMmaS0, j + 1);
           }
           // sub-tile 1: O_1 += P_1 V_j, then S_1 = Q_1 K_{j+1}^T
-          if (!mbar_wait(&p_full[1], j & 1, sAbort, budget)) break;
-          tc_fence_after_sync();
-          stamp(kEvMmaPV1Begin, j);
-          issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
-          if (!more) tc_commit(&pv_done[1]);
-          stamp(kEvMmaPV1, j);
-          if (more) {
-            stamp(kEvMmaS1Begin, j + 1);
-            issue_qk_gemm<D>(tS1, dq1, dk);
-            tc_commit(&s_full[1]);
-            stamp(kEvMmaS1, j + 1);
+          if (has_sub1) {
+            if (!mbar_wait(&p_full[1], j & 1, sAbort, budget)) break;
+            tc_fence_after_sync();
+            stamp(kEvMmaPV1Begin, j);
+            issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
+            if (!more) tc_commit(&pv_done[1]);
+            stamp(kEvMmaPV1, j);
+            if (more) {
+              stamp(kEvMmaS1Begin, j + 1);
+              issue_qk_gemm<D>(tS1, dq1, dk);
+              tc_commit(&s_full[1]);
+              stamp(kEvMmaS1, j + 1);
+            }
           }
           // release the ring slots last: off the critical path
           tc_commit(&kv_empty[sv]);
@@ -526,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // TMA producer (one thread)
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < (has_sub1 ? 2 : 1); ++t) {
         mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
         tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zkv, pol_q);
       }
@@ -545,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // every copy issued must land before the CTA exits (on the normal path
       // these phases completed long ago)
       drain_wait(&q_full[0], 0, budget);
-      drain_wait(&q_full[1], 0, budget);
+      if (has_sub1) drain_wait(&q_full[1], 0, budget);
       const int first = issued > C::kStages ? issued - C::kStages : 0;
       for (int idx = first; idx < issued; ++idx)
         drain_wait(&kv_full[idx % C::kStages], (idx / C::kStages) & 1, budget);

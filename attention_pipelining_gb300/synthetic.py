@@ -30,6 +30,7 @@ class Workload:
     causal: bool
     k_scale: float = 1.0
     seed: int = 0
+    path: str = "fused"   # "fused": attn_fwd; "splitkv": attn_fwd_splitkv (decoding shapes)
 
     @property
     def scale(self) -> float:
@@ -40,6 +41,13 @@ class Workload:
         """4 * B * H_q * S_q * S_kv * D, halved when causal (two GEMMs of 2*M*N*K)."""
         f = 4.0 * self.B * self.H_q * self.S_q * self.S_kv * self.D
         return f / 2.0 if self.causal else f
+
+    @property
+    def io_bytes(self) -> int:
+        """Bytes the operation must move at least: Q, K, V read; O, LSE written."""
+        q = self.B * self.H_q * self.S_q * self.D * 2
+        kv = 2 * self.B * self.H_kv * self.S_kv * self.D * 2
+        return q + kv + q + self.B * self.H_q * self.S_q * 4
 
     def as_dict(self) -> dict:
         d = asdict(self)
@@ -58,6 +66,10 @@ WORKLOADS = {
         Workload("long_b1_h32_s16384_d128", 1, 32, 32, 16384, 16384, 128, False),
         Workload("long_causal_b1_h32_s16384_d128", 1, 32, 32, 16384, 16384, 128, True),
         Workload("gqa_b8_hq32_hkv8_s4096_d64_k3", 8, 32, 8, 4096, 4096, 64, True, k_scale=3.0),
+        # decoding: one query token per sequence against an 8192-token KV cache,
+        # grouped heads of an 8B-class model (32 query heads over 8 KV heads)
+        Workload("decode_b32_hq32_hkv8_sq1_skv8192_d128", 32, 32, 8, 1, 8192, 128, False,
+                 path="splitkv"),
     ]
 }
 

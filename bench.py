@@ -66,6 +66,14 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS * 0.9, "fallback"
 
 
+def load_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
 def load_traffic():
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -285,8 +293,24 @@ def run_ours(args, w):
     out_bytes = o.numel() * 2 + lse.numel() * 4
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        ap.attn_fwd_out(q, k, v, o, lse, w.causal, w.scale, stream)
+    splitkv = (w.path == "splitkv")
+    if splitkv:
+        splits = ap.splitkv_default_splits(w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.causal)
+        ws = torch.empty(int(ap._load().attn_splitkv_workspace_bytes(w.B, w.H_q, w.S_q, w.D, splits)),
+                         dtype=torch.uint8, device=dev)
+
+        def run_path(qq, kk, vv):
+            return ap.attn_fwd_splitkv(qq, kk, vv, w.causal, w.scale, num_splits=splits,
+                                       workspace=ws, stream=stream)
+
+        def step():
+            ap._check(ap._load().attn_fwd_splitkv(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                ws.data_ptr(), ws.numel(), w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.D, int(w.causal),
+                float(w.scale), splits, stream.cuda_stream), "attn_fwd_splitkv")
+    else:
+        def step():
+            ap.attn_fwd_out(q, k, v, o, lse, w.causal, w.scale, stream)
 
     for _ in range(args.warmup):
         step()
@@ -322,7 +346,16 @@ def run_ours(args, w):
     lh = torch.empty((w.B, w.H_q, w.S_q), dtype=torch.float32).pin_memory()
 
     def e2e_step():
-        ap.attn_fwd_host(qh, kh, vh, oh, lh, q, k, v, o, lse, w.causal, w.scale, stream)
+        if splitkv:
+            # the split-KV entry takes device buffers: pinned host copies in and out
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            step()
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+        else:
+            ap.attn_fwd_host(qh, kh, vh, oh, lh, q, k, v, o, lse, w.causal, w.scale, stream)
 
     for _ in range(2):
         e2e_step()
@@ -340,6 +373,7 @@ def run_ours(args, w):
     if rank != 0:
         return
     peak, peak_sustained, peak_kind = load_peaks()
+    hbm_peak = load_hbm_peak()
     flops = w.flops
     value = world * flops * args.steps / t / 1e12
     per_launch = t_local / args.steps
@@ -366,7 +400,7 @@ def run_ours(args, w):
                   if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
         },
         "pct_of_peak": 100.0 * achieved / peak,
-        "roofline": {
+        "roofline": ({
             "bound": "tensor",
             "achieved": achieved,
             "peak": peak,
@@ -377,7 +411,18 @@ def run_ours(args, w):
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
             "algorithmic_flops_per_launch": flops,
             "kernel": "attn_fwd_kernel",
-        },
+        } if not splitkv else {
+            "bound": "hbm",
+            "achieved": w.io_bytes / per_launch / 1e9,
+            "peak": hbm_peak[0],
+            "unit": "GB/s",
+            "frac": w.io_bytes / per_launch / 1e9 / hbm_peak[0],
+            "peak_kind": f"{hbm_peak[1]} HBM copy",
+            "traffic": None,
+            "algorithmic_bytes_per_launch": w.io_bytes,
+            "kernel": "attn_fwd_kernel (split KV) + splitkv_combine_kernel, timed together",
+            "num_splits": splits,
+        }),
         "e2e": {
             "value": world * flops * e2e_steps / t_e2e / 1e12,
             "unit": "TFLOP/s",
@@ -385,7 +430,7 @@ def run_ours(args, w):
             "d2h_bytes_per_step": out_bytes,
             "steps": e2e_steps,
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if splitkv else 1),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

@@ -132,7 +132,12 @@ def test_full_size_sampled_rows(name):
     sampled rows that the oracle computes one by one."""
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    if w.path == "splitkv":
+        o, lse = ap.attn_fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), w.causal, w.scale)
+        torch.cuda.synchronize()
+        o, lse = o.cpu(), lse.cpu()
+    else:
+        o, lse = run_gpu(q, k, v, w.causal, w.scale)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     rows = _sample_rows(w)
     o64, lse64 = oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
@@ -142,14 +147,16 @@ def test_full_size_sampled_rows(name):
 
 
 def test_trace_instantiation_matches_and_stamps():
-    """The trace instantiation computes the same result and stamps every role."""
-    q, k, v = make_qkv(1, 2, 2, 600, 600, 128, seed=8)
+    """The trace instantiation computes the same result and stamps every role
+    (S = 512: every traced tile has both 128-row sub-tiles)."""
+    q, k, v = make_qkv(1, 2, 2, 512, 600, 128, seed=8)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o, lse = ap.attn_fwd(qd, kd, vd, False, 0.09)
     o2, lse2, tr = ap.attn_fwd_trace(qd, kd, vd, False, 0.09, ctas=2)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
     n = (600 + 127) // 128
     t = tr.numpy()
+    assert tr.shape[0] == 2
     for ev in ("sm0_wake", "sm0_done", "sm1_wake", "sm1_done", "mma_pv0", "mma_pv1",
                "mma_s0", "mma_s1", "load_k", "load_v"):
         e = ap.TRACE_EVENTS.index(ev)
