@@ -153,8 +153,11 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   return ATTN_OK;
 }
 
-// Split count used when the caller passes num_splits <= 0: enough CTAs to
-// fill about two waves of the GPU, each split at least two KV blocks long.
+// Split count used when the caller passes num_splits <= 0.  The split-KV
+// forward is bound by streaming K and V, so the CTAs should fill whole waves
+// of the GPU: with fewer query tiles than SMs, one wave of about one CTA per
+// SM; otherwise the split count in 1..4 whose last wave is fullest.  Each
+// split keeps at least two KV blocks.
 int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
   int sms = 152;
   int dev = 0;
@@ -162,8 +165,22 @@ int default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int causal) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long tiles = (long long)n_m_tiles_of(H_q, H_kv, S_q) * H_kv * B;
   const int kv_blocks = ((causal ? (S_kv < S_q ? S_kv : S_q) : S_kv) + 127) / 128;
-  long long want = (2LL * sms + tiles - 1) / tiles;
-  long long cap = kv_blocks / 2;
+  long long want = 1;
+  if (tiles < sms) {
+    want = sms / tiles;
+  } else {
+    double best = 0.0;
+    for (int s = 1; s <= 4; ++s) {
+      const long long ctas = tiles * s;
+      const long long waves = (ctas + sms - 1) / sms;
+      const double fill = (double)ctas / (double)(waves * sms);
+      if (fill > best + 1e-9) {
+        best = fill;
+        want = s;
+      }
+    }
+  }
+  const long long cap = kv_blocks / 2;
   if (want > cap) want = cap;
   if (want > kMaxSplits) want = kMaxSplits;
   return want < 1 ? 1 : (int)want;
