@@ -2,6 +2,7 @@
 //
 // Host-side half of the boundary declared in include/attn.h.  Every check
 // runs before anything touches the device; nothing here allocates memory.
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -82,10 +83,12 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  // grid is (ceil(R / 256) x splits, H_kv, B) with R = (H_q / H_kv) * S_q
-  // rows per K/V head; y and z are limited to 65535, R must fit an int
+  // R = (H_q / H_kv) * S_q rows per K/V head must fit an int, and so must
+  // the number of 256-row work tiles, ceil(R / 256) * B * H_kv
   if (B > 65535 || H_kv > 65535) return ATTN_ERR_UNSUPPORTED;
   if ((int64_t)(H_q / H_kv) * S_q >= (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
+  if ((((int64_t)(H_q / H_kv) * S_q + 255) / 256) * B * H_kv >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
   // tensor-map extents must stay below 2^32 per dimension
   if ((int64_t)B * H_q >= (1ll << 31) || (int64_t)B * H_kv >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
@@ -108,9 +111,9 @@ static attn_status_t make_params(AttnParams* p, const void* q, const void* k, co
   const int R = (H_q / H_kv) * S_q;
   if (!encode_bf16_map_3d(&p->tm_q, q, D, R, (uint64_t)B * H_kv, 128) ||
       !encode_bf16_map_3d(&p->tm_k, k, D, S_kv, (uint64_t)B * H_kv, 128) ||
-      !encode_bf16_map_3d(&p->tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128) ||
-      !encode_bf16_map_3d(&p->tm_o, o, D, R, (uint64_t)B * H_kv, 32))
+      !encode_bf16_map_3d(&p->tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128))
     return ATTN_ERR_CUDA;
+  p->o = o;
   p->lse = lse;
   p->B = B;
   p->H_q = H_q;
@@ -120,15 +123,29 @@ static attn_status_t make_params(AttnParams* p, const void* q, const void* k, co
   p->causal = causal;
   p->rows_per_group = R;
   p->total_rows = (long long)B * H_q * S_q;
-  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+  // The kernel needs scale_log2 > 0 (a masked score -inf must stay -inf
+  // after scaling).  A zero scale runs as the smallest normal float: then
+  // every scaled score of magnitude below 2^100 is under 2^-26, and its
+  // probability rounds to exactly 1, as with a zero scale.
+  p->scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
   p->timeout_ns = kDefaultTimeoutNs;
   p->kv_splits = 1;
   p->kv_blocks_per_split = 1 << 30;
   p->fault_drop_block = -1;
+  p->n_m_tiles = (R + 255) / 256;
+  p->groups = B * H_kv;
+  p->num_tiles = p->n_m_tiles * p->groups;  // times the split count, set by the split-KV path
+  p->lpt_heads = (causal && S_q % 256 == 0) ? H_q / H_kv : 0;
   return ATTN_OK;
 }
 
 static int n_m_tiles_of(int H_q, int H_kv, int S_q) { return ((H_q / H_kv) * S_q + 255) / 256; }
+
+// Work tiles of a call with `splits` KV splits; the kernel indexes them with
+// an int.
+static bool tiles_fit(int B, int H_q, int H_kv, int S_q, int splits) {
+  return (int64_t)n_m_tiles_of(H_q, H_kv, S_q) * B * H_kv * splits < (1ll << 31);
+}
 
 static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
@@ -147,8 +164,7 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.trace_ctas = trace_ctas;
   p.trace_blocks = trace_blocks;
   p.fault_drop_block = fault_drop_block;
-  if (launch_attn_fwd(p, D, n_m_tiles_of(H_q, H_kv, S_q), static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  if (launch_attn_fwd(p, D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -210,16 +226,18 @@ attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o,
   AttnParams p;
   st = make_params(&p, q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
+  if (!tiles_fit(B, H_q, H_kv, S_q, splits)) return ATTN_ERR_UNSUPPORTED;
   const int kv_blocks = (S_kv + 127) / 128;
   p.kv_splits = splits;
   p.kv_blocks_per_split = (kv_blocks + splits - 1) / splits;
+  p.num_tiles = p.n_m_tiles * p.groups * splits;
   const size_t rows = (size_t)B * H_q * S_q;
   const size_t o_bytes = (size_t)splits * rows * D * sizeof(float);
   p.o_part = static_cast<float*>(workspace);
   p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         ((o_bytes + 255) & ~(size_t)255));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_attn_fwd(p, D, n_m_tiles_of(H_q, H_kv, S_q), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_attn_fwd(p, D, s) != cudaSuccess) return ATTN_ERR_CUDA;
   if (launch_splitkv_combine(p.o_part, p.lse_part, o, lse, (long long)rows, D, splits, s) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -10,15 +10,19 @@
 // softmax of two query sub-tiles runs in two warpgroups that ping-pong on the
 // tensor core, and the accumulator rescale runs in a third warpgroup.
 //
-// One CTA = one (batch, query head, 256-row query tile) = two 128-row
-// sub-tiles t = 0, 1.  512 threads:
+// The grid is persistent: at most one CTA per SM, each working through a list
+// of tiles (see AttnParams for the order).  A tile is 256 query rows of one
+// row group against one KV split, as two 128-row sub-tiles t = 0, 1.  Every
+// role keeps its barrier phases running from tile to tile, so the next
+// tile's loads and first GEMMs overlap the current tile's last blocks and its
+// epilogue.  512 threads:
 //   warps 0-3   softmax warpgroup for sub-tile 0 (thread = query row)
 //   warps 4-7   softmax warpgroup for sub-tile 1
 //   warps 8-11  correction warpgroup: rescales O_t in tensor memory when a
-//               row max moved, then the epilogue (O / l -> bf16 -> TMA
-//               store, LSE store)
+//               row max moved, then the epilogue (O / l -> bf16 -> global,
+//               LSE)
 //   warp  12    tensor-core issuer (one thread issues every tcgen05.mma)
-//   warp  13    TMA producer: Q_0, Q_1 once, then K_j, V_j through a ring
+//   warp  13    TMA producer: Q_0, Q_1 per tile, K_j, V_j through a ring
 //   warps 14-15 idle (they complete warpgroup 3 for setmaxnreg)
 //
 // Tensor memory (512 columns x 128 lanes, lane = query row of the sub-tile):
@@ -28,11 +32,21 @@
 // PV GEMM that reads P_t, by the same thread; tcgen05.mma operations issued
 // by one thread execute in issue order.
 //
+// Hand-offs between tiles:
+//   q_free[t]  the tile's last S_t GEMM has read Q_t: the producer may load
+//              the next tile's Q_t into the same buffer;
+//   p_full[t]  for block 0 of a tile, the correction's half of the arrivals
+//              means "the previous tile's O_t has been read out of tensor
+//              memory", so the first PV_t (which overwrites O_t) waits for it;
+//   fin[2][t]  the final row statistics, double-buffered by tile parity so a
+//              one-block tile cannot overwrite them before they are read.
+//
 // Every wait is bounded (see ptx.cuh); a timeout raises a CTA-wide abort
 // flag, every role unwinds to the teardown, and the device status word
 // records ATTN_ERR_TIMEOUT.  No trap, no assert.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <type_traits>
 
 #include "attn_internal.h"
@@ -60,23 +74,24 @@ static_assert((2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma) * 128 <= 65536
 
 template <int D>
 struct Cfg {
-  static constexpr int kHalves = TileShape<D>::kSlabs;  // 128-byte swizzle slabs across D
-  static constexpr int kHalfBytes = kSlabBytes;          // one [128 rows x 64 cols] bf16 slab
   static constexpr int kTileBytes = TileShape<D>::kBytes; // one 128-row tile of Q, K or V
-  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring depth
+  // K/V ring: kSlots tile slots grouped into kPairs stages.  Stage s holds
+  // one V tile in slot (2s - 1) mod kSlots and one K tile in slot 2s.
+  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kPairs = kSlots / 2;
   // shared memory, offsets from a 1024-byte aligned base
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  // kv_full[S], kv_empty[S], q_full[2], s_full[2], p_full[2], stats[2],
-  // pv_done[2], drain[1], fin[2]
-  static constexpr int kNumBars = 2 * kStages + 13;
-  static constexpr int kOffScale = kOffBar + kNumBars * 8;   // float [2][128]
-  static constexpr int kOffRowSum = kOffScale + 2 * 128 * 4;  // float [2][128], fp32 sum of p
-  static constexpr int kOffRowSumP = kOffRowSum + 2 * 128 * 4; // float [2][128], sum of bf16(p)
-  static constexpr int kOffRowMax = kOffRowSumP + 2 * 128 * 4; // float [2][128]
-  static constexpr int kOffMisc = kOffRowMax + 2 * 128 * 4;    // tmem base, abort flag
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + slack to align the base
+  static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
+  // kv_full[P], kv_empty[P], q_full[2], s_full[2], p_full[2], stats[2],
+  // pv_done[2], drain[1], fin[2][2], q_free[2]
+  static constexpr int kNumBars = 2 * kPairs + 17;
+  static constexpr int kOffScale = kOffBar + kNumBars * 8;      // float [2][128]: alpha per row
+  static constexpr int kOffRowSum = kOffScale + 2 * 128 * 4;    // float [2][2][128]: fp32 sum of p
+  static constexpr int kOffRowSumP = kOffRowSum + 4 * 128 * 4;  // float [2][2][128]: sum of bf16(p)
+  static constexpr int kOffRowMax = kOffRowSumP + 4 * 128 * 4;  // float [2][2][128]
+  static constexpr int kOffMisc = kOffRowMax + 4 * 128 * 4;     // tmem base, abort flag
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;       // + slack to align the base
   // tensor memory columns
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
@@ -100,6 +115,73 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+// One work tile.
+struct Tile {
+  int m0;         // first row of the tile within its row group
+  int zkv;        // row group = K/V head index b * H_kv + g
+  int split;      // KV split
+  int jb;         // first KV block the tile visits
+  int n_blocks;   // KV blocks it visits (<= 0: a split with no visible key)
+  bool has_sub1;  // rows m0 + 128 .. m0 + 255 exist in the row group
+};
+
+// Index of the k-th tile of this CTA, or -1 when it has no k-th tile: round
+// k covers list entries [k G, (k + 1) G), taken left to right in even rounds
+// and right to left in odd ones.
+__device__ __forceinline__ int tile_of(const AttnParams& p, int k) {
+  const long long G = gridDim.x;
+  const long long c = blockIdx.x;
+  const long long idx = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+  return idx < (long long)p.num_tiles ? (int)idx : -1;
+}
+
+__device__ __forceinline__ Tile decode_tile(const AttnParams& p, int ti) {
+  const int S = p.kv_splits;
+  int m, zkv, split;
+  if (p.causal) {
+    // cost rank first (longest tiles first), then group, then split
+    const int per_rank = p.groups * S;
+    const int rank = ti / per_rank;
+    const int rr = ti - rank * per_rank;
+    zkv = rr / S;
+    split = rr - zkv * S;
+    if (p.lpt_heads > 0) {
+      const int nh = p.S_q >> 8;  // query tiles per head
+      m = (rank % p.lpt_heads) * nh + (nh - 1 - rank / p.lpt_heads);
+    } else {
+      m = p.n_m_tiles - 1 - rank;
+    }
+  } else {
+    // group-major, query tiles last to first, then split
+    const int per_group = p.n_m_tiles * S;
+    zkv = ti / per_group;
+    const int rr = ti - zkv * per_group;
+    const int mr = rr / S;
+    m = p.n_m_tiles - 1 - mr;
+    split = rr - mr * S;
+  }
+  Tile t;
+  t.m0 = m * (2 * kBlockM);
+  t.zkv = zkv;
+  t.split = split;
+  // keys any row of this tile may see: row rho is query position rho % S_q,
+  // and with the causal mask it sees keys <= its position
+  const int R = p.rows_per_group;
+  int kv_end = p.S_kv;
+  if (p.causal) {
+    const int last = min(t.m0 + 2 * kBlockM, R) - 1;
+    kv_end = min(p.S_kv, (t.m0 / p.S_q == last / p.S_q) ? last % p.S_q + 1 : p.S_q);
+  }
+  const int n_total = (kv_end + kBlockN - 1) / kBlockN;
+  t.jb = split * p.kv_blocks_per_split;
+  t.n_blocks = min(n_total - t.jb, p.kv_blocks_per_split);
+  // sub-tile 1 holds rows m0 + 128 .. m0 + 255; when none of them exists
+  // (short row groups, e.g. one decoding token per head, or a ragged last
+  // tile) every role skips it and the tile costs half
+  t.has_sub1 = (t.m0 + kBlockM) < R;
+  return t;
+}
+
 }  // namespace
 
 template <int D, bool kTrace>
@@ -112,14 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint8_t* sKV = smem + C::kOffKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + C::kStages;
-  uint64_t* q_full = bars + 2 * C::kStages;
+  uint64_t* kv_empty = bars + C::kPairs;
+  uint64_t* q_full = bars + 2 * C::kPairs;
   uint64_t* s_full = q_full + 2;
   uint64_t* p_full = q_full + 4;
   uint64_t* stats = q_full + 6;
   uint64_t* pv_done = q_full + 8;
   uint64_t* drain = q_full + 10;
-  uint64_t* fin = q_full + 11;
+  uint64_t* fin = q_full + 11;     // [buffer][sub-tile]
+  uint64_t* q_free = q_full + 15;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
   float* sRowSum = reinterpret_cast<float*>(smem + C::kOffRowSum);
   float* sRowSumP = reinterpret_cast<float*>(smem + C::kOffRowSumP);
@@ -129,74 +212,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // grid = (query tiles x KV splits, H_kv, B).  A CTA works on 256 rows of
-  // one row group (the query heads sharing KV head g of batch b, see
-  // AttnParams); the tiles of one group are adjacent in launch order, so the
-  // CTAs resident at once share few K/V heads in L2, and within a group the
-  // longest causal tiles launch first.
-  const int R = p.rows_per_group;
-  const int split = blockIdx.x % p.kv_splits;
-  const int m0 = ((int)(gridDim.x / p.kv_splits) - 1 - (int)(blockIdx.x / p.kv_splits)) * (2 * kBlockM);
-  const int b = blockIdx.z;
-  const int zkv = b * p.H_kv + blockIdx.y;  // row group = K/V head index
-  // keys any row of this tile may see: row rho is query position rho % S_q,
-  // and with the causal mask it sees keys <= its position
-  int kv_end = p.S_kv;
-  if (p.causal) {
-    const int last = min(m0 + 2 * kBlockM, R) - 1;
-    kv_end = min(p.S_kv, (m0 / p.S_q == last / p.S_q) ? last % p.S_q + 1 : p.S_q);
-  }
-  const int n_total = (kv_end + kBlockN - 1) / kBlockN;
-  // sub-tile 1 holds rows m0 + 128 .. m0 + 255; when none of them exists
-  // (short row groups, e.g. one decoding token per head, or a ragged last
-  // tile) every role skips it and the tile costs half
-  const bool has_sub1 = (m0 + kBlockM) < R;
-  const int jb = split * p.kv_blocks_per_split;  // first KV block of this CTA
-  const int n_blocks = min(n_total - jb, p.kv_blocks_per_split);
-  if (n_blocks <= 0) {
-    // split-KV only: no key of this split is visible to any row of the tile,
-    // so its partial result is empty (weight 0 in the merge)
-    for (int idx = threadIdx.x; idx < 2 * kBlockM; idx += kThreads) {
-      const int rho = m0 + idx;
-      if (rho < R) {
-        const size_t row = (size_t)split * p.total_rows + (size_t)zkv * R + rho;
-        p.lse_part[row] = -INFINITY;
-        float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
-        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    return;
-  }
   const uint64_t budget = p.timeout_ns;
-  // trace stamps (compiled only into the trace instantiation)
-  const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  const bool traced = kTrace && cta_lin < p.trace_ctas;
-  // The stamp is the SM cycle counter; a slot written by several warps keeps
-  // the latest stamp (a barrier completes when its last warp arrives).
-  auto stamp = [&](int ev, int j) {
+  // trace stamps (compiled only into the trace instantiation): the first
+  // tile of CTAs below trace_ctas.  The stamp is the SM cycle counter; a slot
+  // written by several warps keeps the latest stamp (a barrier completes
+  // when its last warp arrives).
+  const bool trace_cta = kTrace && (int)blockIdx.x < p.trace_ctas;
+  auto stamp = [&](bool on, int ev, int j) {
     if constexpr (kTrace) {
-      if (traced && j < p.trace_blocks)
-        atomicMax(&p.trace[((size_t)cta_lin * kNumTraceEvents + ev) * p.trace_blocks + j],
+      if (on && j < p.trace_blocks)
+        atomicMax(&p.trace[((size_t)blockIdx.x * kNumTraceEvents + ev) * p.trace_blocks + j],
                   (unsigned long long)clock64());
     }
   };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < C::kPairs; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&q_full[t], 1);
+      mbar_init(&q_free[t], 1);
       mbar_init(&s_full[t], 1);
       // p_full[t]: P_t(j) stored by the softmax (128 arrivals) and O_t
-      // rescaled for block j by the correction warpgroup (128 arrivals)
+      // rescaled for block j, or for block 0 read out of the previous tile,
+      // by the correction warpgroup (128 arrivals)
       mbar_init(&p_full[t], 2 * kBlockM);
       // stats[t]: one phase per block j >= 1 (the rescale factor alpha);
-      // fin[t]: one phase, the final row sums and max.  Keeping them apart
-      // means a waiter is never two phases behind on either barrier.
+      // fin[.][t]: one phase per tile, the final row sums and max.  Keeping
+      // them apart, and fin double-buffered, means no waiter is ever two
+      // phases behind.
       mbar_init(&stats[t], kBlockM);
       mbar_init(&fin[t], kBlockM);
+      mbar_init(&fin[2 + t], kBlockM);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -207,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tma_prefetch_map(&p.tm_q);
     tma_prefetch_map(&p.tm_k);
     tma_prefetch_map(&p.tm_v);
-    tma_prefetch_map(&p.tm_o);
   }
   if (warp == 12) {
     tmem_alloc(sTmemBase, C::kTmemCols);
@@ -218,134 +266,148 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after_sync();
   const uint32_t tmem = *sTmemBase;
   const int wg = warp >> 2;
+  const int R = p.rows_per_group;
 
   if (wg < 2) {
     // ------------------------------------------------------------ softmax
-    // (warpgroup 1 has nothing to do when the tile has no sub-tile 1)
-    if (wg == 0 || has_sub1) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsSoftmax) : "memory");
     const int t = wg;
     const int r = (warp & 3) * 32 + lane;                 // row within the sub-tile
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::kTmS1 : C::kTmS0);
-    const int rho = m0 + t * kBlockM + r;                  // row in the row group
-    const int pos = rho % p.S_q;                           // its query position
-    // smallest query position in this sub-tile (0 if it spans two heads)
-    const int sub_first = m0 + t * kBlockM;
-    const int min_pos = (sub_first / p.S_q == (sub_first + kBlockM - 1) / p.S_q) ? sub_first % p.S_q : 0;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
-    // Two row sums: l_run of the fp32 probabilities (for the LSE), and lp_run
-    // of the bf16-rounded probabilities that the PV GEMM actually consumes,
-    // so O is normalised by the same weights it was accumulated with.
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    float lp_run = 0.f;
+    uint32_t nblk = 0;  // blocks of sub-tile t so far: the phase of s_full[t]
+    uint32_t ntl = 0;   // tiles with sub-tile t so far: row-stat buffer, fin phase
     bool ok = true;
-    for (int j = 0; j < n_blocks; ++j) {
-      if (!warp_wait(&s_full[t], j & 1, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
-      if (lane == 0) stamp(t ? kEvSm1Wake : kEvSm0Wake, j);
-      uint32_t s[128];
-      {
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
-        uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-        tmem_ld_x32(tS + 0, s0);
-        tmem_ld_x32(tS + 32, s1);
-        tmem_ld_x32(tS + 64, s2);
-        tmem_ld_x32(tS + 96, s3);
-        tmem_ld_wait();
-        reg_after_wait(s0);
-        reg_after_wait(s1);
-        reg_after_wait(s2);
-        reg_after_wait(s3);
-      }
-      if (lane == 0) stamp(t ? kEvSm1Loaded : kEvSm0Loaded, j);
-      const int kv0 = (jb + j) * kBlockN;
-      const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > min_pos);
-      const int lim = key_limit - kv0;  // columns c < lim are visible to this row
-      float m_use = m_run;
-      float alpha = 1.f;
-      uint64_t l2[2] = {0, 0};                  // packed fp32 partial sums of p
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};       // partial sums of bf16(p)
-      // The unmasked and masked bodies are separate code paths so the common
-      // (unmasked) one carries no per-element predication.
-      auto body = [&](auto masked_tag) {
-        constexpr bool kMasked = decltype(masked_tag)::value;
-        if constexpr (kMasked) {
-          // keys this row may not see drop out of the max
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) s[c] = f2u(-INFINITY);
+    for (int k = 0; ok; ++k) {
+      const int ti = tile_of(p, k);
+      if (ti < 0) break;
+      const Tile tl = decode_tile(p, ti);
+      // (warpgroup 1 has nothing to do when the tile has no sub-tile 1)
+      if (tl.n_blocks <= 0 || (t == 1 && !tl.has_sub1)) continue;
+      const bool tr = trace_cta && k == 0 && lane == 0;
+      const int rho = tl.m0 + t * kBlockM + r;               // row in the row group
+      const int pos = rho % p.S_q;                           // its query position
+      // smallest query position in this sub-tile (0 if it spans two heads)
+      const int sub_first = tl.m0 + t * kBlockM;
+      const int min_pos =
+          (sub_first / p.S_q == (sub_first + kBlockM - 1) / p.S_q) ? sub_first % p.S_q : 0;
+      const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
+      // Two row sums: l_run of the fp32 probabilities (for the LSE), and
+      // lp_run of the bf16-rounded probabilities that the PV GEMM actually
+      // consumes, so O is normalised by the same weights it was accumulated
+      // with.
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      float lp_run = 0.f;
+      for (int j = 0; j < tl.n_blocks; ++j) {
+        if (!warp_wait(&s_full[t], nblk & 1, sAbort, budget)) { ok = false; break; }
+        ++nblk;
+        tc_fence_after_sync();
+        stamp(tr, t ? kEvSm1Wake : kEvSm0Wake, j);
+        uint32_t s[128];
+        {
+          uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+          uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+          uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+          uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+          tmem_ld_x32(tS + 0, s0);
+          tmem_ld_x32(tS + 32, s1);
+          tmem_ld_x32(tS + 64, s2);
+          tmem_ld_x32(tS + 96, s3);
+          tmem_ld_wait();
+          reg_after_wait(s0);
+          reg_after_wait(s1);
+          reg_after_wait(s2);
+          reg_after_wait(s3);
         }
-        // row max of the raw scores (4 independent chains of 3-input max)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        stamp(tr, t ? kEvSm1Loaded : kEvSm0Loaded, j);
+        const int kv0 = (tl.jb + j) * kBlockN;
+        const bool masked = (kv0 + kBlockN > p.S_kv) || (p.causal && kv0 + kBlockN - 1 > min_pos);
+        const int lim = key_limit - kv0;  // columns c < lim are visible to this row
+        float m_use = m_run;
+        float alpha = 1.f;
+        uint64_t l2[2] = {0, 0};                  // packed fp32 partial sums of p
+        float lp[4] = {0.f, 0.f, 0.f, 0.f};       // partial sums of bf16(p)
+        // The unmasked and masked bodies are separate code paths so the
+        // common (unmasked) one carries no per-element predication.
+        auto body = [&](auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
+          if constexpr (kMasked) {
+            // keys this row may not see drop out of the max
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
-        }
-        const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        // scale >= 0, so the max of the scaled scores is the scaled max; a row
-        // whose keys are all masked here leaves the running max unchanged
-        const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
-        if (j == 0) {
-          m_use = m_new;
-        } else if (m_new - m_run > kRescaleThreshold) {
-          m_use = m_new;
-          alpha = ex2_approx(m_run - m_new);
-        }
-        if (j > 0) {
-          sScale[t * kBlockM + r] = alpha;
-          mbar_arrive(&stats[t]);
-        }
-        const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int c = ch * 16 + 2 * i;
-            // x = s * scale * log2(e) - m, two lanes per instruction
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            if constexpr (kMasked) {  // (also covers scale = 0, where -inf * 0 is NaN)
-              p0 = (c < lim) ? p0 : 0.f;
-              p1 = (c + 1 < lim) ? p1 : 0.f;
-            }
-            l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
-            add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) s[c] = f2u(-INFINITY);
           }
-          tmem_st_x8(tS + ch * 8, pk);
-        }
-      };
-      if (masked)
-        body(std::true_type{});
-      else
-        body(std::false_type{});
-      float la, lb;
-      f2_unpack(f2_add(l2[0], l2[1]), la, lb);
-      l_run = l_run * alpha + (la + lb);
-      lp_run = lp_run * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
-      tmem_st_wait();
-      tc_fence_before_sync();
-      if (lane == 0) stamp(t ? kEvSm1Done : kEvSm0Done, j);
-      bool signal = true;
-      if constexpr (kTrace) signal = !(t == 0 && j == p.fault_drop_block);
-      if (signal) mbar_arrive(&p_full[t]);
-      m_run = m_use;
-    }
-    if (ok) {
-      sRowSum[t * kBlockM + r] = l_run;
-      sRowSumP[t * kBlockM + r] = lp_run;
-      sRowMax[t * kBlockM + r] = m_run;
-      mbar_arrive(&fin[t]);
-    }
+          // row max of the raw scores (4 independent chains of 3-input max)
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
+          }
+          const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          // scale >= 0, so the max of the scaled scores is the scaled max; a
+          // row whose keys are all masked here leaves the running max unchanged
+          const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
+          if (j == 0) {
+            m_use = m_new;
+          } else if (m_new - m_run > kRescaleThreshold) {
+            m_use = m_new;
+            alpha = ex2_approx(m_run - m_new);
+          }
+          if (j > 0) {
+            sScale[t * kBlockM + r] = alpha;
+            mbar_arrive(&stats[t]);
+          }
+          // A masked score is -inf, and so is its x below (scale_log2 > 0),
+          // so its p is exactly 0 -- unless the row has seen no key yet
+          // (m_use = -inf, only possible inside one KV split): then subtract
+          // 0 instead, which keeps x = -inf rather than -inf + inf.
+          float m_sub = m_use;
+          if constexpr (kMasked) m_sub = (m_use == -INFINITY) ? 0.f : m_use;
+          const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int c = ch * 16 + 2 * i;
+              // x = s * scale * log2(e) - m, two lanes per instruction
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+              add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);
+            }
+            tmem_st_x8(tS + ch * 8, pk);
+          }
+        };
+        if (masked)
+          body(std::true_type{});
+        else
+          body(std::false_type{});
+        float la, lb;
+        f2_unpack(f2_add(l2[0], l2[1]), la, lb);
+        l_run = l_run * alpha + (la + lb);
+        lp_run = lp_run * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        stamp(tr, t ? kEvSm1Done : kEvSm0Done, j);
+        bool signal = true;
+        if constexpr (kTrace) signal = !(t == 0 && j == p.fault_drop_block);
+        if (signal) mbar_arrive(&p_full[t]);
+        m_run = m_use;
+      }
+      if (!ok) break;
+      const int sb = ((ntl & 1) * 2 + t) * kBlockM + r;  // row-stat slot [buffer][sub-tile][row]
+      sRowSum[sb] = l_run;
+      sRowSumP[sb] = lp_run;
+      sRowMax[sb] = m_run;
+      mbar_arrive(&fin[(ntl & 1) * 2 + t]);
+      ++ntl;
     }
   } else if (wg == 2) {
     // ------------------------------------------------------------ correction + epilogue
@@ -353,184 +415,248 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    uint32_t nst[2] = {0, 0};  // alpha phases consumed, per sub-tile (stats[t])
+    uint32_t ntl[2] = {0, 0};  // tiles finished, per sub-tile (fin, pv_done)
     bool ok = true;
-    // Block 0 needs no rescale.  For block j >= 1 the softmax's alpha arrives
-    // on stats[t]; it is published after the softmax saw S_t(j), whose commit
-    // follows PV_t(j-1), so O_t already holds every earlier block.
-    const int n_sub = has_sub1 ? 2 : 1;
-    mbar_arrive(&p_full[0]);
-    if (has_sub1) mbar_arrive(&p_full[1]);
-    for (int j = 1; j < n_blocks && ok; ++j) {
-      for (int t = 0; t < n_sub; ++t) {
-        if (!warp_wait(&stats[t], (j - 1) & 1, sAbort, budget)) { ok = false; break; }
-        const float alpha = sScale[t * kBlockM + r];
-        tc_fence_after_sync();
-        if (__any_sync(kFull, alpha != 1.f)) {
-          const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + ch * 32, o);
-            tmem_ld_wait();
-            reg_after_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st_x32(tO + ch * 32, o);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before_sync();
-        if (lane == 0) stamp(t ? kEvCorr1 : kEvCorr0, j);
-        mbar_arrive(&p_full[t]);
-      }
-    }
-    for (int t = 0; t < n_sub && ok; ++t) {
-      if (!warp_wait(&fin[t], 0, sAbort, budget)) { ok = false; break; }
-      if (!warp_wait(&pv_done[t], 0, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
-      if (lane == 0) stamp(kEvEpilogue, t);
-      const float l = sRowSum[t * kBlockM + r];
-      const float m = sRowMax[t * kBlockM + r];
-      const float lp = sRowSumP[t * kBlockM + r];
-      // a row with no visible key (possible only within one KV split) has
-      // l = 0: its partial result is O = 0, LSE = -inf
-      const bool empty = !(lp > 0.f);
-      const float inv_l = empty ? 0.f : 1.f / lp;
-      const float lse_row = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
-      const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
-      const int rho = m0 + t * kBlockM + r;
-      if (p.o_part != nullptr) {
-        // split-KV partial: fp32 O normalised within the split, and its LSE.
-        // The tensor-memory loads are warp-wide; only the stores depend on
-        // whether the row exists.
-        const size_t row = (size_t)split * p.total_rows + (size_t)zkv * R + rho;
-        float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld_x32(tO + ch * 32, o);
-          tmem_ld_wait();
-          reg_after_wait(o);
+    // Advances k to the next tile with work and decodes it; a split tile
+    // with no visible key on the way gets its empty partial result here
+    // (weight 0 in the merge).
+    auto next_work = [&](int& k, Tile& tl) -> bool {
+      for (;; ++k) {
+        const int ti = tile_of(p, k);
+        if (ti < 0) return false;
+        tl = decode_tile(p, ti);
+        if (tl.n_blocks > 0) return true;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int rho = tl.m0 + h * kBlockM + r;
           if (rho < R) {
-#pragma unroll
-            for (int qd = 0; qd < 8; ++qd)
-              dst[ch * 8 + qd] = make_float4(u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
-                                             u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
+            const size_t row = (size_t)tl.split * p.total_rows + (size_t)tl.zkv * R + rho;
+            p.lse_part[row] = -INFINITY;
+            float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
+            for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
-        if (rho < R) p.lse_part[row] = lse_row;
-        continue;
       }
-      uint8_t* stage = sQ + t * C::kTileBytes;  // Q_t is no longer read: reuse it
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + ch * 32, o);
-        tmem_ld_wait();
-        reg_after_wait(o);
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-          const int c16 = ch * 4 + qd;     // 16-byte chunk index along the row
-          const int half = c16 >> 3;
-          const int cc = c16 & 7;
-          uint4 val;
-          val.x = pack_bf16x2(u2f(o[qd * 8 + 0]) * inv_l, u2f(o[qd * 8 + 1]) * inv_l);
-          val.y = pack_bf16x2(u2f(o[qd * 8 + 2]) * inv_l, u2f(o[qd * 8 + 3]) * inv_l);
-          val.z = pack_bf16x2(u2f(o[qd * 8 + 4]) * inv_l, u2f(o[qd * 8 + 5]) * inv_l);
-          val.w = pack_bf16x2(u2f(o[qd * 8 + 6]) * inv_l, u2f(o[qd * 8 + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(stage + half * C::kHalfBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = val;
-        }
-      }
-      if (rho < R) p.lse[(size_t)zkv * R + rho] = lse_row;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_store_3d(&p.tm_o, stage + hf * C::kHalfBytes + q4 * 32 * 128, hf * 64,
-                       m0 + t * kBlockM + q4 * 32, zkv);
-        }
-        tma_store_commit();
-      }
-      __syncwarp();
+    };
+    int k = 0;
+    Tile cur;
+    bool have = next_work(k, cur);
+    // block 0 of the first tile needs nothing from this warpgroup
+    if (have) {
+      mbar_arrive(&p_full[0]);
+      if (cur.has_sub1) mbar_arrive(&p_full[1]);
     }
-    if (lane == 0) tma_store_wait_all();
-    __syncwarp();
+    while (have) {
+      const int n_sub = cur.has_sub1 ? 2 : 1;
+      const bool tr = trace_cta && k == 0 && lane == 0;
+      // Block j >= 1: the softmax's alpha arrives on stats[t]; it is
+      // published after the softmax saw S_t(j), whose commit follows
+      // PV_t(j-1), so O_t already holds every earlier block.
+      for (int j = 1; j < cur.n_blocks && ok; ++j) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= n_sub) break;
+          if (!warp_wait(&stats[t], nst[t] & 1, sAbort, budget)) { ok = false; break; }
+          ++nst[t];
+          const float alpha = sScale[t * kBlockM + r];
+          tc_fence_after_sync();
+          if (__any_sync(kFull, alpha != 1.f)) {
+            const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + ch * 32, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+              tmem_st_x32(tO + ch * 32, o);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before_sync();
+          stamp(tr, t ? kEvCorr1 : kEvCorr0, j);
+          mbar_arrive(&p_full[t]);
+        }
+      }
+      if (!ok) break;
+      int k_next = k + 1;
+      Tile nxt;
+      const bool have_next = next_work(k_next, nxt);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t < n_sub) {
+          const int buf = (int)(ntl[t] & 1);
+          if (!warp_wait(&fin[buf * 2 + t], (ntl[t] >> 1) & 1, sAbort, budget)) { ok = false; break; }
+          if (!warp_wait(&pv_done[t], ntl[t] & 1, sAbort, budget)) { ok = false; break; }
+          ++ntl[t];
+          tc_fence_after_sync();
+          stamp(tr, kEvEpilogue, t);
+          const int sb = (buf * 2 + t) * kBlockM + r;
+          const float l = sRowSum[sb];
+          const float m = sRowMax[sb];
+          const float lp = sRowSumP[sb];
+          // a row with no visible key (possible only within one KV split)
+          // has l = 0: its partial result is O = 0, LSE = -inf
+          const bool empty = !(lp > 0.f);
+          const float inv_l = empty ? 0.f : 1.f / lp;
+          const float lse_row = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+          const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
+          const int rho = cur.m0 + t * kBlockM + r;
+          // The tensor-memory loads are warp-wide; only the stores depend on
+          // whether the row exists.
+          if (p.o_part != nullptr) {
+            // split-KV partial: fp32 O normalised within the split, and its LSE
+            const size_t row = (size_t)cur.split * p.total_rows + (size_t)cur.zkv * R + rho;
+            float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + ch * 32, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+              if (rho < R) {
+#pragma unroll
+                for (int qd = 0; qd < 8; ++qd)
+                  dst[ch * 8 + qd] =
+                      make_float4(u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
+                                  u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
+              }
+            }
+            if (rho < R) p.lse_part[row] = lse_row;
+          } else {
+            // bf16 O straight from registers: each thread writes its own row
+            // in 16-byte pieces
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                  ((size_t)cur.zkv * R + rho) * D);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + ch * 32, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+              if (rho < R) {
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                  uint4 val;
+                  val.x = pack_bf16x2(u2f(o[qd * 8 + 0]) * inv_l, u2f(o[qd * 8 + 1]) * inv_l);
+                  val.y = pack_bf16x2(u2f(o[qd * 8 + 2]) * inv_l, u2f(o[qd * 8 + 3]) * inv_l);
+                  val.z = pack_bf16x2(u2f(o[qd * 8 + 4]) * inv_l, u2f(o[qd * 8 + 5]) * inv_l);
+                  val.w = pack_bf16x2(u2f(o[qd * 8 + 6]) * inv_l, u2f(o[qd * 8 + 7]) * inv_l);
+                  dst[ch * 4 + qd] = val;
+                }
+              }
+            }
+            if (rho < R) p.lse[(size_t)cur.zkv * R + rho] = lse_row;
+          }
+          tc_fence_before_sync();
+        }
+        // O_t has been read out and the row statistics are consumed: block 0
+        // of the next tile may start on sub-tile t
+        if (have_next && (t == 0 || nxt.has_sub1)) mbar_arrive(&p_full[t]);
+      }
+      if (!ok) break;
+      stamp(tr && q4 == 0, kEvEnd, 0);
+      k = k_next;
+      cur = nxt;
+      have = have_next;
+    }
   } else {
     // ------------------------------------------------------------ warpgroup 3
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLoadMma) : "memory");
     if (warp == 12 && lane == 0) {
       // tensor-core issuer: one thread, no warp-wide votes, so it needs as
       // few issue slots as possible next to the busy softmax warps
-      const uint64_t dq0 = kmajor_tile_desc(smem_u32(sQ));
-      const uint64_t dq1 = kmajor_tile_desc(smem_u32(sQ + C::kTileBytes));
+      const uint64_t dq[2] = {kmajor_tile_desc(smem_u32(sQ)),
+                              kmajor_tile_desc(smem_u32(sQ + C::kTileBytes))};
       const uint64_t dk0 = kmajor_tile_desc(smem_u32(sKV));
       const uint64_t dv0 = mnmajor_tile_desc<D>(smem_u32(sKV));
-      constexpr uint64_t kStageDesc = C::kTileBytes >> 4;  // start-address step per ring stage
-      const uint32_t tS0 = tmem + C::kTmS0, tS1 = tmem + C::kTmS1;
-      const uint32_t tO0 = tmem + C::kTmO0, tO1 = tmem + C::kTmO1;
-      do {
-        if (!mbar_wait(&kv_full[0], 0, sAbort, budget)) break;
-        if (!mbar_wait(&q_full[0], 0, sAbort, budget)) break;
-        tc_fence_after_sync();
-        issue_qk_gemm<D>(tS0, dq0, dk0);
-        tc_commit(&s_full[0]);
-        stamp(kEvMmaS0, 0);
-        if (has_sub1) {
-          if (!mbar_wait(&q_full[1], 0, sAbort, budget)) break;
-          tc_fence_after_sync();
-          issue_qk_gemm<D>(tS1, dq1, dk0);
-          tc_commit(&s_full[1]);
-          stamp(kEvMmaS1, 0);
+      constexpr uint64_t kSlotDesc = C::kTileBytes >> 4;  // start-address step per ring slot
+      const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
+      const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
+      // The CTA's KV blocks form one stream over its tiles, b = 0, 1, ...
+      // Ring entry 0 holds K of stream block 0; entry e >= 1 holds V of block
+      // e - 1 and K of block e (if any), both used in the iteration of block
+      // e - 1: one wait and one release per block.  The entry holding a
+      // tile's first K is released once that tile's first S GEMMs are issued.
+      uint32_t e_next = 0;       // next ring entry to wait for
+      uint32_t nq[2] = {0, 0};   // tiles so far per sub-tile: the phase of q_full[t]
+      uint32_t nb[2] = {0, 0};   // blocks so far per sub-tile: the phase of p_full[t]
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int ti = tile_of(p, k);
+        if (ti < 0) break;
+        const Tile tl = decode_tile(p, ti);
+        const int n = tl.n_blocks;
+        if (n <= 0) continue;
+        const bool tr = trace_cta && k == 0;
+        const int n_sub = tl.has_sub1 ? 2 : 1;
+        // S_t(0) = Q_t K_0^T.  K_0 sits in entry e_next - 1, already waited
+        // for in the previous tile's last iteration (entry 0 for the first).
+        if (e_next == 0) {
+          if (!mbar_wait(&kv_full[0], 0, sAbort, budget)) { ok = false; break; }
+          e_next = 1;
         }
-        tc_commit(&kv_empty[0]);
-        int sv = 1 % C::kStages, sk = 2 % C::kStages;   // ring stages of V_j and K_{j+1}
-        for (int j = 0; j < n_blocks; ++j) {
-          const bool more = (j + 1) < n_blocks;
-          // V_j lives in ring slot 2j+1, K_{j+1} in slot 2j+2.  Both loads were
-          // issued long before; waiting for them here, while the softmax is
-          // still busy, keeps them off the path from "P ready" to the GEMMs.
-          const uint32_t v_par = ((2 * j + 1) / C::kStages) & 1;
-          const uint32_t k_par = ((2 * j + 2) / C::kStages) & 1;
-          if (!mbar_wait(&kv_full[sv], v_par, sAbort, budget)) break;
-          if (more && !mbar_wait(&kv_full[sk], k_par, sAbort, budget)) break;
-          const uint64_t dv = dv0 + (uint64_t)sv * kStageDesc;
-          const uint64_t dk = dk0 + (uint64_t)sk * kStageDesc;
-          // sub-tile 0: O_0 += P_0 V_j, then S_0 = Q_0 K_{j+1}^T
-          if (!mbar_wait(&p_full[0], j & 1, sAbort, budget)) break;
+        const uint32_t s_k0 = (e_next - 1) % C::kPairs;
+        const uint64_t dk_first = dk0 + (uint64_t)(2 * s_k0) * kSlotDesc;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= n_sub) break;
+          if (!mbar_wait(&q_full[t], nq[t] & 1, sAbort, budget)) { ok = false; break; }
           tc_fence_after_sync();
-          stamp(kEvMmaPV0Begin, j);
-          issue_pv_gemm<D>(tO0, tS0, dv, j > 0);
-          if (!more) tc_commit(&pv_done[0]);  // the epilogue waits for the last PV only
-          stamp(kEvMmaPV0, j);
-          if (more) {
-            stamp(kEvMmaS0Begin, j + 1);
-            issue_qk_gemm<D>(tS0, dq0, dk);
-            tc_commit(&s_full[0]);
-            stamp(kEvMmaS0, j + 1);
+          issue_qk_gemm<D>(tS[t], dq[t], dk_first);
+          tc_commit(&s_full[t]);
+          if (n == 1) tc_commit(&q_free[t]);  // the tile's last read of Q_t
+          stamp(tr, t ? kEvMmaS1 : kEvMmaS0, 0);
+        }
+        if (!ok) break;
+        tc_commit(&kv_empty[s_k0]);
+        for (int j = 0; j < n; ++j) {
+          const bool more = (j + 1) < n;
+          // entry e_next: V_j and the next K (K_{j+1}, or the next tile's
+          // K_0).  Its loads were issued long before; waiting here, while the
+          // softmax is still busy, keeps it off the path from "P ready" to
+          // the GEMMs.
+          const uint32_t st = e_next % C::kPairs;
+          if (!mbar_wait(&kv_full[st], (e_next / C::kPairs) & 1, sAbort, budget)) {
+            ok = false;
+            break;
           }
-          // sub-tile 1: O_1 += P_1 V_j, then S_1 = Q_1 K_{j+1}^T
-          if (has_sub1) {
-            if (!mbar_wait(&p_full[1], j & 1, sAbort, budget)) break;
+          ++e_next;
+          const uint64_t dv = dv0 + (uint64_t)((2 * st + C::kSlots - 1) % C::kSlots) * kSlotDesc;
+          const uint64_t dk = dk0 + (uint64_t)(2 * st) * kSlotDesc;
+          // per sub-tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}^T
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= n_sub) break;
+            if (!mbar_wait(&p_full[t], (nb[t] + j) & 1, sAbort, budget)) { ok = false; break; }
             tc_fence_after_sync();
-            stamp(kEvMmaPV1Begin, j);
-            issue_pv_gemm<D>(tO1, tS1, dv, j > 0);
-            if (!more) tc_commit(&pv_done[1]);
-            stamp(kEvMmaPV1, j);
+            stamp(tr, t ? kEvMmaPV1Begin : kEvMmaPV0Begin, j);
+            issue_pv_gemm<D>(tO[t], tS[t], dv, j > 0);
+            if (!more) tc_commit(&pv_done[t]);  // the epilogue waits for the last PV only
+            stamp(tr, t ? kEvMmaPV1 : kEvMmaPV0, j);
             if (more) {
-              stamp(kEvMmaS1Begin, j + 1);
-              issue_qk_gemm<D>(tS1, dq1, dk);
-              tc_commit(&s_full[1]);
-              stamp(kEvMmaS1, j + 1);
+              stamp(tr, t ? kEvMmaS1Begin : kEvMmaS0Begin, j + 1);
+              issue_qk_gemm<D>(tS[t], dq[t], dk);
+              tc_commit(&s_full[t]);
+              if (j + 2 == n) tc_commit(&q_free[t]);
+              stamp(tr, t ? kEvMmaS1 : kEvMmaS0, j + 1);
             }
           }
-          // release the ring slots last: off the critical path
-          tc_commit(&kv_empty[sv]);
-          if (more) tc_commit(&kv_empty[sk]);
-          sv = (sv + 2) % C::kStages;
-          sk = (sk + 2) % C::kStages;
+          if (!ok) break;
+          // release the entry last, off the critical path (after the last
+          // block its K belongs to the next tile: released there)
+          if (more) tc_commit(&kv_empty[st]);
         }
-      } while (0);
+        if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= n_sub) break;
+          ++nq[t];
+          nb[t] += n;
+        }
+      }
       // let every tensor-core op this thread issued finish before teardown
       tc_commit(drain);
       drain_wait(drain, 0, budget);
@@ -538,29 +664,76 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // TMA producer (one thread)
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      for (int t = 0; t < (has_sub1 ? 2 : 1); ++t) {
-        mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
-        tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], m0 + t * kBlockM, zkv, pol_q);
+      uint32_t e = 0;            // ring entries issued so far
+      uint32_t nq[2] = {0, 0};   // Q_t loads issued so far
+      // V tile owed to the next entry: row group (-1: none), first key, and
+      // for the trace its block index and whether its tile is traced
+      int v_zkv = -1, v_row = 0, v_j = 0;
+      bool v_tr = false;
+      // Issues ring entry e: the owed V tile, if any, and K rows k_row.. of
+      // group k_zkv, if k_zkv >= 0 (see the tensor-core issuer for the layout).
+      auto issue_entry = [&](int k_zkv, int k_row) -> bool {
+        const uint32_t st = e % C::kPairs;
+        const uint32_t round = e / C::kPairs;
+        if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, sAbort, budget)) return false;
+        const uint32_t bytes = (v_zkv >= 0 ? C::kTileBytes : 0) + (k_zkv >= 0 ? C::kTileBytes : 0);
+        mbar_arrive_expect_tx(&kv_full[st], bytes);
+        if (v_zkv >= 0) {
+          tma_load_tile<D>(sKV + ((2 * st + C::kSlots - 1) % C::kSlots) * C::kTileBytes, &p.tm_v,
+                           &kv_full[st], v_row, v_zkv, pol_kv);
+          stamp(v_tr, kEvLoadV, v_j);
+        }
+        if (k_zkv >= 0)
+          tma_load_tile<D>(sKV + 2 * st * C::kTileBytes, &p.tm_k, &kv_full[st], k_row, k_zkv,
+                           pol_kv);
+        ++e;
+        return true;
+      };
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int ti = tile_of(p, k);
+        if (ti < 0) break;
+        const Tile tl = decode_tile(p, ti);
+        if (tl.n_blocks <= 0) continue;
+        const bool tr = trace_cta && k == 0;
+        for (int j = 0; j < tl.n_blocks; ++j) {
+          const int row = (tl.jb + j) * kBlockN;
+          if (!issue_entry(tl.zkv, row)) { ok = false; break; }
+          stamp(tr, kEvLoadK, j);
+          v_zkv = tl.zkv;
+          v_row = row;
+          v_j = j;
+          v_tr = tr;
+          if (j == 0) {
+            // Q of this tile, after the entry with its K_0 (which also holds
+            // the previous tile's last V, needed first)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t == 1 && !tl.has_sub1) break;
+              // the previous tile's last S_t GEMM must be done reading Q_t
+              if (nq[t] > 0 && !mbar_wait(&q_free[t], (nq[t] - 1) & 1, sAbort, budget)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
+              tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], tl.m0 + t * kBlockM,
+                               tl.zkv, pol_q);
+              ++nq[t];
+            }
+            if (!ok) break;
+          }
+        }
       }
-      int issued = 0;
-      for (int idx = 0; idx < 2 * n_blocks; ++idx) {
-        const int slot = idx % C::kStages;
-        const int round = idx / C::kStages;
-        if (round > 0 && !mbar_wait(&kv_empty[slot], (round - 1) & 1, sAbort, budget)) break;
-        mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
-        const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
-        tma_load_tile<D>(sKV + slot * C::kTileBytes, map, &kv_full[slot],
-                         (jb + (idx >> 1)) * kBlockN, zkv, pol_kv);
-        stamp((idx & 1) ? kEvLoadV : kEvLoadK, idx >> 1);
-        issued = idx + 1;
-      }
+      // the last V closes the stream
+      if (ok && v_zkv >= 0) issue_entry(-1, 0);
       // every copy issued must land before the CTA exits (on the normal path
       // these phases completed long ago)
-      drain_wait(&q_full[0], 0, budget);
-      if (has_sub1) drain_wait(&q_full[1], 0, budget);
-      const int first = issued > C::kStages ? issued - C::kStages : 0;
-      for (int idx = first; idx < issued; ++idx)
-        drain_wait(&kv_full[idx % C::kStages], (idx / C::kStages) & 1, budget);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (nq[t] > 0) drain_wait(&q_full[t], (nq[t] - 1) & 1, budget);
+      const uint32_t first = e > (uint32_t)C::kPairs ? e - C::kPairs : 0;
+      for (uint32_t idx = first; idx < e; ++idx)
+        drain_wait(&kv_full[idx % C::kPairs], (idx / C::kPairs) & 1, budget);
     }
     __syncwarp();
   }
@@ -570,40 +743,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   if (warp == 12) tmem_dealloc(tmem, C::kTmemCols);
-  if (threadIdx.x == 0) stamp(kEvEnd, 0);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_attn_status, 0, (int)ATTN_ERR_TIMEOUT);
 }
 
 namespace {
 
+std::mutex g_launch_mu;
+bool g_attr_set[2][2][64] = {};  // [D == 128][trace][device]
+int g_sm_count[64] = {};
+
 template <int D, bool kTrace>
-cudaError_t launch_d(const AttnParams& p, int n_m_tiles, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(attn_fwd_kernel<D, kTrace>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_launch_mu);
+    bool& attr_set = g_attr_set[D == 128][kTrace][dev];
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(attn_fwd_kernel<D, kTrace>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set = true;
+    }
+    if (g_sm_count[dev] == 0) {
+      err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (err != cudaSuccess) return err;
+    }
+    sms = g_sm_count[dev];
   }
-  dim3 grid(n_m_tiles * p.kv_splits, p.H_kv, p.B);
+  if (p.num_tiles <= 0 || sms <= 0) return cudaErrorInvalidValue;
+  // persistent grid: one CTA per SM (the kernel's shared memory allows no
+  // second), fewer when there are fewer tiles
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   attn_fwd_kernel<D, kTrace><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream) {
+cudaError_t launch_attn_fwd(const AttnParams& p, int D, cudaStream_t stream) {
   if (p.trace || p.fault_drop_block >= 0) {
-    if (D == 128) return launch_d<128, true>(p, n_m_tiles, stream);
-    if (D == 64) return launch_d<64, true>(p, n_m_tiles, stream);
+    if (D == 128) return launch_d<128, true>(p, stream);
+    if (D == 64) return launch_d<64, true>(p, stream);
     return cudaErrorInvalidValue;
   }
-  if (D == 128) return launch_d<128, false>(p, n_m_tiles, stream);
-  if (D == 64) return launch_d<64, false>(p, n_m_tiles, stream);
+  if (D == 128) return launch_d<128, false>(p, stream);
+  if (D == 64) return launch_d<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

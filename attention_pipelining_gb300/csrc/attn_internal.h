@@ -18,14 +18,30 @@ struct AttnParams {
   CUtensorMap tm_q;  // Q as [B*H_kv, R, D], box {64, 128, 1}, 128-byte swizzle (load)
   CUtensorMap tm_k;  // K as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
   CUtensorMap tm_v;  // V as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
-  CUtensorMap tm_o;  // O as [B*H_kv, R, D], box {64, 32, 1} (store, rows >= R dropped)
+  void* o;           // [B, H_q, S_q, D] bf16 (row rho of group z at (z * R + rho) * D)
   float* lse;        // [B, H_q, S_q]
   int B, H_q, H_kv, S_q, S_kv, causal;
   int rows_per_group;       // R
   long long total_rows;     // B * H_q * S_q
-  // Split KV: CTA x-index = query tile * kv_splits + split; split s covers KV
-  // blocks [s * kv_blocks_per_split, (s + 1) * kv_blocks_per_split).  With
-  // kv_splits > 1 the CTA writes a partial result instead of O and LSE:
+  // Work tiles: one tile = 256 rows of one row group x one KV split.  The
+  // grid is persistent (at most one CTA per SM); CTA c takes tiles c, then
+  // 2G-1-c, then 2G+c, ... (G = gridDim.x, a snake over rounds of G tiles)
+  // from the list ordered as below, so the longest tiles go first and the
+  // CTAs' total work evens out.
+  //   non-causal: group-major (the tiles running at once share K/V heads
+  //               in L2), query tiles last-to-first, then split;
+  //   causal:     by cost rank (longest first), then group, then split.  A
+  //               rank names one query tile of a group: with lpt_heads > 0
+  //               (S_q a multiple of 256) rank -> position block
+  //               nh - 1 - rank / lpt_heads of head rank % lpt_heads (nh =
+  //               S_q / 256), otherwise query tile n_m_tiles - 1 - rank.
+  int n_m_tiles;            // ceil(R / 256)
+  int groups;               // B * H_kv
+  int num_tiles;            // n_m_tiles * groups * kv_splits
+  int lpt_heads;            // H_q / H_kv when causal and S_q % 256 == 0, else 0
+  // Split KV: split s of a query tile covers KV blocks
+  // [s * kv_blocks_per_split, (s + 1) * kv_blocks_per_split).  With
+  // kv_splits > 1 a tile writes a partial result instead of O and LSE:
   // o_part [kv_splits, total_rows, D] fp32 (normalised within the split) and
   // lse_part [kv_splits, total_rows] fp32 (-inf for a row with no key in it).
   int kv_splits;
@@ -34,8 +50,8 @@ struct AttnParams {
   float* lse_part;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   unsigned long long timeout_ns;  // budget of any single wait inside the kernel
-  // Timeline trace (the trace instantiation only): globaltimer stamps,
-  // layout [cta][event][block] for CTAs with linear index < trace_ctas.
+  // Timeline trace (the trace instantiation only): SM clock stamps of the
+  // first tile of each CTA with index < trace_ctas, layout [cta][event][block].
   unsigned long long* trace;
   int trace_ctas;
   int trace_blocks;
@@ -62,7 +78,7 @@ enum TraceEvent : int {
   kEvLoadK,         // producer: K_j load issued
   kEvLoadV,         // producer: V_j load issued
   kEvEpilogue,      // correction: epilogue of sub-tile j (j = 0, 1) starts
-  kEvEnd,           // j = 0: CTA teardown
+  kEvEnd,           // j = 0: the first tile's epilogue has stored O
   kEvMmaPV0Begin,   // tensor-core issuer: waits for PV_0(j) passed, issue begins
   kEvMmaS0Begin,
   kEvMmaPV1Begin,
@@ -75,10 +91,10 @@ enum TraceEvent : int {
 bool encode_bf16_map_3d(CUtensorMap* map, const void* base, uint64_t D, uint64_t rows,
                         uint64_t outer, uint32_t box_rows);
 
-// Queues the fused kernel (D = 64 or 128); `n_m_tiles` = ceil(R / 256).
+// Queues the fused kernel (D = 64 or 128) on min(p.num_tiles, SM count) CTAs.
 // With p.trace set or p.fault_drop_block >= 0, the diagnostic instantiation
 // (timeline stamps, timeout test) runs instead.
-cudaError_t launch_attn_fwd(const AttnParams& p, int D, int n_m_tiles, cudaStream_t stream);
+cudaError_t launch_attn_fwd(const AttnParams& p, int D, cudaStream_t stream);
 
 // Queues the merge of split-KV partial results into O (bf16) and LSE.
 cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* o, float* lse,
