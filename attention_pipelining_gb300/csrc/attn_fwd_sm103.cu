@@ -565,9 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     // ------------------------------------------------------------ warpgroup 3
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsLoadMma) : "memory");
-    if (warp == 12 && lane == 0) {
-      // tensor-core issuer: one thread, no warp-wide votes, so it needs as
-      // few issue slots as possible next to the busy softmax warps
+    if (warp == 12) {
+      // tensor-core issuer: the whole warp runs the loop and its waits, with
+      // all values warp-uniform; one elected lane issues every tcgen05.mma
+      // and tcgen05.commit (they act for the issuing thread alone, and a
+      // commit tracks the operations of the thread that executes it)
+      const bool leader = elect_one();
       const uint64_t dq[2] = {kmajor_tile_desc(smem_u32(sQ)),
                               kmajor_tile_desc(smem_u32(sQ + C::kTileBytes))};
       const uint64_t dk0 = kmajor_tile_desc(smem_u32(sKV));
@@ -595,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // S_t(0) = Q_t K_0^T.  K_0 sits in entry e_next - 1, already waited
         // for in the previous tile's last iteration (entry 0 for the first).
         if (e_next == 0) {
-          if (!mbar_wait(&kv_full[0], 0, sAbort, budget)) { ok = false; break; }
+          if (!warp_wait(&kv_full[0], 0, sAbort, budget)) { ok = false; break; }
           e_next = 1;
         }
         const uint32_t s_k0 = (e_next - 1) % C::kPairs;
@@ -603,15 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= n_sub) break;
-          if (!mbar_wait(&q_full[t], nq[t] & 1, sAbort, budget)) { ok = false; break; }
+          if (!warp_wait(&q_full[t], nq[t] & 1, sAbort, budget)) { ok = false; break; }
           tc_fence_after_sync();
-          issue_qk_gemm<D>(tS[t], dq[t], dk_first);
-          tc_commit(&s_full[t]);
-          if (n == 1) tc_commit(&q_free[t]);  // the tile's last read of Q_t
-          stamp(tr, t ? kEvMmaS1 : kEvMmaS0, 0);
+          if (leader) {
+            issue_qk_gemm<D>(tS[t], dq[t], dk_first);
+            tc_commit(&s_full[t]);
+            if (n == 1) tc_commit(&q_free[t]);  // the tile's last read of Q_t
+          }
+          stamp(tr && leader, t ? kEvMmaS1 : kEvMmaS0, 0);
         }
         if (!ok) break;
-        tc_commit(&kv_empty[s_k0]);
+        if (leader) tc_commit(&kv_empty[s_k0]);
         for (int j = 0; j < n; ++j) {
           const bool more = (j + 1) < n;
           // entry e_next: V_j and the next K (K_{j+1}, or the next tile's
@@ -619,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           // softmax is still busy, keeps it off the path from "P ready" to
           // the GEMMs.
           const uint32_t st = e_next % C::kPairs;
-          if (!mbar_wait(&kv_full[st], (e_next / C::kPairs) & 1, sAbort, budget)) {
+          if (!warp_wait(&kv_full[st], (e_next / C::kPairs) & 1, sAbort, budget)) {
             ok = false;
             break;
           }
@@ -630,24 +635,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (t >= n_sub) break;
-            if (!mbar_wait(&p_full[t], (nb[t] + j) & 1, sAbort, budget)) { ok = false; break; }
+            if (!warp_wait(&p_full[t], (nb[t] + j) & 1, sAbort, budget)) { ok = false; break; }
             tc_fence_after_sync();
-            stamp(tr, t ? kEvMmaPV1Begin : kEvMmaPV0Begin, j);
-            issue_pv_gemm<D>(tO[t], tS[t], dv, j > 0);
-            if (!more) tc_commit(&pv_done[t]);  // the epilogue waits for the last PV only
-            stamp(tr, t ? kEvMmaPV1 : kEvMmaPV0, j);
+            stamp(tr && leader, t ? kEvMmaPV1Begin : kEvMmaPV0Begin, j);
+            if (leader) {
+              issue_pv_gemm<D>(tO[t], tS[t], dv, j > 0);
+              if (!more) tc_commit(&pv_done[t]);  // the epilogue waits for the last PV only
+            }
+            stamp(tr && leader, t ? kEvMmaPV1 : kEvMmaPV0, j);
             if (more) {
-              stamp(tr, t ? kEvMmaS1Begin : kEvMmaS0Begin, j + 1);
-              issue_qk_gemm<D>(tS[t], dq[t], dk);
-              tc_commit(&s_full[t]);
-              if (j + 2 == n) tc_commit(&q_free[t]);
-              stamp(tr, t ? kEvMmaS1 : kEvMmaS0, j + 1);
+              stamp(tr && leader, t ? kEvMmaS1Begin : kEvMmaS0Begin, j + 1);
+              if (leader) {
+                issue_qk_gemm<D>(tS[t], dq[t], dk);
+                tc_commit(&s_full[t]);
+                if (j + 2 == n) tc_commit(&q_free[t]);
+              }
+              stamp(tr && leader, t ? kEvMmaS1 : kEvMmaS0, j + 1);
             }
           }
           if (!ok) break;
           // release the entry last, off the critical path (after the last
           // block its K belongs to the next tile: released there)
-          if (more) tc_commit(&kv_empty[st]);
+          if (more && leader) tc_commit(&kv_empty[st]);
         }
         if (!ok) break;
 #pragma unroll
@@ -657,9 +666,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           nb[t] += n;
         }
       }
-      // let every tensor-core op this thread issued finish before teardown
-      tc_commit(drain);
-      drain_wait(drain, 0, budget);
+      // let every tensor-core op the leader issued finish before teardown
+      if (leader) {
+        tc_commit(drain);
+        drain_wait(drain, 0, budget);
+      }
+      __syncwarp();
     } else if (warp == 13 && lane == 0) {
       // TMA producer (one thread)
       const uint64_t pol_q = l2_policy_evict_first();

@@ -69,6 +69,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True in exactly one lane of a fully active warp (the lowest).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (and raises *abort_flag) once `budget_ns` has passed, or false at once
 // if another thread of the CTA already raised *abort_flag.
