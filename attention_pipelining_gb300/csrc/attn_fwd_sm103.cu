@@ -672,8 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         drain_wait(drain, 0, budget);
       }
       __syncwarp();
-    } else if (warp == 13 && lane == 0) {
-      // TMA producer (one thread)
+    } else if (warp == 13) {
+      // TMA producer: the whole warp runs the loop and its waits; one
+      // elected lane issues the copies and the expect-tx arrivals
+      const bool leader = elect_one();
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t e = 0;            // ring entries issued so far
@@ -687,17 +689,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto issue_entry = [&](int k_zkv, int k_row) -> bool {
         const uint32_t st = e % C::kPairs;
         const uint32_t round = e / C::kPairs;
-        if (round > 0 && !mbar_wait(&kv_empty[st], (round - 1) & 1, sAbort, budget)) return false;
-        const uint32_t bytes = (v_zkv >= 0 ? C::kTileBytes : 0) + (k_zkv >= 0 ? C::kTileBytes : 0);
-        mbar_arrive_expect_tx(&kv_full[st], bytes);
-        if (v_zkv >= 0) {
-          tma_load_tile<D>(sKV + ((2 * st + C::kSlots - 1) % C::kSlots) * C::kTileBytes, &p.tm_v,
-                           &kv_full[st], v_row, v_zkv, pol_kv);
-          stamp(v_tr, kEvLoadV, v_j);
+        if (round > 0 && !warp_wait(&kv_empty[st], (round - 1) & 1, sAbort, budget)) return false;
+        if (leader) {
+          const uint32_t bytes =
+              (v_zkv >= 0 ? C::kTileBytes : 0) + (k_zkv >= 0 ? C::kTileBytes : 0);
+          mbar_arrive_expect_tx(&kv_full[st], bytes);
+          if (v_zkv >= 0) {
+            tma_load_tile<D>(sKV + ((2 * st + C::kSlots - 1) % C::kSlots) * C::kTileBytes,
+                             &p.tm_v, &kv_full[st], v_row, v_zkv, pol_kv);
+            stamp(v_tr, kEvLoadV, v_j);
+          }
+          if (k_zkv >= 0)
+            tma_load_tile<D>(sKV + 2 * st * C::kTileBytes, &p.tm_k, &kv_full[st], k_row, k_zkv,
+                             pol_kv);
         }
-        if (k_zkv >= 0)
-          tma_load_tile<D>(sKV + 2 * st * C::kTileBytes, &p.tm_k, &kv_full[st], k_row, k_zkv,
-                           pol_kv);
         ++e;
         return true;
       };
@@ -711,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int j = 0; j < tl.n_blocks; ++j) {
           const int row = (tl.jb + j) * kBlockN;
           if (!issue_entry(tl.zkv, row)) { ok = false; break; }
-          stamp(tr, kEvLoadK, j);
+          stamp(tr && leader, kEvLoadK, j);
           v_zkv = tl.zkv;
           v_row = row;
           v_j = j;
@@ -723,13 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int t = 0; t < 2; ++t) {
               if (t == 1 && !tl.has_sub1) break;
               // the previous tile's last S_t GEMM must be done reading Q_t
-              if (nq[t] > 0 && !mbar_wait(&q_free[t], (nq[t] - 1) & 1, sAbort, budget)) {
+              if (nq[t] > 0 && !warp_wait(&q_free[t], (nq[t] - 1) & 1, sAbort, budget)) {
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
-              tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t], tl.m0 + t * kBlockM,
-                               tl.zkv, pol_q);
+              if (leader) {
+                mbar_arrive_expect_tx(&q_full[t], C::kTileBytes);
+                tma_load_tile<D>(sQ + t * C::kTileBytes, &p.tm_q, &q_full[t],
+                                 tl.m0 + t * kBlockM, tl.zkv, pol_q);
+              }
               ++nq[t];
             }
             if (!ok) break;
@@ -740,12 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (ok && v_zkv >= 0) issue_entry(-1, 0);
       // every copy issued must land before the CTA exits (on the normal path
       // these phases completed long ago)
+      if (leader) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (nq[t] > 0) drain_wait(&q_full[t], (nq[t] - 1) & 1, budget);
-      const uint32_t first = e > (uint32_t)C::kPairs ? e - C::kPairs : 0;
-      for (uint32_t idx = first; idx < e; ++idx)
-        drain_wait(&kv_full[idx % C::kPairs], (idx / C::kPairs) & 1, budget);
+        for (int t = 0; t < 2; ++t)
+          if (nq[t] > 0) drain_wait(&q_full[t], (nq[t] - 1) & 1, budget);
+        const uint32_t first = e > (uint32_t)C::kPairs ? e - C::kPairs : 0;
+        for (uint32_t idx = first; idx < e; ++idx)
+          drain_wait(&kv_full[idx % C::kPairs], (idx / C::kPairs) & 1, budget);
+      }
     }
     __syncwarp();
   }
