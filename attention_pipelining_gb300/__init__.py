@@ -170,18 +170,20 @@ def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
 TRACE_EVENTS = ["sm0_wake", "sm0_loaded", "sm0_done", "sm1_wake", "sm1_loaded", "sm1_done",
                 "mma_pv0", "mma_s0", "mma_pv1", "mma_s1", "corr0", "corr1", "load_k", "load_v",
                 "epilogue", "end", "mma_pv0_begin", "mma_s0_begin", "mma_pv1_begin", "mma_s1_begin"]
+MAX_TRACE_BLOCKS = 128  # KV blocks the trace instantiation records per event, at most
 
 
 def attn_fwd_trace(q, k, v, causal: bool, scale: float, ctas: int = 4, blocks: int | None = None,
                    stream=None):
     """Runs the trace instantiation; returns (o, lse, trace) where trace is an
-    int64 CPU tensor [ctas, 16, blocks] of SM clock cycles (0 = no event)."""
+    int64 CPU tensor [ctas, 20, blocks] of SM clock cycles (0 = no event), for the
+    first tile of each traced CTA; blocks <= MAX_TRACE_BLOCKS."""
     import torch
     _check_inputs(q, k, v)
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     if blocks is None:
-        blocks = (Skv + 127) // 128
+        blocks = min((Skv + 127) // 128, MAX_TRACE_BLOCKS)
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     tr = torch.zeros((ctas, len(TRACE_EVENTS), blocks), dtype=torch.int64, device=q.device)

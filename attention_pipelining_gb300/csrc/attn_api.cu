@@ -259,7 +259,8 @@ attn_status_t attn_fwd_trace(const void* q, const void* k, const void* v, void* 
                              int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
                              float scale, unsigned long long* trace, int trace_ctas,
                              int trace_blocks, attn_stream_t stream) {
-  if (!trace || trace_ctas <= 0 || trace_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!trace || trace_ctas <= 0 || trace_blocks <= 0 || trace_blocks > kMaxTraceBlocks)
+    return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(trace) & 7u) != 0) return ATTN_ERR_MISALIGNED;
   return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, trace, trace_ctas,
                   trace_blocks, -1, kDefaultTimeoutNs, stream);

@@ -91,7 +91,9 @@ struct Cfg {
   static constexpr int kOffRowSumP = kOffRowSum + 4 * 128 * 4;  // float [2][2][128]: sum of bf16(p)
   static constexpr int kOffRowMax = kOffRowSumP + 4 * 128 * 4;  // float [2][2][128]
   static constexpr int kOffMisc = kOffRowMax + 4 * 128 * 4;     // tmem base, abort flag
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;       // + slack to align the base
+  // timeline stamps of the trace instantiation, uint64 [event][block]
+  static constexpr int kOffTrace = kOffMisc + 16;
+  static constexpr int kSmemBytes = kOffTrace + kNumTraceEvents * kMaxTraceBlocks * 8 + 1024;
   // tensor memory columns
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
@@ -209,22 +211,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   float* sRowMax = reinterpret_cast<float*>(smem + C::kOffRowMax);
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  unsigned long long* sTrace = reinterpret_cast<unsigned long long*>(smem + C::kOffTrace);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t budget = p.timeout_ns;
   // trace stamps (compiled only into the trace instantiation): the first
-  // tile of CTAs below trace_ctas.  The stamp is the SM cycle counter; a slot
-  // written by several warps keeps the latest stamp (a barrier completes
-  // when its last warp arrives).
+  // tile of CTAs below trace_ctas.  The stamp is the SM cycle counter, kept
+  // in shared memory while the kernel runs and copied out at the end.  One
+  // thread stamps each event (lane 0 of the first warp of a warpgroup, the
+  // elected lane of the issuer and the producer), with a plain store.
   const bool trace_cta = kTrace && (int)blockIdx.x < p.trace_ctas;
   auto stamp = [&](bool on, int ev, int j) {
     if constexpr (kTrace) {
       if (on && j < p.trace_blocks)
-        atomicMax(&p.trace[((size_t)blockIdx.x * kNumTraceEvents + ev) * p.trace_blocks + j],
-                  (unsigned long long)clock64());
+        sTrace[ev * kMaxTraceBlocks + j] = (unsigned long long)clock64();
     }
   };
+  if constexpr (kTrace) {
+    for (int i = threadIdx.x; i < kNumTraceEvents * kMaxTraceBlocks; i += kThreads) sTrace[i] = 0;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kPairs; ++i) {
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const Tile tl = decode_tile(p, ti);
       // (warpgroup 1 has nothing to do when the tile has no sub-tile 1)
       if (tl.n_blocks <= 0 || (t == 1 && !tl.has_sub1)) continue;
-      const bool tr = trace_cta && k == 0 && lane == 0;
+      const bool tr = trace_cta && k == 0 && lane == 0 && (warp & 3) == 0;
       const int rho = tl.m0 + t * kBlockM + r;               // row in the row group
       const int pos = rho % p.S_q;                           // its query position
       // smallest query position in this sub-tile (0 if it spans two heads)
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     while (have) {
       const int n_sub = cur.has_sub1 ? 2 : 1;
-      const bool tr = trace_cta && k == 0 && lane == 0;
+      const bool tr = trace_cta && k == 0 && lane == 0 && (warp & 3) == 0;
       // Block j >= 1: the softmax's alpha arrives on stats[t]; it is
       // published after the softmax saw S_t(j), whose commit follows
       // PV_t(j-1), so O_t already holds every earlier block.
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (have_next && (t == 0 || nxt.has_sub1)) mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
-      stamp(tr && q4 == 0, kEvEnd, 0);
+      stamp(tr, kEvEnd, 0);
       k = k_next;
       cur = nxt;
       have = have_next;
@@ -765,6 +771,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after_sync();
   if (warp == 12) tmem_dealloc(tmem, C::kTmemCols);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_attn_status, 0, (int)ATTN_ERR_TIMEOUT);
+  if constexpr (kTrace) {
+    if (trace_cta) {
+      for (int i = threadIdx.x; i < kNumTraceEvents * p.trace_blocks; i += kThreads) {
+        const int ev = i / p.trace_blocks, j = i - ev * p.trace_blocks;
+        const unsigned long long v = sTrace[ev * kMaxTraceBlocks + j];
+        if (v != 0) p.trace[((size_t)blockIdx.x * kNumTraceEvents + ev) * p.trace_blocks + j] = v;
+      }
+    }
+  }
 }
 
 namespace {

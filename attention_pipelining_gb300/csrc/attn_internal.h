@@ -85,6 +85,7 @@ enum TraceEvent : int {
   kEvMmaS1Begin,
   kNumTraceEvents
 };
+constexpr int kMaxTraceBlocks = 128;  // KV blocks a trace records per event, at most
 
 // Encodes a 3-D bf16 tensor map over a contiguous [outer, rows, D] array with
 // a {64, box_rows, 1} box and 128-byte swizzle.  Returns false on failure.

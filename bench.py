@@ -451,7 +451,7 @@ def run_trace(args, w):
     for _ in range(args.warmup):
         ap.attn_fwd(q, k, v, w.causal, w.scale)
     torch.cuda.synchronize()
-    n_blocks = (w.S_kv + 127) // 128
+    n_blocks = min((w.S_kv + 127) // 128, ap.MAX_TRACE_BLOCKS)
     _, _, t = ap.attn_fwd_trace(q, k, v, w.causal, w.scale, ctas=args.trace, blocks=n_blocks)
     out = {"workload": w.name, "traced_ctas": args.trace, **tr.summarize(t.numpy(), n_blocks)}
     if args.trace_out:
