@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE.
+"""fp64 CPU oracle for the attention forward and backward -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference arm may import this package.  The CUDA product path never touches
@@ -12,7 +12,12 @@ P V = O), with the readings listed at the top of the C file (scale before
 the mask, top-left causal mask j <= i, grouped heads h // (H_q / H_kv),
 natural-log LSE, [B, H, S, D] layout).
 
-This module only builds the shared library and marshals numpy arrays.
+The backward (``attn_bwd_oracle.c``, its own library) is the chain rule
+through that definition: dQ, dK, dV of L = sum(O * dO), with D_i = dO_i . O_i
+and dS = P (dP - D); it also takes fp64 inputs so finite differences of the
+forward can check it.
+
+This module only builds the shared libraries and marshals numpy arrays.
 """
 from __future__ import annotations
 
@@ -25,13 +30,18 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_BWD_SRC = os.path.join(_HERE, "attn_bwd_oracle.c")
+_BWD_LIB = os.path.join(_HERE, "libbwd_oracle.so")
 _default = None
+_bwd_default = None
 
 
 def build(force: bool = False) -> str:
-    """Compile attn_oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        compile_source(_SRC, _LIB)
+    """Compile attn_oracle.c into liboracle.so and attn_bwd_oracle.c into
+    libbwd_oracle.so next to them (gcc, -O2, OpenMP); returns the first."""
+    for src, lib in ((_SRC, _LIB), (_BWD_SRC, _BWD_LIB)):
+        if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+            compile_source(src, lib)
     return _LIB
 
 
@@ -174,3 +184,130 @@ def attn_probs(q, k, v, causal: bool, scale: float):
 
 def num_threads() -> int:
     return default().num_threads()
+
+
+# ---------------------------------------------------------------- backward
+
+
+def _bind_bwd(path: str):
+    lib = ctypes.CDLL(path)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    ci, cd = ctypes.c_int, ctypes.c_double
+    dims = [ci, ci, ci, ci, ci, ci, ci, cd]
+    lib.oracle_attn_bwd.argtypes = [u16p, u16p, u16p, u16p, f64p, f64p, f64p] + dims
+    lib.oracle_attn_bwd_f64.argtypes = [f64p, f64p, f64p, f64p, f64p, f64p, f64p] + dims
+    lib.oracle_attn_fwd_f64.argtypes = [f64p, f64p, f64p, f64p, f64p] + dims
+    lib.oracle_attn_bwd_dq_rows.argtypes = [u16p, u16p, u16p, u16p, i64p, ctypes.c_int64,
+                                            f64p] + dims
+    lib.oracle_attn_bwd_dkv_rows.argtypes = [u16p, u16p, u16p, u16p, i64p, ctypes.c_int64,
+                                             f64p, f64p] + dims
+    for f in ("oracle_attn_bwd", "oracle_attn_bwd_f64", "oracle_attn_fwd_f64",
+              "oracle_attn_bwd_dq_rows", "oracle_attn_bwd_dkv_rows"):
+        getattr(lib, f).restype = ci
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+class BwdOracle:
+    """Handle on one compiled copy of the backward oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.lib = _bind_bwd(path)
+
+    def attn_bwd(self, q, k, v, dout, causal: bool, scale: float):
+        """dQ [B,H_q,S_q,D], dK and dV [B,H_kv,S_kv,D] (float64) for bf16 inputs."""
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        if tuple(dout.shape) != tuple(q.shape):
+            raise ValueError("dout must have q's shape")
+        qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+        dq = np.empty((B, Hq, Sq, D), np.float64)
+        dk = np.empty((B, Hkv, Skv, D), np.float64)
+        dv = np.empty((B, Hkv, Skv, D), np.float64)
+        rc = self.lib.oracle_attn_bwd(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(db, ctypes.c_uint16), _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
+            _p(dv, ctypes.c_double), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd rejected the arguments (rc={rc})")
+        return dq, dk, dv
+
+    def attn_bwd_f64(self, q, k, v, dout, causal: bool, scale: float):
+        """The same for float64 numpy inputs (no bf16 rounding)."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        if dout.shape != q.shape:
+            raise ValueError("dout must have q's shape")
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        rc = self.lib.oracle_attn_bwd_f64(
+            _p(q, ctypes.c_double), _p(k, ctypes.c_double), _p(v, ctypes.c_double),
+            _p(dout, ctypes.c_double), _p(dq, ctypes.c_double), _p(dk, ctypes.c_double),
+            _p(dv, ctypes.c_double), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_f64 rejected the arguments (rc={rc})")
+        return dq, dk, dv
+
+    def attn_fwd_f64(self, q, k, v, causal: bool, scale: float):
+        """Forward O and LSE for float64 numpy inputs."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, Sq), np.float64)
+        rc = self.lib.oracle_attn_fwd_f64(
+            _p(q, ctypes.c_double), _p(k, ctypes.c_double), _p(v, ctypes.c_double),
+            _p(o, ctypes.c_double), _p(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_fwd_f64 rejected the arguments (rc={rc})")
+        return o, lse
+
+    def dq_rows(self, q, k, v, dout, rows, causal: bool, scale: float):
+        """dQ of the flat query rows ``rows`` into [B, H_q, S_q]: [n, D] float64."""
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        if tuple(dout.shape) != tuple(q.shape):
+            raise ValueError("dout must have q's shape")
+        qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        out = np.empty((r.size, D), np.float64)
+        rc = self.lib.oracle_attn_bwd_dq_rows(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(db, ctypes.c_uint16), _p(r, ctypes.c_int64), r.size, _p(out, ctypes.c_double),
+            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_dq_rows rejected the arguments (rc={rc})")
+        return out
+
+    def dkv_rows(self, q, k, v, dout, rows, causal: bool, scale: float):
+        """dK and dV of the flat key rows ``rows`` into [B, H_kv, S_kv]: two [n, D]."""
+        B, Hq, Hkv, Sq, Skv, D = _dims(q, k, v)
+        if tuple(dout.shape) != tuple(q.shape):
+            raise ValueError("dout must have q's shape")
+        qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        dk = np.empty((r.size, D), np.float64)
+        dv = np.empty((r.size, D), np.float64)
+        rc = self.lib.oracle_attn_bwd_dkv_rows(
+            _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+            _p(db, ctypes.c_uint16), _p(r, ctypes.c_int64), r.size, _p(dk, ctypes.c_double),
+            _p(dv, ctypes.c_double), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_dkv_rows rejected the arguments (rc={rc})")
+        return dk, dv
+
+
+def bwd_default() -> BwdOracle:
+    """The backward oracle built from attn_bwd_oracle.c (compiled on first use)."""
+    global _bwd_default
+    if _bwd_default is None:
+        build()
+        _bwd_default = BwdOracle(_BWD_LIB)
+    return _bwd_default
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float):
+    return bwd_default().attn_bwd(q, k, v, dout, causal, scale)
