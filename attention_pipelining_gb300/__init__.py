@@ -35,7 +35,7 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
            "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
-           "attn_splitkv_noalloc_capacity"]
+           "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes"]
 
 
 class AttnError(RuntimeError):
@@ -92,6 +92,10 @@ def _load():
     lib.attn_fwd_splitkv_noalloc.restype = ci
     lib.attn_splitkv_noalloc_capacity.argtypes = []
     lib.attn_splitkv_noalloc_capacity.restype = ctypes.c_size_t
+    lib.attn_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
+    lib.attn_bwd.restype = ci
+    lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -220,6 +224,42 @@ def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int = 0, w
                                     B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
                                     int(splits), _stream_handle(stream)), "attn_fwd_splitkv")
     return o, lse
+
+
+def bwd_workspace_bytes(B, H_q, H_kv, S_q) -> int:
+    return int(_load().attn_bwd_workspace_bytes(B, H_q, H_kv, S_q))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, out=None,
+             stream=None):
+    """Backward of attn_fwd: returns (dq, dk, dv) for the upstream gradient
+    ``dout``, given the forward's ``o`` and ``lse``.  ``workspace``: optional
+    uint8 CUDA tensor of at least bwd_workspace_bytes(...) bytes (allocated if
+    None); ``out``: optional (dq, dk, dv) to write into."""
+    import torch
+    _check_inputs(q, k, v)
+    for name, t, ref in (("o", o, q), ("dout", dout, q)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.shape != ref.shape \
+                or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H_q, S_q] tensor")
+    nbytes = bwd_workspace_bytes(B, Hq, Hkv, Sq)
+    if nbytes == 0:
+        raise AttnError(1, "attn_bwd_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    _check(_load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+                            _stream_handle(stream)), "attn_bwd")
+    return dq, dk, dv
 
 
 def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,

@@ -244,9 +244,79 @@ attn_status_t splitkv_impl(const void* q, const void* k, const void* v, void* o,
   return ATTN_OK;
 }
 
+// Rows of the per-group padded layout of the backward's row vectors.
+static int64_t bwd_padded_rows(int H_q, int H_kv, int S_q) {
+  const int64_t R = (int64_t)(H_q / H_kv) * S_q;
+  return (R + 127) / 128 * 128;
+}
+
+size_t bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q) {
+  return 2 * (size_t)B * H_kv * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
+}
+
+static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                              int S_q, int S_kv, int D, int causal, float scale,
+                              attn_stream_t stream) {
+  attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
+  if (st != ATTN_OK) return st;
+  if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  if (workspace_bytes < bwd_workspace_bytes(B, H_q, H_kv, S_q)) return ATTN_ERR_INVALID_ARG;
+  // grids: (key blocks, groups) and (query blocks, groups); y is limited to 65535
+  if ((int64_t)B * H_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+  st = check_device();
+  if (st != ATTN_OK) return st;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int R = (H_q / H_kv) * S_q;
+  if (!encode_bf16_map_3d(&p.tm_q, q, D, R, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p.tm_do, dout, D, R, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p.tm_k, k, D, S_kv, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p.tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128))
+    return ATTN_ERR_CUDA;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  const int64_t Rp = bwd_padded_rows(H_q, H_kv, S_q);
+  p.lse2 = static_cast<float*>(workspace);
+  p.delta = p.lse2 + (size_t)B * H_kv * Rp;
+  p.B = B;
+  p.H_q = H_q;
+  p.H_kv = H_kv;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.causal = causal;
+  p.R = R;
+  p.Rp = (int)Rp;
+  p.groups = B * H_kv;
+  p.scale = scale;
+  p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+  p.timeout_ns = kDefaultTimeoutNs;
+  if (launch_attn_bwd(p, D, o, dout, lse, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 }  // namespace attnpipe
 
 extern "C" {
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                       int S_q, int S_kv, int D, int causal, float scale, attn_stream_t stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv,
+                  S_q, S_kv, D, causal, scale, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q) {
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || S_q <= 0 || H_q % H_kv != 0) return 0;
+  return bwd_workspace_bytes(B, H_q, H_kv, S_q);
+}
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H_q, int H_kv, int S_q, int S_kv, int D, int causal, float scale,
@@ -320,11 +390,12 @@ attn_status_t attn_device_status(int* status_out, int reset) {
   if (!status_out) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
-  int main_status = 0, selftest_status = 0;
+  int main_status = 0, selftest_status = 0, bwd_status = 0;
   if (read_device_status(&main_status, reset != 0) != cudaSuccess ||
-      read_selftest_status(&selftest_status, reset != 0) != cudaSuccess)
+      read_selftest_status(&selftest_status, reset != 0) != cudaSuccess ||
+      read_bwd_status(&bwd_status, reset != 0) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  *status_out = main_status != 0 ? main_status : selftest_status;
+  *status_out = main_status != 0 ? main_status : (bwd_status != 0 ? bwd_status : selftest_status);
   return ATTN_OK;
 }
 

@@ -1,0 +1,696 @@
+// attn_bwd_sm103.cu -- attention backward for sm_103a (GB300).
+//
+// The gradients of the forward of "PipeThreader: Software-Defined Pipelining
+// for Efficient DNN Execution" (section A2, Fig. 7): with P the forward's
+// softmax rows, D_i = dO_i . O_i, dP = dO V^T and dS = P o (dP - D),
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K
+// (summed over the query heads that share a key/value head).  The backward
+// is the subject of "GPU软件流水线与Warp Specialization优化技术解析", section
+// 3.2 (Flash Attention backward on Blackwell: loads, tensor-core GEMMs and
+// the elementwise work in separate warp groups).
+//
+// Three kernels:
+//   prep   D_i and the base-2 LSE per row, into a padded per-group layout;
+//   dK/dV  one CTA per (row group, 128 keys): over the group's query blocks,
+//          S^T = K Q^T and dP^T = V dO^T on the tensor core, P^T and dS^T by
+//          two elementwise warpgroups (64 queries each), then dV += P^T dO and
+//          dK += dS^T Q accumulate in tensor memory;
+//   dQ     one CTA per (row group, 128 query rows): over the key blocks,
+//          S = Q K^T and dP = dO V^T, dS by the elementwise warpgroups (64
+//          keys each), dQ += dS K in tensor memory.
+// P needs no running max in the backward (the forward's LSE normalises it),
+// so the elementwise work splits over columns with no exchange.  Every GEMM
+// has the forward's shapes (M = 128, N = 128 or D, K = D or 128).
+//
+// 384 threads: warps 0-7 elementwise (warpgroup w takes columns 64w..64w+63
+// of every 128 x 128 block, thread = TMEM lane = the tile's row), warp 8
+// tensor-core issuer and warp 9 TMA producer (warp-wide, one elected lane
+// issues), warps 10-11 idle.  Every wait is bounded; a timeout raises a
+// CTA-wide abort flag and the device status word records ATTN_ERR_TIMEOUT.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "attn_tiles.cuh"
+#include "ptx.cuh"
+
+namespace attnpipe {
+
+__device__ int g_bwd_status = 0;
+
+namespace {
+
+constexpr int kThreadsB = 384;
+constexpr int kRows = 128;       // rows of a tile: keys (dK/dV kernel) or queries (dQ kernel)
+constexpr uint32_t kAll = 0xffffffffu;
+
+__device__ __forceinline__ bool warp_wait_b(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag, uint64_t budget) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, budget);
+  return __all_sync(kAll, ok);
+}
+
+__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, uint64_t budget) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, &never, budget);
+}
+
+__device__ __forceinline__ float u2f_b(uint32_t x) { return __uint_as_float(x); }
+
+// Acc[tmem, 128 x D fp32] (+)= A B where A [128 x 128] bf16 sits in tensor
+// memory split by warpgroup: K elements 0-63 in columns [0, 32), 64-127 in
+// [64, 96) (two per column), and B is a [128 x D] tile used MN-major (D
+// contiguous), given its MN-major tile descriptor: the forward's PV GEMM
+// with A read from the two halves.
+template <int D>
+__device__ __forceinline__ void issue_split_a_gemm(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t b_desc, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileRows / 16; ++kk) {
+    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+           b_desc + (uint64_t)((kk * 2048) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = TileShape<D>::kBytes;
+  // dK/dV kernel: K, V, then a ring of (Q, dO, base-2 LSE, D) stages
+  static constexpr int kQStages = (D == 128) ? 2 : 4;
+  static constexpr int kVecBytes = kRows * 4;                 // one [128] fp32 vector
+  static constexpr int kQStageBytes = 2 * kTileBytes + 2 * kVecBytes;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQRing = 2 * kTileBytes;
+  static constexpr int kOffBarKV = kOffQRing + kQStages * kQStageBytes;
+  // kv_full, q_full[S], q_empty[S], sp_full, ps_ready, acc_done, drain
+  static constexpr int kNumBarsKV = 2 * kQStages + 5;
+  static constexpr int kOffMiscKV = kOffBarKV + kNumBarsKV * 8;
+  static constexpr int kSmemKV = kOffMiscKV + 16 + 1024;
+  // dQ kernel: Q, dO, then a ring of (K, V) stages
+  static constexpr int kKVStages = (D == 128) ? 2 : 4;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTileBytes;
+  static constexpr int kOffKVRing = 2 * kTileBytes;
+  static constexpr int kOffBarQ = kOffKVRing + kKVStages * 2 * kTileBytes;
+  // q_full, kv_full[S], kv_empty[S], sp_full, ds_ready, acc_done, drain
+  static constexpr int kNumBarsQ = 2 * kKVStages + 5;
+  static constexpr int kOffMiscQ = kOffBarQ + kNumBarsQ * 8;
+  static constexpr int kSmemQ = kOffMiscQ + 16 + 1024;
+  // tensor memory: S (or S^T) [0,128), dP [128,256), accumulators after
+  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemKV <= 227 * 1024 && kSmemQ <= 227 * 1024, "shared memory budget");
+};
+
+// Does query block [r0, r0 + 128) of a row group hold a row that sees a key
+// of the block starting at kv0?  (Rows are head-in-group * S_q + position.)
+__device__ __forceinline__ bool qblock_sees(const BwdParams& p, int r0, int kv0) {
+  if (!p.causal) return true;
+  const int last = min(r0 + kRows, p.R) - 1;
+  if (r0 / p.S_q != last / p.S_q) return true;  // spans two heads: some row has a late position
+  return last % p.S_q >= kv0;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- prep
+
+// D_i = dO_i . O_i and LSE_i * log2(e), per row of the padded per-group
+// layout [groups, Rp] (rows R..Rp-1 of a group get 0).  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
+                                                            const uint16_t* __restrict__ o,
+                                                            const uint16_t* __restrict__ dout,
+                                                            const float* __restrict__ lse) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)p.groups * p.Rp) return;
+  const long long z = row / p.Rp;
+  const int rho = (int)(row - z * p.Rp);
+  if (rho >= p.R) {
+    if (lane == 0) {
+      p.delta[row] = 0.f;
+      p.lse2[row] = 0.f;
+    }
+    return;
+  }
+  const long long src = (z * p.R + rho) * D;
+  constexpr int kPer = D / 32;  // elements per lane
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + src + lane * 4);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + src + lane * 4);
+    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      acc += __uint_as_float(av[t] << 16) * __uint_as_float(bv[t] << 16);
+      acc += __uint_as_float(av[t] & 0xffff0000u) * __uint_as_float(bv[t] & 0xffff0000u);
+    }
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + src + lane * 2);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + src + lane * 2);
+    acc += __uint_as_float(a << 16) * __uint_as_float(b << 16);
+    acc += __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kAll, acc, off);
+  if (lane == 0) {
+    p.delta[row] = acc;
+    p.lse2[row] = lse[z * p.R + rho] * 1.4426950408889634f;
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw_b[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_b) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarKV);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::kQStages;
+  uint64_t* sp_full = q_empty + C::kQStages;
+  uint64_t* ps_ready = sp_full + 1;
+  uint64_t* acc_done = sp_full + 2;
+  uint64_t* drain = sp_full + 3;
+  uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscKV);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscKV + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t budget = p.timeout_ns;
+
+  const int kv0 = blockIdx.x * kRows;       // first key of the block
+  const int zkv = blockIdx.y;               // row group = key/value head
+  const int n_qb = (p.R + kRows - 1) / kRows;
+  // query blocks with work, counted once here (every role walks the same list)
+  int n_work = 0;
+  for (int qb = 0; qb < n_qb; ++qb) n_work += qblock_sees(p, qb * kRows, kv0) ? 1 : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ps_ready, 2 * 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *sAbort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(sTmemBase, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *sTmemBase;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  auto stage_q = [&](int s) { return smem + C::kOffQRing + s * C::kQStageBytes; };
+  auto stage_do = [&](int s) { return stage_q(s) + C::kTileBytes; };
+  auto stage_lse = [&](int s) {
+    return reinterpret_cast<float*>(stage_q(s) + 2 * C::kTileBytes);
+  };
+  auto stage_delta = [&](int s) {
+    return reinterpret_cast<float*>(stage_q(s) + 2 * C::kTileBytes + C::kVecBytes);
+  };
+
+  if (warp < 8) {
+    // -------------------------------------------------------- elementwise
+    const int w = warp >> 2;                       // columns 64w .. 64w + 63
+    const int r = (warp & 3) * 32 + lane;          // key row within the block
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int key = kv0 + r;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int n = 0;
+    for (int qb = 0; qb < n_qb && ok; ++qb) {
+      const int r0 = qb * kRows;
+      if (!qblock_sees(p, r0, kv0)) continue;
+      const int s = n % C::kQStages;
+      if (!warp_wait_b(sp_full, n & 1, sAbort, budget)) { ok = false; break; }
+      // the stage's LSE and D vectors arrived with its tiles: observe that
+      // phase here too before reading them
+      if (!warp_wait_b(&q_full[s], (n / C::kQStages) & 1, sAbort, budget)) { ok = false; break; }
+      tc_fence_after_sync();
+      const float* lse2 = stage_lse(s);
+      const float* dl = stage_delta(s);
+      // masking: rows past R, keys past S_kv, and (causal) keys after a row's
+      // position; a block needs none when every row sees every key
+      bool masked = (r0 + kRows > p.R) || (kv0 + kRows > p.S_kv);
+      int base_pos = 0;
+      if (p.causal) {
+        base_pos = r0 % p.S_q;
+        const bool one_head = (base_pos + kRows <= p.S_q);
+        masked = masked || !(one_head && base_pos >= kv0 + kRows - 1);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * w + 32 * c;
+        uint32_t sv[32], dp[32];
+        tmem_ld_x32(tmem + lane_base + C::kTmS + col0, sv);
+        tmem_ld_x32(tmem + lane_base + C::kTmDP + col0, dp);
+        tmem_ld_wait();
+        reg_after_wait(sv);
+        reg_after_wait(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pr[2], dsr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = col0 + 2 * i + h;
+            float pv = ex2_approx(u2f_b(sv[2 * i + h]) * sl2 - lse2[col]);
+            if (masked) {
+              const int rho = r0 + col;
+              bool vis = (rho < p.R) && (key < p.S_kv);
+              if (p.causal) {
+                int pos;
+                if (p.S_q >= kRows) {
+                  pos = base_pos + col;
+                  if (pos >= p.S_q) pos -= p.S_q;
+                } else {
+                  pos = rho % p.S_q;
+                }
+                vis = vis && (key <= pos);
+              }
+              pv = vis ? pv : 0.f;
+            }
+            pr[h] = pv;
+            dsr[h] = pv * (u2f_b(dp[2 * i + h]) - dl[col]);
+          }
+          pk[i] = pack_bf16x2(pr[0], pr[1]);
+          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
+        }
+        // P^T and dS^T of these 32 queries: columns 64w + 16c .. in the
+        // S^T and dP^T regions (this warpgroup's own, already-read columns)
+        tmem_st_x16(tmem + lane_base + C::kTmS + 64 * w + 16 * c, pk);
+        tmem_st_x16(tmem + lane_base + C::kTmDP + 64 * w + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(ps_ready);
+      ++n;
+    }
+    // ---------------------------------------------------------- epilogue
+    // warpgroup w writes columns [D/2 w, D/2 (w + 1)) of dV and dK
+    bool have_acc = ok && n_work > 0;
+    if (have_acc) {
+      if (!warp_wait_b(acc_done, 0, sAbort, budget)) { ok = false; have_acc = false; }
+      tc_fence_after_sync();
+    }
+    const bool row_ok = key < p.S_kv;
+    uint16_t* dk_row = static_cast<uint16_t*>(p.dk) + ((size_t)zkv * p.S_kv + key) * D;
+    uint16_t* dv_row = static_cast<uint16_t*>(p.dv) + ((size_t)zkv * p.S_kv + key) * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+      uint16_t* dst = which ? dk_row : dv_row;
+      const float mult = which ? p.scale : 1.f;
+      const uint32_t acc = tmem + lane_base + (which ? C::kTmAcc1 : C::kTmAcc0) + (D / 2) * w;
+#pragma unroll
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t v[32];
+        if (have_acc) {
+          tmem_ld_x32(acc + ch * 32, v);
+          tmem_ld_wait();
+          reg_after_wait(v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys
+        }
+        if (row_ok && ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + (D / 2) * w + ch * 32);
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            uint4 val;
+            val.x = pack_bf16x2(u2f_b(v[qd * 8 + 0]) * mult, u2f_b(v[qd * 8 + 1]) * mult);
+            val.y = pack_bf16x2(u2f_b(v[qd * 8 + 2]) * mult, u2f_b(v[qd * 8 + 3]) * mult);
+            val.z = pack_bf16x2(u2f_b(v[qd * 8 + 4]) * mult, u2f_b(v[qd * 8 + 5]) * mult);
+            val.w = pack_bf16x2(u2f_b(v[qd * 8 + 6]) * mult, u2f_b(v[qd * 8 + 7]) * mult);
+            d4[qd] = val;
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // -------------------------------------------------------- tensor-core issuer
+    const bool leader = elect_one();
+    const uint64_t dK = kmajor_tile_desc(smem_u32(sK));
+    const uint64_t dV = kmajor_tile_desc(smem_u32(sV));
+    const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP;
+    const uint32_t tdV = tmem + C::kTmAcc0, tdK = tmem + C::kTmAcc1;
+    bool ok = n_work > 0 && warp_wait_b(kv_full, 0, sAbort, budget);
+    // S^T, dP^T of work item n (its Q / dO stage must be loaded)
+    auto issue_sp = [&](int n) -> bool {
+      const int s = n % C::kQStages;
+      if (!warp_wait_b(&q_full[s], (n / C::kQStages) & 1, sAbort, budget)) return false;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_qk_gemm<D>(tS, dK, kmajor_tile_desc(smem_u32(stage_q(s))));
+        issue_qk_gemm<D>(tDP, dV, kmajor_tile_desc(smem_u32(stage_do(s))));
+        tc_commit(sp_full);
+      }
+      return true;
+    };
+    if (ok) ok = issue_sp(0);
+    for (int n = 0; n < n_work && ok; ++n) {
+      const int s = n % C::kQStages;
+      if (!warp_wait_b(ps_ready, n & 1, sAbort, budget)) { ok = false; break; }
+      tc_fence_after_sync();
+      if (leader) {
+        // dV += P^T dO, dK += dS^T Q; then the stage is free
+        issue_split_a_gemm<D>(tdV, tS, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), n > 0);
+        issue_split_a_gemm<D>(tdK, tDP, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), n > 0);
+        tc_commit(&q_empty[s]);
+      }
+      // the next S^T / dP^T overwrite what these GEMMs read: issued after
+      // them by the same thread, they run after them
+      if (n + 1 < n_work && !issue_sp(n + 1)) { ok = false; break; }
+    }
+    if (ok && leader) tc_commit(acc_done);
+    if (leader) {
+      tc_commit(drain);
+      drain_wait_b(drain, 0, budget);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // -------------------------------------------------------- TMA producer
+    const bool leader = elect_one();
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    int issued = 0;
+    bool ok = n_work > 0;
+    if (ok && leader) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+      tma_load_tile<D>(sK, &p.tm_k, kv_full, kv0, zkv, pol_kv);
+      tma_load_tile<D>(sV, &p.tm_v, kv_full, kv0, zkv, pol_kv);
+    }
+    for (int qb = 0; qb < n_qb && ok; ++qb) {
+      const int r0 = qb * kRows;
+      if (!qblock_sees(p, r0, kv0)) continue;
+      const int s = issued % C::kQStages;
+      const int round = issued / C::kQStages;
+      if (round > 0 && !warp_wait_b(&q_empty[s], (round - 1) & 1, sAbort, budget)) {
+        ok = false;
+        break;
+      }
+      if (leader) {
+        mbar_arrive_expect_tx(&q_full[s], 2 * C::kTileBytes + 2 * C::kVecBytes);
+        tma_load_tile<D>(stage_q(s), &p.tm_q, &q_full[s], r0, zkv, pol_q);
+        tma_load_tile<D>(stage_do(s), &p.tm_do, &q_full[s], r0, zkv, pol_q);
+        const size_t vo = (size_t)zkv * p.Rp + r0;
+        bulk_load(stage_lse(s), p.lse2 + vo, C::kVecBytes, &q_full[s]);
+        bulk_load(stage_delta(s), p.delta + vo, C::kVecBytes, &q_full[s]);
+      }
+      ++issued;
+    }
+    if (leader) {
+      if (n_work > 0) drain_wait_b(kv_full, 0, budget);
+      const int first = issued > C::kQStages ? issued - C::kQStages : 0;
+      for (int t = first; t < issued; ++t)
+        drain_wait_b(&q_full[t % C::kQStages], (t / C::kQStages) & 1, budget);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
+  if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_bwd_status, 0, (int)ATTN_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw_b[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_b) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + C::kKVStages;
+  uint64_t* sp_full = kv_empty + C::kKVStages;
+  uint64_t* ds_ready = sp_full + 1;
+  uint64_t* acc_done = sp_full + 2;
+  uint64_t* drain = sp_full + 3;
+  uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscQ);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscQ + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t budget = p.timeout_ns;
+
+  // query blocks last to first, so the longest causal blocks start first
+  const int n_qb = (p.R + kRows - 1) / kRows;
+  const int r0 = (n_qb - 1 - (int)blockIdx.x) * kRows;
+  const int zkv = blockIdx.y;
+  int kv_end = p.S_kv;
+  if (p.causal) {
+    const int last = min(r0 + kRows, p.R) - 1;
+    kv_end = min(p.S_kv, (r0 / p.S_q == last / p.S_q) ? last % p.S_q + 1 : p.S_q);
+  }
+  const int n_kb = (kv_end + kRows - 1) / kRows;   // >= 1: every row sees key 0
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kKVStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ds_ready, 2 * 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *sAbort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(sTmemBase, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *sTmemBase;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDO = smem + C::kOffDO;
+  auto stage_k = [&](int s) { return smem + C::kOffKVRing + s * 2 * C::kTileBytes; };
+  auto stage_v = [&](int s) { return stage_k(s) + C::kTileBytes; };
+
+  if (warp < 8) {
+    // -------------------------------------------------------- elementwise
+    const int w = warp >> 2;                       // key columns 64w .. 64w + 63
+    const int r = (warp & 3) * 32 + lane;          // query row within the block
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int rho = r0 + r;
+    const bool row_ok = rho < p.R;
+    const size_t vo = (size_t)zkv * p.Rp + rho;    // in the padded layout (rho < Rp)
+    const float lse2 = p.lse2[vo];
+    const float dl = p.delta[vo];
+    const int pos = rho % p.S_q;
+    const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kb; ++j) {
+      if (!warp_wait_b(sp_full, j & 1, sAbort, budget)) { ok = false; break; }
+      tc_fence_after_sync();
+      const int kb0 = j * kRows;
+      const bool masked = !row_ok || (kb0 + kRows > key_limit);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * w + 32 * c;
+        uint32_t sv[32], dp[32];
+        tmem_ld_x32(tmem + lane_base + C::kTmS + col0, sv);
+        tmem_ld_x32(tmem + lane_base + C::kTmDP + col0, dp);
+        tmem_ld_wait();
+        reg_after_wait(sv);
+        reg_after_wait(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float dsr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = col0 + 2 * i + h;
+            float pv = ex2_approx(u2f_b(sv[2 * i + h]) * sl2 - lse2);
+            if (masked) pv = (row_ok && kb0 + col < key_limit) ? pv : 0.f;
+            dsr[h] = pv * (u2f_b(dp[2 * i + h]) - dl);
+          }
+          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
+        }
+        // dS of these 32 keys: columns 64w + 16c .. of the S region
+        tmem_st_x16(tmem + lane_base + C::kTmS + 64 * w + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(ds_ready);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && warp_wait_b(acc_done, 0, sAbort, budget)) {
+      tc_fence_after_sync();
+      uint16_t* dst = static_cast<uint16_t*>(p.dq) + ((size_t)zkv * p.R + rho) * D + (D / 2) * w;
+      const uint32_t acc = tmem + lane_base + C::kTmAcc0 + (D / 2) * w;
+#pragma unroll
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(acc + ch * 32, v);
+        tmem_ld_wait();
+        reg_after_wait(v);
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+          const float mult = p.scale;
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            uint4 val;
+            val.x = pack_bf16x2(u2f_b(v[qd * 8 + 0]) * mult, u2f_b(v[qd * 8 + 1]) * mult);
+            val.y = pack_bf16x2(u2f_b(v[qd * 8 + 2]) * mult, u2f_b(v[qd * 8 + 3]) * mult);
+            val.z = pack_bf16x2(u2f_b(v[qd * 8 + 4]) * mult, u2f_b(v[qd * 8 + 5]) * mult);
+            val.w = pack_bf16x2(u2f_b(v[qd * 8 + 6]) * mult, u2f_b(v[qd * 8 + 7]) * mult);
+            d4[qd] = val;
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // -------------------------------------------------------- tensor-core issuer
+    const bool leader = elect_one();
+    const uint64_t dQd = kmajor_tile_desc(smem_u32(sQ));
+    const uint64_t dOd = kmajor_tile_desc(smem_u32(sDO));
+    const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP, tdQ = tmem + C::kTmAcc0;
+    bool ok = warp_wait_b(q_full, 0, sAbort, budget);
+    auto issue_sp = [&](int j) -> bool {
+      const int s = j % C::kKVStages;
+      if (!warp_wait_b(&kv_full[s], (j / C::kKVStages) & 1, sAbort, budget)) return false;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_qk_gemm<D>(tS, dQd, kmajor_tile_desc(smem_u32(stage_k(s))));
+        issue_qk_gemm<D>(tDP, dOd, kmajor_tile_desc(smem_u32(stage_v(s))));
+        tc_commit(sp_full);
+      }
+      return true;
+    };
+    if (ok) ok = issue_sp(0);
+    for (int j = 0; j < n_kb && ok; ++j) {
+      const int s = j % C::kKVStages;
+      if (!warp_wait_b(ds_ready, j & 1, sAbort, budget)) { ok = false; break; }
+      tc_fence_after_sync();
+      if (leader) {
+        issue_split_a_gemm<D>(tdQ, tS, mnmajor_tile_desc<D>(smem_u32(stage_k(s))), j > 0);
+        tc_commit(&kv_empty[s]);
+      }
+      if (j + 1 < n_kb && !issue_sp(j + 1)) { ok = false; break; }
+    }
+    if (ok && leader) tc_commit(acc_done);
+    if (leader) {
+      tc_commit(drain);
+      drain_wait_b(drain, 0, budget);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // -------------------------------------------------------- TMA producer
+    const bool leader = elect_one();
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    if (leader) {
+      mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
+      tma_load_tile<D>(sQ, &p.tm_q, q_full, r0, zkv, pol_q);
+      tma_load_tile<D>(sDO, &p.tm_do, q_full, r0, zkv, pol_q);
+    }
+    int issued = 0;
+    for (int j = 0; j < n_kb; ++j) {
+      const int s = j % C::kKVStages;
+      const int round = j / C::kKVStages;
+      if (round > 0 && !warp_wait_b(&kv_empty[s], (round - 1) & 1, sAbort, budget)) break;
+      if (leader) {
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::kTileBytes);
+        tma_load_tile<D>(stage_k(s), &p.tm_k, &kv_full[s], j * kRows, zkv, pol_kv);
+        tma_load_tile<D>(stage_v(s), &p.tm_v, &kv_full[s], j * kRows, zkv, pol_kv);
+      }
+      ++issued;
+    }
+    if (leader) {
+      drain_wait_b(q_full, 0, budget);
+      const int first = issued > C::kKVStages ? issued - C::kKVStages : 0;
+      for (int t = first; t < issued; ++t)
+        drain_wait_b(&kv_full[t % C::kKVStages], (t / C::kKVStages) & 1, budget);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
+  if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_bwd_status, 0, (int)ATTN_ERR_TIMEOUT);
+}
+
+namespace {
+
+std::mutex g_bwd_mu;
+bool g_bwd_attr[2][64] = {};  // [D == 128][device]
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, const float* lse,
+                         cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_bwd_mu);
+    if (!g_bwd_attr[D == 128][dev]) {
+      err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemKV);
+      if (err != cudaSuccess) return err;
+      err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemQ);
+      if (err != cudaSuccess) return err;
+      g_bwd_attr[D == 128][dev] = true;
+    }
+  }
+  const long long prep_rows = (long long)p.groups * p.Rp;
+  attn_bwd_prep_kernel<D><<<(unsigned)((prep_rows + 7) / 8), 256, 0, stream>>>(
+      p, static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const dim3 grid_kv((p.S_kv + kRows - 1) / kRows, p.groups);
+  attn_bwd_dkdv_kernel<D><<<grid_kv, kThreadsB, C::kSmemKV, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const dim3 grid_q((p.R + kRows - 1) / kRows, p.groups);
+  attn_bwd_dq_kernel<D><<<grid_q, kThreadsB, C::kSmemQ, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdParams& p, int D, const void* o, const void* dout,
+                            const float* lse, cudaStream_t stream) {
+  if (D == 128) return launch_bwd_d<128>(p, o, dout, lse, stream);
+  if (D == 64) return launch_bwd_d<64>(p, o, dout, lse, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_bwd_status(int* status, bool reset) {
+  cudaError_t err = cudaMemcpyFromSymbol(status, g_bwd_status, sizeof(int));
+  if (err != cudaSuccess) return err;
+  if (reset) {
+    const int zero = 0;
+    err = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int));
+  }
+  return err;
+}
+
+}  // namespace attnpipe

@@ -61,6 +61,30 @@ struct AttnParams {
   int fault_drop_block;
 };
 
+// Everything the backward kernels read.  Q and dO are viewed as [B*H_kv,
+// R, D] (row groups, as in the forward), K and V as [B*H_kv, S_kv, D].  The
+// per-row vectors live in a padded per-group layout [groups, Rp] with Rp = R
+// rounded up to 128, so every 128-row block of them is 16-byte aligned.
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  void* dq;           // [B, H_q, S_q, D] bf16
+  void* dk;           // [B, H_kv, S_kv, D] bf16
+  void* dv;           // [B, H_kv, S_kv, D] bf16
+  float* lse2;        // [groups, Rp]: LSE * log2(e) (workspace)
+  float* delta;       // [groups, Rp]: D_i = dO_i . O_i (workspace)
+  int B, H_q, H_kv, S_q, S_kv, causal;
+  int R, Rp, groups;
+  float scale, scale_log2;
+  unsigned long long timeout_ns;
+};
+
+// Queues the three backward kernels (D_i, dK/dV, dQ) on `stream`.
+cudaError_t launch_attn_bwd(const BwdParams& p, int D, const void* o, const void* dout,
+                            const float* lse, cudaStream_t stream);
+
+// Reads (and optionally clears) the backward kernels' status word.
+cudaError_t read_bwd_status(int* status, bool reset);
+
 // Events stamped by the trace instantiation, one slot per KV block j.
 enum TraceEvent : int {
   kEvSm0Wake = 0,   // softmax 0: S_0(j) ready (wait returned)

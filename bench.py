@@ -440,6 +440,168 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_bwd(args, w):
+    """The backward (attn_bwd: three kernels) on the same workload: one step =
+    dQ, dK, dV for one upstream gradient, inputs (q, k, v, O, LSE, dO)
+    resident in HBM.  FLOPs: the five GEMMs of a FlashAttention backward,
+    2.5 x the forward's count (halved when causal)."""
+    import torch
+    import attention_pipelining_gb300 as ap
+    from attention_pipelining_gb300.synthetic import make_workload
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    ap.build()
+    dev = torch.device("cuda", local)
+    q_cpu, k_cpu, v_cpu = make_workload(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    do_cpu = torch.randn(q_cpu.shape, generator=g).to(torch.bfloat16)
+    q, k, v, dout = (t.to(dev) for t in (q_cpu, k_cpu, v_cpu, do_cpu))
+    o, lse = ap.attn_fwd(q, k, v, w.causal, w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(ap.bwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ap.attn_bwd(q, k, v, o, lse, dout, w.causal, w.scale, workspace=ws, out=(dq, dk, dv),
+                    stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, world)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+
+    # end to end: pinned host inputs in, gradients back, copies timed
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = [t.pin_memory() for t in (q_cpu, k_cpu, v_cpu, do_cpu)]
+    o_h, lse_h = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    dev_in = [q, k, v, dout]
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        o.copy_(o_h, non_blocking=True)
+        lse.copy_(lse_h, non_blocking=True)
+        step()
+        for h_, d_ in zip(host_out, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    if rank != 0:
+        return
+    peak, peak_sustained, peak_kind = load_peaks()
+    flops = 2.5 * w.flops
+    per_launch = t_local / args.steps
+    achieved = flops / per_launch / 1e12
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dout, o, lse))
+    out_bytes = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
+    line = {
+        "metric": "attention bwd TFLOP/s (bf16, fp32 acc; 2.5x the forward's FLOPs)",
+        "value": world * flops * args.steps / t / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "pass": "bwd",
+        "config": {
+            "workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S_q": w.S_q,
+            "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
+            "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
+                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+        },
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_kind": f"{peak_kind} bf16 dense (burst)",
+            "frac_of_sustained": achieved / peak_sustained,
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "kernel": "attn_bwd_prep + attn_bwd_dkdv + attn_bwd_dq, timed together",
+        },
+        "e2e": {
+            "value": world * flops * e2e_steps / t_e2e / 1e12,
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out_bytes,
+            "steps": e2e_steps,
+        },
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline_bwd(q_cpu, k_cpu, v_cpu, do_cpu, w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_bwd(q, k, v, dout, w, target_s: float = 12.0) -> dict:
+    """The fp64 backward oracle on a bounded sample: dQ of random query rows
+    (each formed from its full softmax row), counted at 2.5x the rows' forward
+    FLOPs."""
+    import oracle
+    bo = oracle.bwd_default()
+    n = 8
+    while True:
+        rows = sample_rows(w, n, seed=1)
+        t0 = time.perf_counter()
+        bo.dq_rows(q, k, v, dout, rows, w.causal, w.scale)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or n >= w.B * w.H_q * w.S_q:
+            break
+        n = min(w.B * w.H_q * w.S_q, max(n * 2, int(n * target_s / max(dt, 1e-3) / 2)))
+    flops = 2.5 * row_flops(w, rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.default().num_threads(),
+            "kind": "oracle",
+            "sample": f"dQ of {len(rows)} random query rows of {w.name} (each over its full "
+                      f"visible key range), fp64, {dt:.1f} s"}
+
+
 def run_trace(args, w):
     """Timeline of the first CTAs from the trace instantiation (not a bench line)."""
     import torch
@@ -474,6 +636,8 @@ def main(argv=None):
     ap_.add_argument("--trace", type=int, default=0,
                      help="print a timeline summary of the first N CTAs instead of a bench line")
     ap_.add_argument("--trace-out", default="", help="also save the raw trace (.npy)")
+    ap_.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                     help="bwd: time the backward (attn_bwd) instead of the forward")
     args = ap_.parse_args(argv)
     if args.warmup < 3:
         ap_.error("--warmup must be >= 3")
@@ -483,6 +647,8 @@ def main(argv=None):
         return
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.which == "bwd":
+        run_bwd(args, w)
     else:
         run_ours(args, w)
     world, _, _ = dist_env()

@@ -157,13 +157,52 @@ attn_status_t attn_fwd_splitkv_noalloc(const void *q, const void *k, const void 
 /* Bytes of the built-in scratch array attn_fwd_splitkv_noalloc uses. */
 size_t attn_splitkv_noalloc_capacity(void);
 
+/*
+ * Backward of attn_fwd: the gradients of L = sum(O * dO) with respect to Q, K
+ * and V, given the forward's O and LSE and the upstream gradient dO.  With
+ * P_ij = exp(scale q_i . k_j - LSE_i) (0 where masked), D_i = dO_i . O_i,
+ * dP_ij = dO_i . v_j and dS_ij = P_ij (dP_ij - D_i):
+ *
+ *     dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i,
+ *     dQ_i = scale sum_j dS_ij k_j,
+ *
+ * where dK_j and dV_j also sum over the H_q / H_kv query heads sharing key /
+ * value head j's head.  The backward on Blackwell is the subject of "GPU软件
+ * 流水线与Warp Specialization优化技术解析", section 3.2; the pages give no
+ * formulas, these are the chain rule through the forward's definition.
+ *
+ *   q, k, v     as for attn_fwd (device, read)
+ *   o, lse      attn_fwd's outputs for the same q, k, v, causal, scale (read)
+ *   dout        [B, H_q, S_q, D] bf16, device, read
+ *   dq          [B, H_q, S_q, D] bf16, device, written
+ *   dk, dv      [B, H_kv, S_kv, D] bf16, device, written
+ *   workspace   caller-owned device scratch, 256-byte aligned, of at least
+ *               attn_bwd_workspace_bytes(B, H_q, H_kv, S_q) bytes (per-row
+ *               D_i and LSE; no need to clear it)
+ *
+ * Arithmetic: bf16 operands, fp32 accumulation; P and dS are rounded to
+ * bf16 before the GEMMs that consume them.  Three kernels are queued on
+ * `stream`; the workspace must not be shared with concurrent calls.  Errors
+ * as attn_fwd, plus ATTN_ERR_INVALID_ARG for a null dout / dq / dk / dv /
+ * workspace or a too small workspace, ATTN_ERR_MISALIGNED for a workspace not
+ * 256-byte aligned, and ATTN_ERR_UNSUPPORTED for B * H_kv > 65535.
+ */
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                       void *workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                       int S_q, int S_kv, int D, int causal, float scale, attn_stream_t stream);
+
+/* Workspace bytes attn_bwd needs (0 if the arguments are invalid). */
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
+
 /* Static English description of a status code (never NULL). */
 const char *attn_status_string(attn_status_t status);
 
 /*
- * Reads the device-side status word of the current device: ATTN_OK, or
- * ATTN_ERR_TIMEOUT if a launch since the last reset gave up on a wait (that
- * launch's outputs are then unspecified).  Synchronises the device.  With
+ * Reads the device-side status words of the current device (forward,
+ * backward and self-test kernels): ATTN_OK, or ATTN_ERR_TIMEOUT if a launch
+ * since the last reset gave up on a wait (that launch's outputs are then
+ * unspecified).  Synchronises the device.  With
  * reset != 0 the word is cleared afterwards.
  */
 attn_status_t attn_device_status(int *status_out, int reset);
