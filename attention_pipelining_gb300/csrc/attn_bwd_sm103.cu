@@ -58,19 +58,39 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, uin
 
 __device__ __forceinline__ float u2f_b(uint32_t x) { return __uint_as_float(x); }
 
-// Acc[tmem, 128 x D fp32] (+)= A B where A [128 x 128] bf16 sits in tensor
-// memory split by warpgroup: K elements 0-63 in columns [0, 32), 64-127 in
-// [64, 96) (two per column), and B is a [128 x D] tile used MN-major (D
-// contiguous), given its MN-major tile descriptor: the forward's PV GEMM
-// with A read from the two halves.
+// The work of a 128 x 128 block is done in two halves h = 0, 1 of 64
+// columns, so the elementwise warpgroups work on one half while the tensor
+// core runs the other half's GEMMs.
+
+// C[tmem, 128 x 64 fp32] = A B_h^T: A a [128 x D] tile, B_h rows 64h..64h+63
+// of a [128 x D] tile, both K-major (given as tile descriptors; the half's
+// rows start 64 rows = 8 KB into each 128-byte-swizzled slab).
 template <int D>
-__device__ __forceinline__ void issue_split_a_gemm(uint32_t d_tmem, uint32_t a_tmem,
-                                                   uint64_t b_desc, bool accumulate) {
+__device__ __forceinline__ void issue_qk_half(uint32_t c_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              int h) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64, false, false);
+  const uint64_t b_half = b_desc + (uint64_t)((h * 64 * 128) >> 4);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4);
+    mma_ss(c_tmem, a_desc + off, b_half + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Acc[tmem, 128 x D fp32] (+)= A_h B_h: A_h [128 x 64] bf16 in tensor memory,
+// two per column, written by the elementwise warpgroups (warpgroup w's 32
+// elements at columns 32w .. 32w + 15 from `a_tmem`); B_h rows 64h..64h+63
+// of a [128 x D] tile used MN-major (D contiguous), given its MN-major tile
+// descriptor.  `accumulate` = false overwrites Acc.
+template <int D>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              int h, bool accumulate) {
   constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
 #pragma unroll
-  for (int kk = 0; kk < kTileRows / 16; ++kk) {
-    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
-           b_desc + (uint64_t)((kk * 2048) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 4; ++kk) {
+    mma_ts(d_tmem, a_tmem + (kk >> 1) * 32 + (kk & 1) * 8,
+           b_desc + (uint64_t)(((4 * h + kk) * 2048) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -85,8 +105,8 @@ struct BwdCfg {
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQRing = 2 * kTileBytes;
   static constexpr int kOffBarKV = kOffQRing + kQStages * kQStageBytes;
-  // kv_full, q_full[S], q_empty[S], sp_full, ps_ready, acc_done, drain
-  static constexpr int kNumBarsKV = 2 * kQStages + 5;
+  // kv_full, q_full[S], q_empty[S], sp_full[2], ps_ready[2], acc_done, drain
+  static constexpr int kNumBarsKV = 2 * kQStages + 7;
   static constexpr int kOffMiscKV = kOffBarKV + kNumBarsKV * 8;
   static constexpr int kSmemKV = kOffMiscKV + 16 + 1024;
   // dQ kernel: Q, dO, then a ring of (K, V) stages
@@ -95,8 +115,8 @@ struct BwdCfg {
   static constexpr int kOffDO = kTileBytes;
   static constexpr int kOffKVRing = 2 * kTileBytes;
   static constexpr int kOffBarQ = kOffKVRing + kKVStages * 2 * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], sp_full, ds_ready, acc_done, drain
-  static constexpr int kNumBarsQ = 2 * kKVStages + 5;
+  // q_full, kv_full[S], kv_empty[S], sp_full[2], ds_ready[2], acc_done, drain
+  static constexpr int kNumBarsQ = 2 * kKVStages + 7;
   static constexpr int kOffMiscQ = kOffBarQ + kNumBarsQ * 8;
   static constexpr int kSmemQ = kOffMiscQ + 16 + 1024;
   // tensor memory: S (or S^T) [0,128), dP [128,256), accumulators after
@@ -175,10 +195,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::kQStages;
-  uint64_t* sp_full = q_empty + C::kQStages;
-  uint64_t* ps_ready = sp_full + 1;
-  uint64_t* acc_done = sp_full + 2;
-  uint64_t* drain = sp_full + 3;
+  uint64_t* sp_full = q_empty + C::kQStages;   // [half]: S^T, dP^T of the half computed
+  uint64_t* ps_ready = sp_full + 2;            // [half]: P^T, dS^T of the half stored
+  uint64_t* acc_done = sp_full + 4;
+  uint64_t* drain = sp_full + 5;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscKV);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscKV + 4);
   const int warp = threadIdx.x >> 5;
@@ -198,8 +218,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(sp_full, 1);
-    mbar_init(ps_ready, 2 * 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sp_full[h], 1);
+      mbar_init(&ps_ready[h], 2 * 128);
+    }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *sAbort = 0;
@@ -226,7 +248,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
 
   if (warp < 8) {
     // -------------------------------------------------------- elementwise
-    const int w = warp >> 2;                       // columns 64w .. 64w + 63
+    // half h of a block is queries 64h .. 64h + 63; warpgroup w takes
+    // queries 64h + 32w .. 64h + 32w + 31 of it
+    const int w = warp >> 2;
     const int r = (warp & 3) * 32 + lane;          // key row within the block
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kv0 + r;
@@ -237,13 +261,6 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
       const int r0 = qb * kRows;
       if (!qblock_sees(p, r0, kv0)) continue;
       const int s = n % C::kQStages;
-      if (!warp_wait_b(sp_full, n & 1, sAbort, budget)) { ok = false; break; }
-      // the stage's LSE and D vectors arrived with its tiles: observe that
-      // phase here too before reading them
-      if (!warp_wait_b(&q_full[s], (n / C::kQStages) & 1, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
-      const float* lse2 = stage_lse(s);
-      const float* dl = stage_delta(s);
       // masking: rows past R, keys past S_kv, and (causal) keys after a row's
       // position; a block needs none when every row sees every key
       bool masked = (r0 + kRows > p.R) || (kv0 + kRows > p.S_kv);
@@ -253,30 +270,44 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         const bool one_head = (base_pos + kRows <= p.S_q);
         masked = masked || !(one_head && base_pos >= kv0 + kRows - 1);
       }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * w + 32 * c;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait_b(&sp_full[h], n & 1, sAbort, budget)) { ok = false; break; }
+        // the stage's LSE and D vectors arrived with its tiles: observe that
+        // phase here too before reading them
+        if (h == 0 && !warp_wait_b(&q_full[s], (n / C::kQStages) & 1, sAbort, budget)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int col0 = 64 * h + 32 * w;            // first query of this thread's slice
         uint32_t sv[32], dp[32];
         tmem_ld_x32(tmem + lane_base + C::kTmS + col0, sv);
         tmem_ld_x32(tmem + lane_base + C::kTmDP + col0, dp);
+        const float4* lse4 = reinterpret_cast<const float4*>(stage_lse(s) + col0);
+        const float4* dl4 = reinterpret_cast<const float4*>(stage_delta(s) + col0);
         tmem_ld_wait();
         reg_after_wait(sv);
         reg_after_wait(dp);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pr[2], dsr[2];
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = lse4[i4];
+          const float4 d4 = dl4[i4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], dsr[4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = col0 + 2 * i + h;
-            float pv = ex2_approx(u2f_b(sv[2 * i + h]) * sl2 - lse2[col]);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * i4 + e;                // element of the slice
+            float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lv[e]);
             if (masked) {
-              const int rho = r0 + col;
+              const int rho = r0 + col0 + c;
               bool vis = (rho < p.R) && (key < p.S_kv);
               if (p.causal) {
                 int pos;
                 if (p.S_q >= kRows) {
-                  pos = base_pos + col;
+                  pos = base_pos + col0 + c;
                   if (pos >= p.S_q) pos -= p.S_q;
                 } else {
                   pos = rho % p.S_q;
@@ -285,20 +316,22 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
               }
               pv = vis ? pv : 0.f;
             }
-            pr[h] = pv;
-            dsr[h] = pv * (u2f_b(dp[2 * i + h]) - dl[col]);
+            pr[e] = pv;
+            dsr[e] = pv * (u2f_b(dp[c]) - dv4[e]);
           }
-          pk[i] = pack_bf16x2(pr[0], pr[1]);
-          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
+          pk[2 * i4] = pack_bf16x2(pr[0], pr[1]);
+          pk[2 * i4 + 1] = pack_bf16x2(pr[2], pr[3]);
+          dk[2 * i4] = pack_bf16x2(dsr[0], dsr[1]);
+          dk[2 * i4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
         }
-        // P^T and dS^T of these 32 queries: columns 64w + 16c .. in the
-        // S^T and dP^T regions (this warpgroup's own, already-read columns)
-        tmem_st_x16(tmem + lane_base + C::kTmS + 64 * w + 16 * c, pk);
-        tmem_st_x16(tmem + lane_base + C::kTmDP + 64 * w + 16 * c, dk);
+        // P^T and dS^T of the slice: 16 columns from col0 in the S^T and
+        // dP^T regions (this warpgroup's own, already-read columns)
+        tmem_st_x16(tmem + lane_base + C::kTmS + col0, pk);
+        tmem_st_x16(tmem + lane_base + C::kTmDP + col0, dk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&ps_ready[h]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(ps_ready);
       ++n;
     }
     // ---------------------------------------------------------- epilogue
@@ -349,32 +382,50 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP;
     const uint32_t tdV = tmem + C::kTmAcc0, tdK = tmem + C::kTmAcc1;
     bool ok = n_work > 0 && warp_wait_b(kv_full, 0, sAbort, budget);
-    // S^T, dP^T of work item n (its Q / dO stage must be loaded)
-    auto issue_sp = [&](int n) -> bool {
+    // S^T and dP^T of half h of work item n (its Q / dO stage is loaded)
+    auto issue_sp = [&](int n, int h) {
       const int s = n % C::kQStages;
-      if (!warp_wait_b(&q_full[s], (n / C::kQStages) & 1, sAbort, budget)) return false;
-      tc_fence_after_sync();
       if (leader) {
-        issue_qk_gemm<D>(tS, dK, kmajor_tile_desc(smem_u32(stage_q(s))));
-        issue_qk_gemm<D>(tDP, dV, kmajor_tile_desc(smem_u32(stage_do(s))));
-        tc_commit(sp_full);
+        issue_qk_half<D>(tS + 64 * h, dK, kmajor_tile_desc(smem_u32(stage_q(s))), h);
+        issue_qk_half<D>(tDP + 64 * h, dV, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+        tc_commit(&sp_full[h]);
       }
-      return true;
     };
-    if (ok) ok = issue_sp(0);
+    if (ok && warp_wait_b(&q_full[0], 0, sAbort, budget)) {
+      tc_fence_after_sync();
+      issue_sp(0, 0);
+      issue_sp(0, 1);
+    } else {
+      ok = false;
+    }
     for (int n = 0; n < n_work && ok; ++n) {
       const int s = n % C::kQStages;
-      if (!warp_wait_b(ps_ready, n & 1, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
-      if (leader) {
-        // dV += P^T dO, dK += dS^T Q; then the stage is free
-        issue_split_a_gemm<D>(tdV, tS, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), n > 0);
-        issue_split_a_gemm<D>(tdK, tDP, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), n > 0);
-        tc_commit(&q_empty[s]);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait_b(&ps_ready[h], n & 1, sAbort, budget)) { ok = false; break; }
+        tc_fence_after_sync();
+        if (leader) {
+          // dV += P^T dO and dK += dS^T Q over this half's 64 queries
+          issue_pv_half<D>(tdV, tS + 64 * h, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), h,
+                           n > 0 || h > 0);
+          issue_pv_half<D>(tdK, tDP + 64 * h, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h,
+                           n > 0 || h > 0);
+          if (h == 1) tc_commit(&q_empty[s]);  // both halves read: the stage is free
+        }
+        // the next item's half h overwrites what these GEMMs read: issued
+        // after them by the same thread, it runs after them
+        if (n + 1 < n_work) {
+          if (h == 0) {
+            if (!warp_wait_b(&q_full[(n + 1) % C::kQStages], ((n + 1) / C::kQStages) & 1,
+                             sAbort, budget)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+          }
+          issue_sp(n + 1, h);
+        }
       }
-      // the next S^T / dP^T overwrite what these GEMMs read: issued after
-      // them by the same thread, they run after them
-      if (n + 1 < n_work && !issue_sp(n + 1)) { ok = false; break; }
     }
     if (ok && leader) tc_commit(acc_done);
     if (leader) {
@@ -441,10 +492,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + C::kKVStages;
-  uint64_t* sp_full = kv_empty + C::kKVStages;
-  uint64_t* ds_ready = sp_full + 1;
-  uint64_t* acc_done = sp_full + 2;
-  uint64_t* drain = sp_full + 3;
+  uint64_t* sp_full = kv_empty + C::kKVStages;  // [half]: S, dP of the half computed
+  uint64_t* ds_ready = sp_full + 2;             // [half]: dS of the half stored
+  uint64_t* acc_done = sp_full + 4;
+  uint64_t* drain = sp_full + 5;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscQ);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscQ + 4);
   const int warp = threadIdx.x >> 5;
@@ -468,8 +519,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(sp_full, 1);
-    mbar_init(ds_ready, 2 * 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sp_full[h], 1);
+      mbar_init(&ds_ready[h], 2 * 128);
+    }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *sAbort = 0;
@@ -502,14 +555,16 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int j = 0; j < n_kb; ++j) {
-      if (!warp_wait_b(sp_full, j & 1, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
+    for (int j = 0; j < n_kb && ok; ++j) {
       const int kb0 = j * kRows;
       const bool masked = !row_ok || (kb0 + kRows > key_limit);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * w + 32 * c;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait_b(&sp_full[h], j & 1, sAbort, budget)) { ok = false; break; }
+        tc_fence_after_sync();
+        // half h is keys 64h .. 64h + 63 of the block; this warpgroup's
+        // slice is keys 64h + 32w .. 64h + 32w + 31
+        const int col0 = 64 * h + 32 * w;
         uint32_t sv[32], dp[32];
         tmem_ld_x32(tmem + lane_base + C::kTmS + col0, sv);
         tmem_ld_x32(tmem + lane_base + C::kTmDP + col0, dp);
@@ -521,20 +576,21 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
         for (int i = 0; i < 16; ++i) {
           float dsr[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = col0 + 2 * i + h;
-            float pv = ex2_approx(u2f_b(sv[2 * i + h]) * sl2 - lse2);
-            if (masked) pv = (row_ok && kb0 + col < key_limit) ? pv : 0.f;
-            dsr[h] = pv * (u2f_b(dp[2 * i + h]) - dl);
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * i + e;
+            float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lse2);
+            if (masked) pv = (row_ok && kb0 + col0 + c < key_limit) ? pv : 0.f;
+            dsr[e] = pv * (u2f_b(dp[c]) - dl);
           }
           dk[i] = pack_bf16x2(dsr[0], dsr[1]);
         }
-        // dS of these 32 keys: columns 64w + 16c .. of the S region
-        tmem_st_x16(tmem + lane_base + C::kTmS + 64 * w + 16 * c, dk);
+        // dS of the slice: 16 columns from col0 of the S region (this
+        // warpgroup's own, already-read columns)
+        tmem_st_x16(tmem + lane_base + C::kTmS + col0, dk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&ds_ready[h]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(ds_ready);
     }
     // ---------------------------------------------------------- epilogue
     if (ok && warp_wait_b(acc_done, 0, sAbort, budget)) {
@@ -569,27 +625,47 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     const uint64_t dOd = kmajor_tile_desc(smem_u32(sDO));
     const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP, tdQ = tmem + C::kTmAcc0;
     bool ok = warp_wait_b(q_full, 0, sAbort, budget);
-    auto issue_sp = [&](int j) -> bool {
+    // S and dP of half h of key block j (its K / V stage is loaded)
+    auto issue_sp = [&](int j, int h) {
       const int s = j % C::kKVStages;
-      if (!warp_wait_b(&kv_full[s], (j / C::kKVStages) & 1, sAbort, budget)) return false;
-      tc_fence_after_sync();
       if (leader) {
-        issue_qk_gemm<D>(tS, dQd, kmajor_tile_desc(smem_u32(stage_k(s))));
-        issue_qk_gemm<D>(tDP, dOd, kmajor_tile_desc(smem_u32(stage_v(s))));
-        tc_commit(sp_full);
+        issue_qk_half<D>(tS + 64 * h, dQd, kmajor_tile_desc(smem_u32(stage_k(s))), h);
+        issue_qk_half<D>(tDP + 64 * h, dOd, kmajor_tile_desc(smem_u32(stage_v(s))), h);
+        tc_commit(&sp_full[h]);
       }
-      return true;
     };
-    if (ok) ok = issue_sp(0);
+    if (ok && warp_wait_b(&kv_full[0], 0, sAbort, budget)) {
+      tc_fence_after_sync();
+      issue_sp(0, 0);
+      issue_sp(0, 1);
+    } else {
+      ok = false;
+    }
     for (int j = 0; j < n_kb && ok; ++j) {
       const int s = j % C::kKVStages;
-      if (!warp_wait_b(ds_ready, j & 1, sAbort, budget)) { ok = false; break; }
-      tc_fence_after_sync();
-      if (leader) {
-        issue_split_a_gemm<D>(tdQ, tS, mnmajor_tile_desc<D>(smem_u32(stage_k(s))), j > 0);
-        tc_commit(&kv_empty[s]);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait_b(&ds_ready[h], j & 1, sAbort, budget)) { ok = false; break; }
+        tc_fence_after_sync();
+        if (leader) {
+          // dQ += dS K over this half's 64 keys
+          issue_pv_half<D>(tdQ, tS + 64 * h, mnmajor_tile_desc<D>(smem_u32(stage_k(s))), h,
+                           j > 0 || h > 0);
+          if (h == 1) tc_commit(&kv_empty[s]);  // both halves read: the stage is free
+        }
+        // the next block's half h overwrites the dS these GEMMs read
+        if (j + 1 < n_kb) {
+          if (h == 0) {
+            if (!warp_wait_b(&kv_full[(j + 1) % C::kKVStages], ((j + 1) / C::kKVStages) & 1,
+                             sAbort, budget)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+          }
+          issue_sp(j + 1, h);
+        }
       }
-      if (j + 1 < n_kb && !issue_sp(j + 1)) { ok = false; break; }
     }
     if (ok && leader) tc_commit(acc_done);
     if (leader) {
