@@ -266,8 +266,11 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
     return ATTN_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
   if (workspace_bytes < bwd_workspace_bytes(B, H_q, H_kv, S_q)) return ATTN_ERR_INVALID_ARG;
-  // grids: (key blocks, groups) and (query blocks, groups); y is limited to 65535
-  if ((int64_t)B * H_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // grids: key blocks x groups and query blocks x groups CTAs, in one dimension
+  const int64_t R64 = (int64_t)(H_q / H_kv) * S_q;
+  if (((S_kv + 127) / 128) * (int64_t)B * H_kv >= (1ll << 31) ||
+      ((R64 + 127) / 128) * (int64_t)B * H_kv >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
   st = check_device();
   if (st != ATTN_OK) return st;
   BwdParams p;

@@ -205,8 +205,20 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   const int lane = threadIdx.x & 31;
   const uint64_t budget = p.timeout_ns;
 
-  const int kv0 = blockIdx.x * kRows;       // first key of the block
-  const int zkv = blockIdx.y;               // row group = key/value head
+  // CTA -> (key block, row group): with the causal mask the first key
+  // blocks carry the most query blocks, so all groups' first blocks go
+  // first; without it the blocks of one group are adjacent (they share
+  // their Q and dO tiles in L2)
+  const int n_kvb = (p.S_kv + kRows - 1) / kRows;
+  int kvb, zkv;
+  if (p.causal) {
+    kvb = blockIdx.x / p.groups;
+    zkv = blockIdx.x - kvb * p.groups;
+  } else {
+    zkv = blockIdx.x / n_kvb;
+    kvb = blockIdx.x - zkv * n_kvb;
+  }
+  const int kv0 = kvb * kRows;              // first key of the block
   const int n_qb = (p.R + kRows - 1) / kRows;
   // query blocks with work, counted once here (every role walks the same list)
   int n_work = 0;
@@ -502,10 +514,27 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
   const int lane = threadIdx.x & 31;
   const uint64_t budget = p.timeout_ns;
 
-  // query blocks last to first, so the longest causal blocks start first
+  // CTA -> (query block, row group): with the causal mask by cost rank,
+  // longest first (with S_q a multiple of 128 a rank is one position block
+  // of one head of the group, so the group's heads interleave), then group;
+  // without it group-major, query blocks last to first
   const int n_qb = (p.R + kRows - 1) / kRows;
-  const int r0 = (n_qb - 1 - (int)blockIdx.x) * kRows;
-  const int zkv = blockIdx.y;
+  int qb, zkv;
+  if (p.causal) {
+    const int rank = blockIdx.x / p.groups;
+    zkv = blockIdx.x - rank * p.groups;
+    const int hr = p.R / p.S_q;  // heads per group
+    if (p.S_q % kRows == 0) {
+      const int nh = p.S_q / kRows;
+      qb = (rank % hr) * nh + (nh - 1 - rank / hr);
+    } else {
+      qb = n_qb - 1 - rank;
+    }
+  } else {
+    zkv = blockIdx.x / n_qb;
+    qb = n_qb - 1 - (blockIdx.x - zkv * n_qb);
+  }
+  const int r0 = qb * kRows;
   int kv_end = p.S_kv;
   if (p.causal) {
     const int last = min(r0 + kRows, p.R) - 1;
@@ -741,11 +770,11 @@ cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, co
       p, static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 grid_kv((p.S_kv + kRows - 1) / kRows, p.groups);
+  const unsigned grid_kv = (unsigned)((p.S_kv + kRows - 1) / kRows) * (unsigned)p.groups;
   attn_bwd_dkdv_kernel<D><<<grid_kv, kThreadsB, C::kSmemKV, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 grid_q((p.R + kRows - 1) / kRows, p.groups);
+  const unsigned grid_q = (unsigned)((p.R + kRows - 1) / kRows) * (unsigned)p.groups;
   attn_bwd_dq_kernel<D><<<grid_q, kThreadsB, C::kSmemQ, stream>>>(p);
   return cudaGetLastError();
 }

@@ -184,8 +184,8 @@ size_t attn_splitkv_noalloc_capacity(void);
  * bf16 before the GEMMs that consume them.  Three kernels are queued on
  * `stream`; the workspace must not be shared with concurrent calls.  Errors
  * as attn_fwd, plus ATTN_ERR_INVALID_ARG for a null dout / dq / dk / dv /
- * workspace or a too small workspace, ATTN_ERR_MISALIGNED for a workspace not
- * 256-byte aligned, and ATTN_ERR_UNSUPPORTED for B * H_kv > 65535.
+ * workspace or a too small workspace, and ATTN_ERR_MISALIGNED for a workspace
+ * not 256-byte aligned.
  */
 attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
                        const float *lse, const void *dout, void *dq, void *dk, void *dv,
