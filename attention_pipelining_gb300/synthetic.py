@@ -91,3 +91,80 @@ def make_qkv(B: int, H_q: int, H_kv: int, S_q: int, S_kv: int, D: int,
 
 def make_workload(w: Workload):
     return make_qkv(w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.D, w.k_scale, w.seed)
+
+
+# ---------------------------------------------------------------- chunk scan
+
+
+@dataclass(frozen=True)
+class ChunkScanWorkload:
+    """Shapes of the Mamba2 chunk scan: batch B, sequence L, H heads of width
+    P in G groups, chunk length Q."""
+    name: str
+    B: int
+    L: int
+    H: int = 64
+    P: int = 64
+    G: int = 1
+    Q: int = 256
+    seed: int = 0
+
+    @property
+    def nchunks(self) -> int:
+        return self.L // self.Q
+
+    @property
+    def flops(self) -> float:
+        """2 * P multiply-adds per (row, visible key): sum over a chunk of
+        (m + 1) keys for rows m = 0..Q-1."""
+        per_chunk = self.Q * (self.Q + 1) / 2
+        return 2.0 * self.P * per_chunk * self.nchunks * self.B * self.H
+
+    @property
+    def io_bytes(self) -> int:
+        """cb, dA_cs, dt, x read; out written."""
+        cb = self.B * self.nchunks * self.G * self.Q * self.Q * 4
+        vec = 2 * self.B * self.H * self.L * 4
+        x = self.B * self.L * self.H * self.P * 2
+        return cb + vec + 2 * x
+
+    def as_dict(self) -> dict:
+        return asdict(self)
+
+
+# Mamba2-1.3B (64 heads of width 64, one group, chunk 256) at the batch and
+# sequence sizes of the pages' chunk-scan microbenchmarks
+CHUNK_SCAN_WORKLOADS = {
+    w.name: w
+    for w in [
+        ChunkScanWorkload("chunkscan_b1_s1024", 1, 1024),
+        ChunkScanWorkload("chunkscan_b1_s8192", 1, 8192),
+        ChunkScanWorkload("chunkscan_b64_s8192", 64, 8192),
+    ]
+}
+
+CHUNK_SCAN_HEADLINE = "chunkscan_b64_s8192"
+
+
+def make_chunk_scan(B: int, L: int, H: int, P: int, G: int, Q: int, seed: int = 0):
+    """Seeded chunk-scan inputs on the CPU: cb [B, L/Q, G, Q, Q] fp32,
+    dA_cs [B, H, L/Q, Q] fp32, dt [B, H, L/Q, Q] fp32, x [B, L, H, P] bf16.
+
+    Recipe: x ~ N(0, 1) rounded to bf16; dt = softplus(0.5 N(0, 1) - 3) (about
+    0.05); a per-head decay rate A_h = -exp(U(0, ln 16)); dA = dt A_h and
+    dA_cs its running sum within each chunk; cb ~ N(0, 1).  Drawn in the
+    order x, dt, A, cb."""
+    nch = L // Q
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn((B, L, H, P), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dt = torch.nn.functional.softplus(
+        0.5 * torch.randn((B, H, nch, Q), generator=g, dtype=torch.float32) - 3.0)
+    A = -torch.exp(torch.rand((H,), generator=g, dtype=torch.float32) * math.log(16.0))
+    dA_cs = torch.cumsum(dt * A.view(1, H, 1, 1), dim=-1)
+    cb = torch.randn((B, nch, G, Q, Q), generator=g, dtype=torch.float32)
+    return cb, dA_cs.contiguous(), dt.contiguous(), x
+
+
+def make_chunk_scan_workload(w: ChunkScanWorkload):
+    return make_chunk_scan(w.B, w.L, w.H, w.P, w.G, w.Q, w.seed)

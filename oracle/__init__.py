@@ -17,6 +17,10 @@ through that definition: dQ, dK, dV of L = sum(O * dO), with D_i = dO_i . O_i
 and dS = P (dP - D); it also takes fp64 inputs so finite differences of the
 forward can check it.
 
+The Mamba2 chunk scan (``chunk_scan_oracle.c``, its own library) is the
+intra-chunk sum out[m] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k]
+x[k], written out row by row.
+
 This module only builds the shared libraries and marshals numpy arrays.
 """
 from __future__ import annotations
@@ -32,14 +36,18 @@ _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _BWD_SRC = os.path.join(_HERE, "attn_bwd_oracle.c")
 _BWD_LIB = os.path.join(_HERE, "libbwd_oracle.so")
+_CS_SRC = os.path.join(_HERE, "chunk_scan_oracle.c")
+_CS_LIB = os.path.join(_HERE, "libchunk_scan_oracle.so")
 _default = None
 _bwd_default = None
+_cs_default = None
 
 
 def build(force: bool = False) -> str:
-    """Compile attn_oracle.c into liboracle.so and attn_bwd_oracle.c into
-    libbwd_oracle.so next to them (gcc, -O2, OpenMP); returns the first."""
-    for src, lib in ((_SRC, _LIB), (_BWD_SRC, _BWD_LIB)):
+    """Compile attn_oracle.c, attn_bwd_oracle.c and chunk_scan_oracle.c into
+    liboracle.so, libbwd_oracle.so and libchunk_scan_oracle.so next to them
+    (gcc, -O2, OpenMP); returns the first."""
+    for src, lib in ((_SRC, _LIB), (_BWD_SRC, _BWD_LIB), (_CS_SRC, _CS_LIB)):
         if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
             compile_source(src, lib)
     return _LIB
@@ -311,3 +319,81 @@ def bwd_default() -> BwdOracle:
 
 def attn_bwd(q, k, v, dout, causal: bool, scale: float):
     return bwd_default().attn_bwd(q, k, v, dout, causal, scale)
+
+
+# ---------------------------------------------------------------- chunk scan
+
+
+def _bind_cs(path: str):
+    lib = ctypes.CDLL(path)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    ci = ctypes.c_int
+    dims = [ci] * 6
+    lib.oracle_chunk_scan.argtypes = [f32p, f32p, f32p, u16p, f64p] + dims
+    lib.oracle_chunk_scan.restype = ci
+    lib.oracle_chunk_scan_rows.argtypes = [f32p, f32p, f32p, u16p, i64p, ctypes.c_int64,
+                                           f64p] + dims
+    lib.oracle_chunk_scan_rows.restype = ci
+    return lib
+
+
+def _f32(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+class ChunkScanOracle:
+    """Handle on one compiled copy of the chunk-scan oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.lib = _bind_cs(path)
+
+    @staticmethod
+    def _dims(cb, dA_cs, dt, x):
+        B, L, H, P = x.shape
+        Bc, nch, G, Q, Q2 = cb.shape
+        if Bc != B or Q != Q2 or nch * Q != L or tuple(dA_cs.shape) != (B, H, nch, Q) \
+                or tuple(dt.shape) != (B, H, nch, Q):
+            raise ValueError(f"shape mismatch cb{tuple(cb.shape)} dA_cs{tuple(dA_cs.shape)} "
+                             f"dt{tuple(dt.shape)} x{tuple(x.shape)}")
+        return B, L, H, G, P, Q
+
+    def chunk_scan(self, cb, dA_cs, dt, x):
+        """out [B, L, H, P] float64 for cb, dA_cs, dt (float32) and x (bf16)."""
+        B, L, H, G, P, Q = self._dims(cb, dA_cs, dt, x)
+        c, a, d, xb = _f32(cb), _f32(dA_cs), _f32(dt), _bits(x)
+        out = np.empty((B, L, H, P), np.float64)
+        rc = self.lib.oracle_chunk_scan(_p(c, ctypes.c_float), _p(a, ctypes.c_float),
+                                        _p(d, ctypes.c_float), _p(xb, ctypes.c_uint16),
+                                        _p(out, ctypes.c_double), B, L, H, G, P, Q)
+        if rc != 0:
+            raise ValueError(f"oracle_chunk_scan rejected the arguments (rc={rc})")
+        return out
+
+    def rows(self, cb, dA_cs, dt, x, rows):
+        """Output rows (flat indices into [B, L, H]): [n, P] float64."""
+        B, L, H, G, P, Q = self._dims(cb, dA_cs, dt, x)
+        c, a, d, xb = _f32(cb), _f32(dA_cs), _f32(dt), _bits(x)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        out = np.empty((r.size, P), np.float64)
+        rc = self.lib.oracle_chunk_scan_rows(_p(c, ctypes.c_float), _p(a, ctypes.c_float),
+                                             _p(d, ctypes.c_float), _p(xb, ctypes.c_uint16),
+                                             _p(r, ctypes.c_int64), r.size,
+                                             _p(out, ctypes.c_double), B, L, H, G, P, Q)
+        if rc != 0:
+            raise ValueError(f"oracle_chunk_scan_rows rejected the arguments (rc={rc})")
+        return out
+
+
+def chunk_scan_default() -> ChunkScanOracle:
+    """The chunk-scan oracle built from chunk_scan_oracle.c (compiled on first use)."""
+    global _cs_default
+    if _cs_default is None:
+        build()
+        _cs_default = ChunkScanOracle(_CS_LIB)
+    return _cs_default
