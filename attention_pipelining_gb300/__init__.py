@@ -35,7 +35,8 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
            "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
-           "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes"]
+           "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes",
+           "chunk_scan_fwd"]
 
 
 class AttnError(RuntimeError):
@@ -96,6 +97,8 @@ def _load():
     lib.attn_bwd.restype = ci
     lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.chunk_scan_fwd.argtypes = [vp] * 5 + [ci] * 6 + [vp]
+    lib.chunk_scan_fwd.restype = ci
     _lib = lib
     return lib
 
@@ -260,6 +263,29 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, 
                             B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
                             _stream_handle(stream)), "attn_bwd")
     return dq, dk, dv
+
+
+def chunk_scan(cb, dA_cs, dt, x, out=None, stream=None):
+    """Mamba2 chunk scan (intra-chunk part, include/chunk_scan.h): returns out
+    [B, L, H, P] bf16 for cb [B, L/Q, G, Q, Q], dA_cs and dt [B, H, L/Q, Q]
+    (float32) and x [B, L, H, P] (bf16), all contiguous CUDA tensors."""
+    import torch
+    for name, t, dt_ in (("cb", cb, torch.float32), ("dA_cs", dA_cs, torch.float32),
+                         ("dt", dt, torch.float32), ("x", x, torch.bfloat16)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dt_ \
+                or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA {dt_} tensor")
+    B, L, H, P = x.shape
+    Bc, nch, G, Q, Q2 = cb.shape
+    if Bc != B or Q != Q2 or nch * Q != L or tuple(dA_cs.shape) != (B, H, nch, Q) \
+            or tuple(dt.shape) != (B, H, nch, Q):
+        raise ValueError("shape mismatch between cb, dA_cs, dt and x")
+    if out is None:
+        out = torch.empty_like(x)
+    _check(_load().chunk_scan_fwd(cb.data_ptr(), dA_cs.data_ptr(), dt.data_ptr(), x.data_ptr(),
+                                  out.data_ptr(), B, L, H, G, P, Q, _stream_handle(stream)),
+           "chunk_scan_fwd")
+    return out
 
 
 def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
 
 SOURCES = ["attn_fwd_sm103.cu", "attn_api.cu", "selftest.cu", "attn_combine.cu",
-           "attn_noalloc.cu", "attn_bwd_sm103.cu"]
+           "attn_noalloc.cu", "attn_bwd_sm103.cu", "chunk_scan_sm103.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

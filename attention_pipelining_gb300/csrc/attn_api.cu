@@ -304,9 +304,58 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   return ATTN_OK;
 }
 
+static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const float* dt,
+                                     const void* x, void* out, int B, int L, int H, int G, int P,
+                                     int Q, attn_stream_t stream) {
+  if (!cb || !dA_cs || !dt || !x || !out) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || P <= 0 || Q <= 0) return ATTN_ERR_INVALID_ARG;
+  if (H % G != 0 || L % Q != 0) return ATTN_ERR_INVALID_ARG;
+  if (P != 64 || (Q != 128 && Q != 256)) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * L * H >= (1ll << 31) || (int64_t)B * (L / Q) * H * (Q / 128) >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(cb) || !aligned16(dA_cs) || !aligned16(dt) || !aligned16(x) || !aligned16(out))
+    return ATTN_ERR_MISALIGNED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return ATTN_ERR_CUDA;
+  ChunkScanParams p;
+  std::memset(&p, 0, sizeof(p));
+  // x [B, L, H, P] as a 4-D map {P, H, L, B}: box {64, 1, 64, 1} = 64 rows of
+  // one head, 128 bytes each
+  cuuint64_t dims[4] = {(cuuint64_t)P, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)P * 2, (cuuint64_t)H * P * 2, (cuuint64_t)L * H * P * 2};
+  cuuint32_t box[4] = {64, 1, 64, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (fn(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  p.cb = cb;
+  p.dA_cs = dA_cs;
+  p.dt = dt;
+  p.out = out;
+  p.B = B;
+  p.L = L;
+  p.H = H;
+  p.G = G;
+  p.Q = Q;
+  p.nchunks = L / Q;
+  p.timeout_ns = kDefaultTimeoutNs;
+  if (launch_chunk_scan(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 }  // namespace attnpipe
 
 extern "C" {
+
+attn_status_t chunk_scan_fwd(const float* cb, const float* dA_cs, const float* dt, const void* x,
+                             void* out, int B, int L, int H, int G, int P, int Q,
+                             attn_stream_t stream) {
+  return chunk_scan_impl(cb, dA_cs, dt, x, out, B, L, H, G, P, Q, stream);
+}
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
@@ -393,12 +442,16 @@ attn_status_t attn_device_status(int* status_out, int reset) {
   if (!status_out) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
-  int main_status = 0, selftest_status = 0, bwd_status = 0;
+  int main_status = 0, selftest_status = 0, bwd_status = 0, cs_status = 0;
   if (read_device_status(&main_status, reset != 0) != cudaSuccess ||
       read_selftest_status(&selftest_status, reset != 0) != cudaSuccess ||
-      read_bwd_status(&bwd_status, reset != 0) != cudaSuccess)
+      read_bwd_status(&bwd_status, reset != 0) != cudaSuccess ||
+      read_chunk_scan_status(&cs_status, reset != 0) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  *status_out = main_status != 0 ? main_status : (bwd_status != 0 ? bwd_status : selftest_status);
+  *status_out = main_status != 0 ? main_status
+                : bwd_status != 0 ? bwd_status
+                : cs_status != 0  ? cs_status
+                                  : selftest_status;
   return ATTN_OK;
 }
 

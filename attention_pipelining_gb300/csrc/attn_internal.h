@@ -85,6 +85,24 @@ cudaError_t launch_attn_bwd(const BwdParams& p, int D, const void* o, const void
 // Reads (and optionally clears) the backward kernels' status word.
 cudaError_t read_bwd_status(int* status, bool reset);
 
+// Everything the chunk-scan kernel reads.  x and out are [B, L, H, P] bf16
+// (P = 64), cb [B, L / Q, G, Q, Q] fp32, dA_cs and dt [B, H, L / Q, Q] fp32.
+struct ChunkScanParams {
+  CUtensorMap tm_x;   // x as a 4-D map {P, H, L, B}, box {64, 1, 64, 1}, 128-byte swizzle
+  const float* cb;
+  const float* dA_cs;
+  const float* dt;
+  void* out;
+  int B, L, H, G, Q, nchunks;
+  unsigned long long timeout_ns;
+};
+
+// Queues the chunk-scan kernel on `stream`.
+cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t stream);
+
+// Reads (and optionally clears) the chunk-scan kernel's status word.
+cudaError_t read_chunk_scan_status(int* status, bool reset);
+
 // Events stamped by the trace instantiation, one slot per KV block j.
 enum TraceEvent : int {
   kEvSm0Wake = 0,   // softmax 0: S_0(j) ready (wait returned)

@@ -115,6 +115,17 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
 
 // 3-D tiled load global -> shared, completion counted on `bar` in bytes.
 // `hint` is an L2 cache policy (createpolicy) for the read.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w,
+                                            uint64_t hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w),
+      "l"(hint)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t x, int32_t y, int32_t z, uint64_t hint) {
   asm volatile(

@@ -146,8 +146,9 @@ CHUNK_SCAN_WORKLOADS = {
 CHUNK_SCAN_HEADLINE = "chunkscan_b64_s8192"
 
 
-def make_chunk_scan(B: int, L: int, H: int, P: int, G: int, Q: int, seed: int = 0):
-    """Seeded chunk-scan inputs on the CPU: cb [B, L/Q, G, Q, Q] fp32,
+def make_chunk_scan(B: int, L: int, H: int, P: int, G: int, Q: int, seed: int = 0,
+                    device: str = "cpu"):
+    """Seeded chunk-scan inputs (on `device`): cb [B, L/Q, G, Q, Q] fp32,
     dA_cs [B, H, L/Q, Q] fp32, dt [B, H, L/Q, Q] fp32, x [B, L, H, P] bf16.
 
     Recipe: x ~ N(0, 1) rounded to bf16; dt = softplus(0.5 N(0, 1) - 3) (about
@@ -155,16 +156,16 @@ def make_chunk_scan(B: int, L: int, H: int, P: int, G: int, Q: int, seed: int = 
     dA_cs its running sum within each chunk; cb ~ N(0, 1).  Drawn in the
     order x, dt, A, cb."""
     nch = L // Q
-    g = torch.Generator(device="cpu")
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
-    x = torch.randn((B, L, H, P), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    dt = torch.nn.functional.softplus(
-        0.5 * torch.randn((B, H, nch, Q), generator=g, dtype=torch.float32) - 3.0)
-    A = -torch.exp(torch.rand((H,), generator=g, dtype=torch.float32) * math.log(16.0))
+    kw = dict(generator=g, dtype=torch.float32, device=device)
+    x = torch.randn((B, L, H, P), **kw).to(torch.bfloat16)
+    dt = torch.nn.functional.softplus(0.5 * torch.randn((B, H, nch, Q), **kw) - 3.0)
+    A = -torch.exp(torch.rand((H,), **kw) * math.log(16.0))
     dA_cs = torch.cumsum(dt * A.view(1, H, 1, 1), dim=-1)
-    cb = torch.randn((B, nch, G, Q, Q), generator=g, dtype=torch.float32)
+    cb = torch.randn((B, nch, G, Q, Q), **kw)
     return cb, dA_cs.contiguous(), dt.contiguous(), x
 
 
-def make_chunk_scan_workload(w: ChunkScanWorkload):
-    return make_chunk_scan(w.B, w.L, w.H, w.P, w.G, w.Q, w.seed)
+def make_chunk_scan_workload(w: ChunkScanWorkload, device: str = "cpu"):
+    return make_chunk_scan(w.B, w.L, w.H, w.P, w.G, w.Q, w.seed, device=device)

@@ -602,6 +602,155 @@ def cpu_baseline_bwd(q, k, v, dout, w, target_s: float = 12.0) -> dict:
                       f"visible key range), fp64, {dt:.1f} s"}
 
 
+def run_chunk_scan(args, name):
+    """The Mamba2 chunk scan (chunk_scan_fwd) on one of the chunk-scan
+    workloads: one step = one launch over the whole batch, inputs resident in
+    HBM (drawn on the device with the recipe's distributions)."""
+    import torch
+    import attention_pipelining_gb300 as ap
+    from attention_pipelining_gb300.synthetic import CHUNK_SCAN_WORKLOADS, make_chunk_scan_workload
+
+    w = CHUNK_SCAN_WORKLOADS[name]
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    ap.build()
+    dev = torch.device("cuda", local)
+    cb, dA_cs, dt, x = make_chunk_scan_workload(w, device=f"cuda:{local}")
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ap.chunk_scan(cb, dA_cs, dt, x, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, world)
+    if ap.device_status(reset=True) != 0:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+
+    # end to end: pinned host inputs in, the output back, copies timed
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    dev_in = [cb, dA_cs, dt, x]
+    host_in = [tt.cpu().pin_memory() for tt in dev_in]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    if rank != 0:
+        return
+    hbm_peak = load_hbm_peak()
+    per_launch = t_local / args.steps
+    in_bytes = sum(tt.numel() * tt.element_size() for tt in dev_in)
+    line = {
+        "metric": "Mamba2 chunk scan TFLOP/s (bf16 products, fp32 acc; 2 P per visible key)",
+        "value": world * w.flops * args.steps / t / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "pass": "chunkscan",
+        "config": {
+            "workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P, "G": w.G, "Q": w.Q,
+            "seed": w.seed, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
+                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": w.io_bytes / per_launch / 1e9,
+            "peak": hbm_peak[0],
+            "unit": "GB/s",
+            "frac": w.io_bytes / per_launch / 1e9 / hbm_peak[0],
+            "peak_kind": f"{hbm_peak[1]} HBM copy",
+            "traffic": None,
+            "algorithmic_bytes_per_launch": w.io_bytes,
+            "kernel": "chunk_scan_kernel",
+        },
+        "e2e": {
+            "value": world * w.flops * e2e_steps / t_e2e / 1e12,
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out.numel() * out.element_size(),
+            "steps": e2e_steps,
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_chunk_scan(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_chunk_scan(w, target_s: float = 12.0) -> dict:
+    """The fp64 chunk-scan oracle on a bounded sample: random output rows of
+    one batch item of the workload's shapes (inputs drawn on the CPU with the
+    same recipe), counted at 2 P FLOPs per visible key."""
+    import numpy as np
+    import oracle
+    from attention_pipelining_gb300.synthetic import make_chunk_scan
+    cs = oracle.chunk_scan_default()
+    cb, dA_cs, dt, x = make_chunk_scan(1, w.L, w.H, w.P, w.G, w.Q, w.seed)
+    total = w.L * w.H
+    rng = np.random.default_rng(0)
+    n = 256
+    while True:
+        rows = np.sort(rng.choice(total, size=min(n, total), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        cs.rows(cb, dA_cs, dt, x, rows)
+        dt_s = time.perf_counter() - t0
+        if dt_s >= target_s / 4 or n >= total:
+            break
+        n = min(total, max(n * 2, int(n * target_s / max(dt_s, 1e-3) / 2)))
+    m = (rows // w.H) % w.Q                      # row within its chunk
+    flops = float(2.0 * w.P * (m + 1).sum())
+    return {"value": flops / dt_s / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.default().num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} random output rows of one batch item of {w.name}, fp64, "
+                      f"{dt_s:.1f} s"}
+
+
 def run_trace(args, w):
     """Timeline of the first CTAs from the trace instantiation (not a bench line)."""
     import torch
@@ -636,8 +785,11 @@ def main(argv=None):
     ap_.add_argument("--trace", type=int, default=0,
                      help="print a timeline summary of the first N CTAs instead of a bench line")
     ap_.add_argument("--trace-out", default="", help="also save the raw trace (.npy)")
-    ap_.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
-                     help="bwd: time the backward (attn_bwd) instead of the forward")
+    ap_.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd", "chunkscan"],
+                     help="bwd: time the backward (attn_bwd) instead of the forward; "
+                          "chunkscan: time the Mamba2 chunk scan (see --cs-workload)")
+    ap_.add_argument("--cs-workload", default=None,
+                     help="chunk-scan workload for --pass chunkscan (default: the 64 x 8192 one)")
     args = ap_.parse_args(argv)
     if args.warmup < 3:
         ap_.error("--warmup must be >= 3")
@@ -649,6 +801,12 @@ def main(argv=None):
         run_reference(args, w)
     elif args.which == "bwd":
         run_bwd(args, w)
+    elif args.which == "chunkscan":
+        from attention_pipelining_gb300.synthetic import CHUNK_SCAN_HEADLINE, CHUNK_SCAN_WORKLOADS
+        name = args.cs_workload or CHUNK_SCAN_HEADLINE
+        if name not in CHUNK_SCAN_WORKLOADS:
+            ap_.error(f"--cs-workload must be one of {sorted(CHUNK_SCAN_WORKLOADS)}")
+        run_chunk_scan(args, name)
     else:
         run_ours(args, w)
     world, _, _ = dist_env()

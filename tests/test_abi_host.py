@@ -23,7 +23,7 @@ def _declared_functions():
     for h in os.listdir(os.path.join(ROOT, "include")):
         text = open(os.path.join(ROOT, "include", h)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(attn_[a-z0-9_]+)\s*\(",
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*((?:attn|chunk_scan)_[a-z0-9_]+)\s*\(",
                              text, flags=re.M):
             names.add(m.group(1))
     return sorted(names)
@@ -129,3 +129,21 @@ def test_binding_raises_without_cuda_tensors():
     q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         ap.attn_fwd(q, q, q, False, 0.125)
+
+
+def test_chunk_scan_rejects_bad_arguments_on_host(lib):
+    """chunk_scan_fwd validates before any CUDA call (fake pointers)."""
+    f = lib.chunk_scan_fwd
+    good = dict(B=1, L=256, H=4, G=1, P=64, Q=256)
+
+    def call(cb=A, da=A, dt=A, x=A, out=A, **kw):
+        d = dict(good, **kw)
+        return f(cb, da, dt, x, out, d["B"], d["L"], d["H"], d["G"], d["P"], d["Q"], None)
+
+    assert call(cb=0) == 1                      # null pointer
+    assert call(L=300) == 1                     # L not a multiple of Q
+    assert call(H=3, G=2) == 1                  # H not a multiple of G
+    assert call(B=0) == 1
+    assert call(P=128) == 2                     # head width other than 64
+    assert call(Q=64, L=256) == 2               # chunk other than 128 or 256
+    assert call(x=A + 8) == 3                   # misaligned

@@ -1,0 +1,100 @@
+"""Parity of the CUDA chunk scan (chunk_scan_fwd) against the fp64 oracle.
+
+Tolerance (derived, the pages fix none): each output element is a sum of up
+to Q products whose scaled-cb factor is rounded to bf16 (2^-9 relative) with
+bf16 x, accumulated in fp32, then rounded to bf16 once more; terms of both
+signs partly cancel, so the error is measured against the tensor's scale:
+relative Frobenius error <= 2^-7 and every element within 2^-5 of the
+largest magnitude.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_pipelining_gb300 as ap
+import oracle
+from attention_pipelining_gb300.synthetic import (CHUNK_SCAN_WORKLOADS, make_chunk_scan,
+                                                  make_chunk_scan_workload)
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 2.0 ** -7
+REL_MAX = 2.0 ** -5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ap.build()
+    ap.device_status(reset=True)
+    yield
+
+
+def assert_close(name, got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    err = np.abs(got - ref)
+    fro = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
+    mx = err.max() / max(np.abs(ref).max(), 1e-30)
+    assert fro <= REL_FRO and mx <= REL_MAX, (
+        f"{name}: relative Frobenius error {fro:.3e} (<= {REL_FRO:.3e}), "
+        f"max error / max |ref| {mx:.3e} (<= {REL_MAX:.3e})")
+
+
+def run(cb, dA_cs, dt, x):
+    out = ap.chunk_scan(cb.cuda(), dA_cs.cuda(), dt.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    return out.float().cpu().numpy()
+
+
+SHAPES = [
+    # B, L, H, P, G, Q
+    (1, 256, 4, 64, 1, 256),
+    (2, 512, 4, 64, 2, 256),
+    (1, 384, 3, 64, 1, 128),
+    (2, 256, 6, 64, 3, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_chunk_scan_matches_oracle(shape):
+    B, L, H, P, G, Q = shape
+    cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=31)
+    got = run(cb, dA_cs, dt, x)
+    ref = oracle.chunk_scan_default().chunk_scan(cb, dA_cs, dt, x)
+    assert_close("out", got, ref)
+
+
+def test_chunk_scan_single_key_and_zero_dt():
+    """Closed forms on the GPU: dt = 0 gives 0; x non-zero at one key gives
+    nothing before that key within its chunk and nothing in other chunks."""
+    B, L, H, P, G, Q = 1, 512, 2, 64, 1, 256
+    cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=32)
+    assert not np.any(run(cb, dA_cs, torch.zeros_like(dt), x))
+    x1 = torch.zeros_like(x)
+    k0 = Q + 70
+    x1[0, k0] = x[0, k0]
+    got = run(cb, dA_cs, dt, x1)
+    assert not np.any(got[0, :k0])
+    ref = oracle.chunk_scan_default().chunk_scan(cb, dA_cs, dt, x1)
+    assert_close("single key", got, ref)
+
+
+@pytest.mark.parametrize("name", ["chunkscan_b1_s8192"])
+def test_chunk_scan_workload_sampled_rows(name):
+    w = CHUNK_SCAN_WORKLOADS[name]
+    cb, dA_cs, dt, x = make_chunk_scan_workload(w)
+    got = run(cb, dA_cs, dt, x)
+    rng = np.random.default_rng(33)
+    total = w.B * w.L * w.H
+    rows = np.unique(np.concatenate([[0, total - 1], rng.integers(0, total, 400)]))
+    ref = oracle.chunk_scan_default().rows(cb, dA_cs, dt, x, rows)
+    assert_close("rows", got.reshape(-1, w.P)[rows], ref)
+
+
+def test_chunk_scan_rejects_bad_arguments():
+    cb, dA_cs, dt, x = (t.cuda() for t in make_chunk_scan(1, 256, 2, 64, 1, 256, seed=34))
+    with pytest.raises(ap.AttnError):   # P = 32 is not supported
+        ap.chunk_scan(cb, dA_cs, dt, x[..., :32].contiguous())
+    assert ap.device_status(reset=True) == 0
