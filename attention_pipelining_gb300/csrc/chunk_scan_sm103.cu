@@ -139,24 +139,38 @@ __global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_
     bool ok = cs_warp_wait(vec_full, 0, sAbort, budget);
     const float l2e = 1.4426950408889634f;
     const float da_m = ok ? sDA[m] * l2e : 0.f;
+    // exponent (dA_cs[m] - dA_cs[k]) * log2(e) as da_m - dA_cs[k] * log2(e),
+    // two keys per instruction
+    const uint64_t dam2 = f2_pack(da_m, da_m);
+    const uint64_t nl2e2 = f2_pack(-l2e, -l2e);
     for (int s = 0; s < n_slices && ok; ++s) {
       const int k0 = s * kCsSlice + 32 * w;    // first key of this thread's 32
       const bool diag = (k0 + 31 > m0);        // the slice may hold keys after some row
       uint32_t pk[16];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 cv = ldg_f4(cb_row + k0 + 4 * q);
-        const float cvs[4] = {cv.x, cv.y, cv.z, cv.w};
-        float wv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = k0 + 4 * q + e;
-          float v = cvs[e] * ex2_approx(da_m - sDA[k] * l2e) * sDT[k];
-          if (diag) v = (k <= m) ? v : 0.f;
-          wv[e] = v;
+        const int k = k0 + 4 * q;
+        const float4 cv = ldg_f4(cb_row + k);
+        const float4 da = *reinterpret_cast<const float4*>(sDA + k);
+        const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
+        float e0, e1, e2, e3;
+        f2_unpack(f2_fma(f2_pack(da.x, da.y), nl2e2, dam2), e0, e1);
+        f2_unpack(f2_fma(f2_pack(da.z, da.w), nl2e2, dam2), e2, e3);
+        const uint64_t w01 = f2_mul(f2_mul(f2_pack(ex2_approx(e0), ex2_approx(e1)),
+                                           f2_pack(cv.x, cv.y)), f2_pack(dtv.x, dtv.y));
+        const uint64_t w23 = f2_mul(f2_mul(f2_pack(ex2_approx(e2), ex2_approx(e3)),
+                                           f2_pack(cv.z, cv.w)), f2_pack(dtv.z, dtv.w));
+        float v0, v1, v2, v3;
+        f2_unpack(w01, v0, v1);
+        f2_unpack(w23, v2, v3);
+        if (diag) {  // keys after the row drop out (select: the decay may be inf there)
+          v0 = (k + 0 <= m) ? v0 : 0.f;
+          v1 = (k + 1 <= m) ? v1 : 0.f;
+          v2 = (k + 2 <= m) ? v2 : 0.f;
+          v3 = (k + 3 <= m) ? v3 : 0.f;
         }
-        pk[2 * q] = pack_bf16x2(wv[0], wv[1]);
-        pk[2 * q + 1] = pack_bf16x2(wv[2], wv[3]);
+        pk[2 * q] = pack_bf16x2(v0, v1);
+        pk[2 * q + 1] = pack_bf16x2(v2, v3);
       }
       // row r of slice s: 16-byte chunks 4w .. 4w + 3, 128-byte swizzle
       uint8_t* row_base = sA + s * kCsSliceBytesA + r * 128;
