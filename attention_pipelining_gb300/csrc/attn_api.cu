@@ -311,7 +311,8 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
   if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || P <= 0 || Q <= 0) return ATTN_ERR_INVALID_ARG;
   if (H % G != 0 || L % Q != 0) return ATTN_ERR_INVALID_ARG;
   if (P != 64 || (Q != 128 && Q != 256)) return ATTN_ERR_UNSUPPORTED;
-  if ((int64_t)B * L * H >= (1ll << 31) || (int64_t)B * (L / Q) * H * (Q / 128) >= (1ll << 31))
+  if ((int64_t)B * L * H >= (1ll << 31) || (int64_t)B * (L / Q) * H * (Q / 128) >= (1ll << 31) ||
+      (int64_t)B * (L / Q) * G >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(cb) || !aligned16(dA_cs) || !aligned16(dt) || !aligned16(x) || !aligned16(out))
     return ATTN_ERR_MISALIGNED;
@@ -331,7 +332,19 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  p.cb = cb;
+  // cb [B * nchunks * G, Q, Q] fp32 as a 3-D map: box {32, 128, 1} = 128 rows
+  // of 32 keys (128 bytes each)
+  cuuint64_t cdims[3] = {(cuuint64_t)Q, (cuuint64_t)Q, (cuuint64_t)B * (L / Q) * G};
+  cuuint64_t cstrides[2] = {(cuuint64_t)Q * 4, (cuuint64_t)Q * Q * 4};
+  cuuint32_t cbox[3] = {32, 128, 1};
+  cuuint32_t cestr[3] = {1, 1, 1};
+  if (fn(&p.tm_cb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(cb), cdims, cstrides,
+         cbox, cestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
+  // heads per CTA: the largest of 8, 4, 2, 1 that divides the group size
+  const int group = H / G;
+  p.HB = (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
   p.dA_cs = dA_cs;
   p.dt = dt;
   p.out = out;

@@ -8,18 +8,23 @@
 // consecutive slices overlap.  Per chunk c, head h, row m of the chunk:
 //   out[m, :] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k] x[k, :]
 //
-// One CTA = (batch, chunk, head, 128-row tile of the chunk), 384 threads:
+// One CTA = (batch, chunk, 128-row tile of the chunk, block of HB heads of
+// one group), 384 threads:
 //   warps 0-7  two elementwise warpgroups, thread = row of the tile; for each
-//              64-key slice warpgroup w scales keys 32w .. 32w + 31 of its
-//              row (cb read from global, the decay by exp2) into bf16 and
-//              writes them into the slice's 128-byte-swizzled K-major A tile;
-//   warp 8     tensor-core issuer: per slice, 4 tcgen05.mma (M = 128, N = 64,
-//              K = 16) of A (shared memory) with x (shared memory, MN-major)
-//              into a 128 x 64 fp32 accumulator in tensor memory;
-//   warp 9     TMA producer: the chunk's dA_cs and dt vectors (1-D bulk
-//              copies) and the x slices (4-D tensor map over [B, L, H, P]).
-// Slices of the A tile are handed over one at a time (an mbarrier per
-// slice), so the tensor core works on slice s while slice s + 1 is scaled.
+//              head and each 64-key slice, warpgroup w scales keys
+//              32w .. 32w + 31 of its row of cb (kept in shared memory for
+//              all the CTA's heads) by exp2 of the decay and dt into bf16,
+//              written into a ring of 128-byte-swizzled K-major A slices;
+//              after each head they also store the previous head's output;
+//   warp 8     tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
+//              N = 64, K = 16) of the A slice with the x slice (MN-major)
+//              into one of two 128 x 64 fp32 accumulators in tensor memory
+//              (heads alternate between them);
+//   warp 9     TMA producer: the tile's cb once (3-D map, 32-key boxes), then
+//              per head its dA_cs and dt vectors (1-D bulk copies) and its x
+//              slices (4-D map over [B, L, H, P]) through rings.
+// The rings and the two accumulators let the next head's loads and scaling
+// overlap the current head's products and the previous head's output.
 // Every wait is bounded; a timeout raises a CTA-wide abort flag and the
 // device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
@@ -36,25 +41,33 @@ __device__ int g_cs_status = 0;
 namespace {
 
 constexpr int kCsThreads = 384;
-constexpr int kCsRows = 128;     // rows of a CTA's tile
-constexpr int kCsSlice = 64;     // keys per slice of the reduction axis
-constexpr int kCsP = 64;         // head width
-constexpr int kCsMaxQ = 256;     // longest chunk
-constexpr int kCsMaxSlices = kCsMaxQ / kCsSlice;
+constexpr int kCsRows = 128;       // rows of a CTA's tile
+constexpr int kCsSlice = 64;       // keys per slice of the reduction axis
+constexpr int kCsP = 64;           // head width
+constexpr int kCsMaxQ = 256;       // longest chunk
+constexpr int kCsBox = 32;         // keys per cb box (128 bytes of fp32)
+constexpr int kCsRingA = 3;        // A slices in flight
+constexpr int kCsRingX = 3;        // x slices in flight
+constexpr int kCsRingV = 2;        // heads' vectors in flight
 constexpr uint32_t kCsAll = 0xffffffffu;
 
 // shared memory, offsets from a 1024-byte aligned base
-constexpr int kCsOffA = 0;                                   // [slices][128 x 64] bf16 K-major
-constexpr int kCsSliceBytesA = kCsRows * kCsSlice * 2;        // 16 KB
-constexpr int kCsOffX = kCsOffA + kCsMaxSlices * kCsSliceBytesA;  // [slices][64 x 64] bf16
-constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;           // 8 KB
-constexpr int kCsOffVec = kCsOffX + kCsMaxSlices * kCsSliceBytesX;  // dA_cs [Q], dt [Q] fp32
-constexpr int kCsOffBar = kCsOffVec + 2 * kCsMaxQ * 4;
-// vec_full, x_full[S], a_ready[S], acc_done, drain
-constexpr int kCsNumBars = 3 + 2 * kCsMaxSlices;
+constexpr int kCsBoxBytes = kCsRows * kCsBox * 4;                    // 16 KB
+constexpr int kCsOffCb = 0;                                          // [Q / 32 boxes]
+constexpr int kCsSliceBytesA = kCsRows * kCsSlice * 2;               // 16 KB
+constexpr int kCsOffA = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
+constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;                  // 8 KB
+constexpr int kCsOffX = kCsOffA + kCsRingA * kCsSliceBytesA;         // [ring]
+constexpr int kCsVecBytes = 2 * kCsMaxQ * 4;                         // dA_cs, dt of one head
+constexpr int kCsOffVec = kCsOffX + kCsRingX * kCsSliceBytesX;       // [ring]
+constexpr int kCsOffBar = kCsOffVec + kCsRingV * kCsVecBytes;
+// cb_full, a_full[RA], a_free[RA], x_full[RX], x_free[RX], v_full[RV],
+// v_free[RV], acc_full[2], acc_free[2], drain
+constexpr int kCsNumBars = 1 + 2 * kCsRingA + 2 * kCsRingX + 2 * kCsRingV + 4 + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
-constexpr uint32_t kCsTmemCols = 64;
+constexpr uint32_t kCsTmemCols = 128;                                // two accumulators
+static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ bool cs_warp_wait(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, uint64_t budget) {
@@ -67,53 +80,68 @@ __device__ __forceinline__ void cs_drain_wait(uint64_t* bar, uint32_t parity, ui
   mbar_wait(bar, parity, &never, budget);
 }
 
-__device__ __forceinline__ float4 ldg_f4(const float* p) {
-  return __ldg(reinterpret_cast<const float4*>(p));
-}
-
 }  // namespace
 
-__global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
+__global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
   extern __shared__ uint8_t smem_raw_cs[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_cs) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  uint8_t* sCb = smem + kCsOffCb;
   uint8_t* sA = smem + kCsOffA;
   uint8_t* sX = smem + kCsOffX;
-  float* sDA = reinterpret_cast<float*>(smem + kCsOffVec);
-  float* sDT = sDA + kCsMaxQ;
+  uint8_t* sVec = smem + kCsOffVec;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCsOffBar);
-  uint64_t* vec_full = bars;
-  uint64_t* x_full = bars + 1;
-  uint64_t* a_ready = x_full + kCsMaxSlices;
-  uint64_t* acc_done = a_ready + kCsMaxSlices;
-  uint64_t* drain = acc_done + 1;
+  uint64_t* cb_full = bars;
+  uint64_t* a_full = bars + 1;
+  uint64_t* a_free = a_full + kCsRingA;
+  uint64_t* x_full = a_free + kCsRingA;
+  uint64_t* x_free = x_full + kCsRingX;
+  uint64_t* v_full = x_free + kCsRingX;
+  uint64_t* v_free = v_full + kCsRingV;
+  uint64_t* acc_full = v_free + kCsRingV;   // [2]
+  uint64_t* acc_free = acc_full + 2;        // [2]
+  uint64_t* drain = acc_free + 2;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + kCsOffMisc);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + kCsOffMisc + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t budget = p.timeout_ns;
 
-  // CTA -> (b, c, h, tile): the tiles and heads of one chunk are adjacent, so
-  // the heads of a group read their shared cb from L2
+  // CTA -> (b, c, tile, head block): the head blocks and tiles of one chunk
+  // are adjacent, so the CTAs of a chunk read its cb from L2
   const int tiles = p.Q / kCsRows;
+  const int hblocks = p.H / p.HB;
   int idx = blockIdx.x;
+  const int hb = idx % hblocks;
+  idx /= hblocks;
   const int mt = idx % tiles;
   idx /= tiles;
-  const int h = idx % p.H;
-  idx /= p.H;
   const int c = idx % p.nchunks;
   const int b = idx / p.nchunks;
-  const int g = h / (p.H / p.G);
+  const int h0 = hb * p.HB;                    // first head of the block
+  const int g = h0 / (p.H / p.G);              // the block's group (HB divides H / G)
   const int m0 = mt * kCsRows;                 // first row of the tile within the chunk
   const int n_slices = (m0 + kCsRows) / kCsSlice;  // keys 0 .. m0 + 127 are visible to some row
+  const int n_boxes = 2 * n_slices;
 
   if (threadIdx.x == 0) {
-    mbar_init(vec_full, 1);
-    for (int s = 0; s < kCsMaxSlices; ++s) {
-      mbar_init(&x_full[s], 1);
-      mbar_init(&a_ready[s], 2 * 128);
+    mbar_init(cb_full, 1);
+    for (int i = 0; i < kCsRingA; ++i) {
+      mbar_init(&a_full[i], 2 * 128);
+      mbar_init(&a_free[i], 1);
     }
-    mbar_init(acc_done, 1);
+    for (int i = 0; i < kCsRingX; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_free[i], 1);
+    }
+    for (int i = 0; i < kCsRingV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_free[i], 2 * 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_free[i], 2 * 128);
+    }
     mbar_init(drain, 1);
     *sAbort = 0;
     fence_mbar_init();
@@ -126,7 +154,6 @@ __global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *sTmemBase;
-  const size_t vec_off = (((size_t)b * p.H + h) * p.nchunks + c) * p.Q;
 
   if (warp < 8) {
     // ---------------------------------------------------------- elementwise
@@ -134,65 +161,22 @@ __global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_
     const int r = (warp & 3) * 32 + lane;      // row of the tile
     const int m = m0 + r;                      // row of the chunk
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const float* cb_row =
-        p.cb + ((((size_t)b * p.nchunks + c) * p.G + g) * p.Q + m) * (size_t)p.Q;
-    bool ok = cs_warp_wait(vec_full, 0, sAbort, budget);
     const float l2e = 1.4426950408889634f;
-    const float da_m = ok ? sDA[m] * l2e : 0.f;
-    // exponent (dA_cs[m] - dA_cs[k]) * log2(e) as da_m - dA_cs[k] * log2(e),
-    // two keys per instruction
-    const uint64_t dam2 = f2_pack(da_m, da_m);
     const uint64_t nl2e2 = f2_pack(-l2e, -l2e);
-    for (int s = 0; s < n_slices && ok; ++s) {
-      const int k0 = s * kCsSlice + 32 * w;    // first key of this thread's 32
-      const bool diag = (k0 + 31 > m0);        // the slice may hold keys after some row
-      uint32_t pk[16];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int k = k0 + 4 * q;
-        const float4 cv = ldg_f4(cb_row + k);
-        const float4 da = *reinterpret_cast<const float4*>(sDA + k);
-        const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
-        float e0, e1, e2, e3;
-        f2_unpack(f2_fma(f2_pack(da.x, da.y), nl2e2, dam2), e0, e1);
-        f2_unpack(f2_fma(f2_pack(da.z, da.w), nl2e2, dam2), e2, e3);
-        const uint64_t w01 = f2_mul(f2_mul(f2_pack(ex2_approx(e0), ex2_approx(e1)),
-                                           f2_pack(cv.x, cv.y)), f2_pack(dtv.x, dtv.y));
-        const uint64_t w23 = f2_mul(f2_mul(f2_pack(ex2_approx(e2), ex2_approx(e3)),
-                                           f2_pack(cv.z, cv.w)), f2_pack(dtv.z, dtv.w));
-        float v0, v1, v2, v3;
-        f2_unpack(w01, v0, v1);
-        f2_unpack(w23, v2, v3);
-        if (diag) {  // keys after the row drop out (select: the decay may be inf there)
-          v0 = (k + 0 <= m) ? v0 : 0.f;
-          v1 = (k + 1 <= m) ? v1 : 0.f;
-          v2 = (k + 2 <= m) ? v2 : 0.f;
-          v3 = (k + 3 <= m) ? v3 : 0.f;
-        }
-        pk[2 * q] = pack_bf16x2(v0, v1);
-        pk[2 * q + 1] = pack_bf16x2(v2, v3);
-      }
-      // row r of slice s: 16-byte chunks 4w .. 4w + 3, 128-byte swizzle
-      uint8_t* row_base = sA + s * kCsSliceBytesA + r * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = (4 * w + q) ^ (r & 7);
-        *reinterpret_cast<uint4*>(row_base + chunk * 16) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      }
-      fence_proxy_async_smem();   // generic-proxy writes before the tensor core reads them
-      mbar_arrive(&a_ready[s]);
-    }
-    // ---------------------------------------------------------- epilogue
-    if (ok && cs_warp_wait(acc_done, 0, sAbort, budget)) {
+    bool ok = cs_warp_wait(cb_full, 0, sAbort, budget);
+    // stores the output rows of head j from accumulator j & 1
+    auto epilogue = [&](int j) -> bool {
+      if (!cs_warp_wait(&acc_full[j & 1], (j >> 1) & 1, sAbort, budget)) return false;
       tc_fence_after_sync();
       uint32_t v[32];
-      tmem_ld_x32(tmem + lane_base + 32 * w, v);
+      tmem_ld_x32(tmem + lane_base + (j & 1) * kCsP + 32 * w, v);
       tmem_ld_wait();
       reg_after_wait(v);
+      tc_fence_before_sync();
+      mbar_arrive(&acc_free[j & 1]);           // the accumulator may take head j + 2
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<uint16_t*>(p.out) +
-          ((((size_t)b * p.L + (size_t)c * p.Q + m) * p.H + h) * kCsP) + 32 * w);
+          ((((size_t)b * p.L + (size_t)c * p.Q + m) * p.H + h0 + j) * kCsP) + 32 * w);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 val;
@@ -202,31 +186,105 @@ __global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_
         val.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
         dst[q] = val;
       }
+      return true;
+    };
+    int gs = 0;                                // A slices produced so far
+    for (int j = 0; j < p.HB && ok; ++j) {
+      const int vs = j % kCsRingV;
+      if (!cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget)) { ok = false; break; }
+      const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
+      const float* sDT = sDA + kCsMaxQ;
+      const float da_m = sDA[m] * l2e;
+      const uint64_t dam2 = f2_pack(da_m, da_m);
+      for (int s = 0; s < n_slices; ++s, ++gs) {
+        const int slot = gs % kCsRingA;
+        if (gs >= kCsRingA &&
+            !cs_warp_wait(&a_free[slot], ((gs / kCsRingA) - 1) & 1, sAbort, budget)) {
+          ok = false;
+          break;
+        }
+        const int k0 = s * kCsSlice + 32 * w;  // first key of this thread's 32
+        const bool diag = (k0 + 31 > m0);      // keys after some row of the tile
+        // row r of cb box 2s + w: 16-byte chunks in the 128-byte swizzle
+        const uint8_t* cb_row = sCb + (2 * s + w) * kCsBoxBytes + r * 128;
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int k = k0 + 4 * q;
+          const float4 cv = *reinterpret_cast<const float4*>(cb_row + ((q ^ (r & 7)) << 4));
+          const float4 da = *reinterpret_cast<const float4*>(sDA + k);
+          const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
+          float e0, e1, e2, e3;
+          f2_unpack(f2_fma(f2_pack(da.x, da.y), nl2e2, dam2), e0, e1);
+          f2_unpack(f2_fma(f2_pack(da.z, da.w), nl2e2, dam2), e2, e3);
+          const uint64_t w01 = f2_mul(f2_mul(f2_pack(ex2_approx(e0), ex2_approx(e1)),
+                                             f2_pack(cv.x, cv.y)), f2_pack(dtv.x, dtv.y));
+          const uint64_t w23 = f2_mul(f2_mul(f2_pack(ex2_approx(e2), ex2_approx(e3)),
+                                             f2_pack(cv.z, cv.w)), f2_pack(dtv.z, dtv.w));
+          float v0, v1, v2, v3;
+          f2_unpack(w01, v0, v1);
+          f2_unpack(w23, v2, v3);
+          if (diag) {  // keys after the row drop out (select: the decay may be inf there)
+            v0 = (k + 0 <= m) ? v0 : 0.f;
+            v1 = (k + 1 <= m) ? v1 : 0.f;
+            v2 = (k + 2 <= m) ? v2 : 0.f;
+            v3 = (k + 3 <= m) ? v3 : 0.f;
+          }
+          pk[2 * q] = pack_bf16x2(v0, v1);
+          pk[2 * q + 1] = pack_bf16x2(v2, v3);
+        }
+        uint8_t* row_base = sA + slot * kCsSliceBytesA + r * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = (4 * w + q) ^ (r & 7);
+          *reinterpret_cast<uint4*>(row_base + chunk * 16) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes before the tensor core reads them
+        mbar_arrive(&a_full[slot]);
+      }
+      if (!ok) break;
+      mbar_arrive(&v_free[vs]);                // this head's vectors are no longer read
+      // the previous head's output, while the tensor core works on this one
+      if (j > 0 && !epilogue(j - 1)) { ok = false; break; }
     }
+    if (ok && p.HB > 0) epilogue(p.HB - 1);
   } else if (warp == 8) {
     // ---------------------------------------------------------- tensor-core issuer
     const bool leader = elect_one();
     constexpr uint32_t idesc = make_idesc_bf16_f32(128, kCsP, false, true);
     bool ok = true;
-    for (int s = 0; s < n_slices && ok; ++s) {
-      if (!cs_warp_wait(&a_ready[s], 0, sAbort, budget) ||
-          !cs_warp_wait(&x_full[s], 0, sAbort, budget)) {
+    int gs = 0;                                // slices consumed (A and x rings advance together)
+    for (int j = 0; j < p.HB && ok; ++j) {
+      // accumulator j & 1 must have been read out (head j - 2)
+      if (j >= 2 && !cs_warp_wait(&acc_free[j & 1], ((j >> 1) - 1) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
-      tc_fence_after_sync();
-      if (leader) {
-        const uint64_t a_desc = make_smem_desc_sw128(smem_u32(sA + s * kCsSliceBytesA), 16, 1024);
-        // the x slice is a single 64-wide slab: the leading offset is unused
-        const uint64_t b_desc = make_smem_desc_sw128(smem_u32(sX + s * kCsSliceBytesX), 1024, 1024);
+      for (int s = 0; s < n_slices; ++s, ++gs) {
+        const int sa = gs % kCsRingA, sx = gs % kCsRingX;
+        if (!cs_warp_wait(&a_full[sa], (gs / kCsRingA) & 1, sAbort, budget) ||
+            !cs_warp_wait(&x_full[sx], (gs / kCsRingX) & 1, sAbort, budget)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (leader) {
+          const uint64_t a_desc = make_smem_desc_sw128(smem_u32(sA + sa * kCsSliceBytesA), 16, 1024);
+          // the x slice is a single 64-wide slab: the leading offset is unused
+          const uint64_t b_desc =
+              make_smem_desc_sw128(smem_u32(sX + sx * kCsSliceBytesX), 1024, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kCsSlice / 16; ++kk) {
-          mma_ss(tmem, a_desc + (uint64_t)((kk * 32) >> 4), b_desc + (uint64_t)((kk * 2048) >> 4),
-                 idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kCsSlice / 16; ++kk) {
+            mma_ss(tmem + (j & 1) * kCsP, a_desc + (uint64_t)((kk * 32) >> 4),
+                   b_desc + (uint64_t)((kk * 2048) >> 4), idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&a_free[sa]);
+          tc_commit(&x_free[sx]);
+          if (s + 1 == n_slices) tc_commit(&acc_full[j & 1]);
         }
       }
     }
-    if (ok && leader) tc_commit(acc_done);
     if (leader) {
       tc_commit(drain);
       cs_drain_wait(drain, 0, budget);
@@ -235,19 +293,55 @@ __global__ void __launch_bounds__(kCsThreads, 2) chunk_scan_kernel(const __grid_
   } else if (warp == 9) {
     // ---------------------------------------------------------- TMA producer
     const bool leader = elect_one();
+    const uint64_t pol_x = l2_policy_evict_first();
+    const uint64_t pol_cb = l2_policy_evict_last();
+    bool ok = true;
+    int gs = 0, issued_v = 0;
     if (leader) {
-      mbar_arrive_expect_tx(vec_full, 2 * p.Q * 4);
-      bulk_load(sDA, p.dA_cs + vec_off, p.Q * 4, vec_full);
-      bulk_load(sDT, p.dt + vec_off, p.Q * 4, vec_full);
-      const uint64_t pol = l2_policy_evict_first();
-      for (int s = 0; s < n_slices; ++s) {
-        mbar_arrive_expect_tx(&x_full[s], kCsSliceBytesX);
-        tma_load_4d(sX + s * kCsSliceBytesX, &p.tm_x, &x_full[s], 0, h,
-                    c * p.Q + s * kCsSlice, b, pol);
+      mbar_arrive_expect_tx(cb_full, n_boxes * kCsBoxBytes);
+      const int zc = (b * p.nchunks + c) * p.G + g;
+      for (int i = 0; i < n_boxes; ++i)
+        tma_load_3d(sCb + i * kCsBoxBytes, &p.tm_cb, cb_full, i * kCsBox, m0, zc, pol_cb);
+    }
+    for (int j = 0; j < p.HB && ok; ++j) {
+      const int h = h0 + j;
+      const int vs = j % kCsRingV;
+      if (j >= kCsRingV &&
+          !cs_warp_wait(&v_free[vs], ((j / kCsRingV) - 1) & 1, sAbort, budget)) {
+        ok = false;
+        break;
       }
-      // all copies land before the CTA exits
-      cs_drain_wait(vec_full, 0, budget);
-      for (int s = 0; s < n_slices; ++s) cs_drain_wait(&x_full[s], 0, budget);
+      if (leader) {
+        const size_t vec_off = (((size_t)b * p.H + h) * p.nchunks + c) * p.Q;
+        float* dst = reinterpret_cast<float*>(sVec + vs * kCsVecBytes);
+        mbar_arrive_expect_tx(&v_full[vs], 2 * p.Q * 4);
+        bulk_load(dst, p.dA_cs + vec_off, p.Q * 4, &v_full[vs]);
+        bulk_load(dst + kCsMaxQ, p.dt + vec_off, p.Q * 4, &v_full[vs]);
+      }
+      ++issued_v;
+      for (int s = 0; s < n_slices; ++s, ++gs) {
+        const int sx = gs % kCsRingX;
+        if (gs >= kCsRingX &&
+            !cs_warp_wait(&x_free[sx], ((gs / kCsRingX) - 1) & 1, sAbort, budget)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_arrive_expect_tx(&x_full[sx], kCsSliceBytesX);
+          tma_load_4d(sX + sx * kCsSliceBytesX, &p.tm_x, &x_full[sx], 0, h,
+                      c * p.Q + s * kCsSlice, b, pol_x);
+        }
+      }
+    }
+    // every copy issued lands before the CTA exits
+    if (leader) {
+      cs_drain_wait(cb_full, 0, budget);
+      const int first_v = issued_v > kCsRingV ? issued_v - kCsRingV : 0;
+      for (int j = first_v; j < issued_v; ++j)
+        cs_drain_wait(&v_full[j % kCsRingV], (j / kCsRingV) & 1, budget);
+      const int first_x = gs > kCsRingX ? gs - kCsRingX : 0;
+      for (int t = first_x; t < gs; ++t)
+        cs_drain_wait(&x_full[t % kCsRingX], (t / kCsRingX) & 1, budget);
     }
     __syncwarp();
   }
@@ -278,7 +372,7 @@ cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t stream) {
       g_cs_attr[dev] = true;
     }
   }
-  const long long ctas = (long long)p.B * p.nchunks * p.H * (p.Q / kCsRows);
+  const long long ctas = (long long)p.B * p.nchunks * (p.Q / kCsRows) * (p.H / p.HB);
   if (ctas <= 0 || ctas >= (1ll << 31)) return cudaErrorInvalidValue;
   chunk_scan_kernel<<<(unsigned)ctas, kCsThreads, kCsSmemBytes, stream>>>(p);
   return cudaGetLastError();
