@@ -9,18 +9,18 @@
 //   out[m, :] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k] x[k, :]
 //
 // One CTA = (batch, chunk, 128-row tile of the chunk, block of HB heads of
-// one group), 384 threads:
-//   warps 0-7  two elementwise warpgroups, thread = row of the tile; for each
-//              head and each 64-key slice, warpgroup w scales keys
-//              32w .. 32w + 31 of its row of cb (kept in shared memory for
+// one group), 640 threads:
+//   warps 0-15 four elementwise warpgroups, thread = row of the tile; for
+//              each head and each 64-key slice, warpgroup w scales keys
+//              16w .. 16w + 15 of its row of cb (kept in shared memory for
 //              all the CTA's heads) by exp2 of the decay and dt into bf16,
 //              written into a ring of 128-byte-swizzled K-major A slices;
 //              after each head they also store the previous head's output;
-//   warp 8     tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
+//   warp 16    tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
 //              N = 64, K = 16) of the A slice with the x slice (MN-major)
 //              into one of two 128 x 64 fp32 accumulators in tensor memory
 //              (heads alternate between them);
-//   warp 9     TMA producer: the tile's cb once (3-D map, 32-key boxes), then
+//   warp 17    TMA producer: the tile's cb once (3-D map, 32-key boxes), then
 //              per head its dA_cs and dt vectors (1-D bulk copies) and its x
 //              slices (4-D map over [B, L, H, P]) through rings.
 // The rings and the two accumulators let the next head's loads and scaling
@@ -40,9 +40,11 @@ __device__ int g_cs_status = 0;
 
 namespace {
 
-constexpr int kCsThreads = 384;
+constexpr int kCsThreads = 640;
+constexpr int kCsEwGroups = 4;     // elementwise warpgroups
 constexpr int kCsRows = 128;       // rows of a CTA's tile
 constexpr int kCsSlice = 64;       // keys per slice of the reduction axis
+constexpr int kCsEwKeys = kCsSlice / kCsEwGroups;  // keys of a slice per thread
 constexpr int kCsP = 64;           // head width
 constexpr int kCsMaxQ = 256;       // longest chunk
 constexpr int kCsBox = 32;         // keys per cb box (128 bytes of fp32)
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   if (threadIdx.x == 0) {
     mbar_init(cb_full, 1);
     for (int i = 0; i < kCsRingA; ++i) {
-      mbar_init(&a_full[i], 2 * 128);
+      mbar_init(&a_full[i], kCsEwGroups * 128);
       mbar_init(&a_free[i], 1);
     }
     for (int i = 0; i < kCsRingX; ++i) {
@@ -136,17 +138,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     }
     for (int i = 0; i < kCsRingV; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_free[i], 2 * 128);
+      mbar_init(&v_free[i], kCsEwGroups * 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_free[i], 2 * 128);
+      mbar_init(&acc_free[i], kCsEwGroups * 128);
     }
     mbar_init(drain, 1);
     *sAbort = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 16) {
     tmem_alloc(sTmemBase, kCsTmemCols);
     tmem_relinquish();
   }
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   tc_fence_after_sync();
   const uint32_t tmem = *sTmemBase;
 
-  if (warp < 8) {
+  if (warp < 4 * kCsEwGroups) {
     // ---------------------------------------------------------- elementwise
     const int w = warp >> 2;
     const int r = (warp & 3) * 32 + lane;      // row of the tile
@@ -168,17 +170,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     auto epilogue = [&](int j) -> bool {
       if (!cs_warp_wait(&acc_full[j & 1], (j >> 1) & 1, sAbort, budget)) return false;
       tc_fence_after_sync();
-      uint32_t v[32];
-      tmem_ld_x32(tmem + lane_base + (j & 1) * kCsP + 32 * w, v);
+      uint32_t v[16];
+      tmem_ld_x16(tmem + lane_base + (j & 1) * kCsP + kCsEwKeys * w, v);
       tmem_ld_wait();
       reg_after_wait(v);
       tc_fence_before_sync();
       mbar_arrive(&acc_free[j & 1]);           // the accumulator may take head j + 2
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<uint16_t*>(p.out) +
-          ((((size_t)b * p.L + (size_t)c * p.Q + m) * p.H + h0 + j) * kCsP) + 32 * w);
+          ((((size_t)b * p.L + (size_t)c * p.Q + m) * p.H + h0 + j) * kCsP) + kCsEwKeys * w);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kCsEwKeys / 8; ++q) {
         uint4 val;
         val.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
         val.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
@@ -203,15 +205,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
           ok = false;
           break;
         }
-        const int k0 = s * kCsSlice + 32 * w;  // first key of this thread's 32
-        const bool diag = (k0 + 31 > m0);      // keys after some row of the tile
-        // row r of cb box 2s + w: 16-byte chunks in the 128-byte swizzle
-        const uint8_t* cb_row = sCb + (2 * s + w) * kCsBoxBytes + r * 128;
-        uint32_t pk[16];
+        const int k0 = s * kCsSlice + kCsEwKeys * w;  // first key of this thread's 16
+        const bool diag = (k0 + kCsEwKeys - 1 > m0);   // keys after some row of the tile
+        // row r of the cb box holding these keys: 16-byte chunks in the
+        // 128-byte swizzle, this thread's 4 chunks from (w % 2) * 4
+        const uint8_t* cb_row = sCb + (2 * s + (w >> 1)) * kCsBoxBytes + r * 128;
+        uint32_t pk[kCsEwKeys / 2];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < kCsEwKeys / 4; ++q) {
           const int k = k0 + 4 * q;
-          const float4 cv = *reinterpret_cast<const float4*>(cb_row + ((q ^ (r & 7)) << 4));
+          const int cq = (w & 1) * 4 + q;
+          const float4 cv = *reinterpret_cast<const float4*>(cb_row + ((cq ^ (r & 7)) << 4));
           const float4 da = *reinterpret_cast<const float4*>(sDA + k);
           const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
           float e0, e1, e2, e3;
@@ -235,8 +239,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
         }
         uint8_t* row_base = sA + slot * kCsSliceBytesA + r * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = (4 * w + q) ^ (r & 7);
+        for (int q = 0; q < kCsEwKeys / 8; ++q) {
+          const int chunk = ((kCsEwKeys / 8) * w + q) ^ (r & 7);
           *reinterpret_cast<uint4*>(row_base + chunk * 16) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       if (j > 0 && !epilogue(j - 1)) { ok = false; break; }
     }
     if (ok && p.HB > 0) epilogue(p.HB - 1);
-  } else if (warp == 8) {
+  } else if (warp == 16) {
     // ---------------------------------------------------------- tensor-core issuer
     const bool leader = elect_one();
     constexpr uint32_t idesc = make_idesc_bf16_f32(128, kCsP, false, true);
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       cs_drain_wait(drain, 0, budget);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     // ---------------------------------------------------------- TMA producer
     const bool leader = elect_one();
     const uint64_t pol_x = l2_policy_evict_first();
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 8) tmem_dealloc(tmem, kCsTmemCols);
+  if (warp == 16) tmem_dealloc(tmem, kCsTmemCols);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_cs_status, 0, (int)ATTN_ERR_TIMEOUT);
 }
 
