@@ -189,8 +189,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw_b[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_b) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw_b);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarKV);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
@@ -498,8 +497,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw_b[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_b) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw_b);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBarQ);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;

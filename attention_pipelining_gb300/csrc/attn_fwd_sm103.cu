@@ -190,8 +190,7 @@ template <int D, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sKV = smem + C::kOffKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);

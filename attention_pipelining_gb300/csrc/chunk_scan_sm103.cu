@@ -86,8 +86,7 @@ __device__ __forceinline__ void cs_drain_wait(uint64_t* bar, uint32_t parity, ui
 
 __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_constant__ ChunkScanParams p) {
   extern __shared__ uint8_t smem_raw_cs[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw_cs) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw_cs);
   uint8_t* sCb = smem + kCsOffCb;
   uint8_t* sA = smem + kCsOffA;
   uint8_t* sX = smem + kCsOffX;

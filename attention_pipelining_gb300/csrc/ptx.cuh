@@ -16,6 +16,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned address at or after `p`, a pointer into the
+// CTA's shared memory.  Formed by pointer arithmetic on `p` (not through an
+// integer) so that the compiler still sees a shared-memory address and emits
+// shared loads and stores rather than generic ones.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* p) {
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

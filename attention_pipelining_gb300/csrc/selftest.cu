@@ -25,18 +25,13 @@ struct SelftestSmem {
   int abort_flag;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                    ~static_cast<uintptr_t>(1023));
-}
-
 // 128 threads: thread i owns row i (TMEM lane i).
 template <int D>
 __global__ void __launch_bounds__(128, 1)
     selftest_qk_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        float* s_out) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
+  uint8_t* base = align_smem_1024(smem_raw);
   uint8_t* sQ = base;
   uint8_t* sK = base + TileShape<D>::kBytes;
   SelftestSmem* ctl = reinterpret_cast<SelftestSmem*>(base + 2 * TileShape<D>::kBytes);
@@ -97,7 +92,7 @@ __global__ void __launch_bounds__(128, 1)
     selftest_pv_kernel(const uint16_t* __restrict__ p_in, const __grid_constant__ CUtensorMap tv,
                        float* o_out) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
+  uint8_t* base = align_smem_1024(smem_raw);
   uint8_t* sV = base;
   SelftestSmem* ctl = reinterpret_cast<SelftestSmem*>(base + TileShape<D>::kBytes);
   const int warp = threadIdx.x >> 5;
