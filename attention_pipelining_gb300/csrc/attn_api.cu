@@ -332,6 +332,13 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
+  // out [B, L, H, P] as the same 4-D map with 128 rows per box (one head's
+  // rows of a 128-row tile)
+  cuuint32_t obox[4] = {64, 1, 128, 1};
+  if (fn(&p.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, obox, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ATTN_ERR_CUDA;
   // cb [B * nchunks * G, Q, Q] fp32 as a 3-D map: box {32, 128, 1} = 128 rows
   // of 32 keys (128 bytes each)
   cuuint64_t cdims[3] = {(cuuint64_t)Q, (cuuint64_t)Q, (cuuint64_t)B * (L / Q) * G};
@@ -342,9 +349,7 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
          cbox, cestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ERR_CUDA;
-  // heads per CTA: the largest of 8, 4, 2, 1 that divides the group size
-  const int group = H / G;
-  p.HB = (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
+  p.HB = 0;  // heads per CTA: chosen at launch from the SM count
   p.dA_cs = dA_cs;
   p.dt = dt;
   p.out = out;

@@ -90,11 +90,12 @@ cudaError_t read_bwd_status(int* status, bool reset);
 struct ChunkScanParams {
   CUtensorMap tm_x;   // x as a 4-D map {P, H, L, B}, box {64, 1, 64, 1}, 128-byte swizzle
   CUtensorMap tm_cb;  // cb as a 3-D map {Q, Q, B * nchunks * G}, box {32, 128, 1} fp32, 128-byte swizzle
+  CUtensorMap tm_out; // out as a 4-D map {P, H, L, B}, box {64, 1, 128, 1}, 128-byte swizzle
   const float* dA_cs;
   const float* dt;
   void* out;
   int B, L, H, G, Q, nchunks;
-  int HB;             // heads per CTA (divides H / G)
+  int HB;             // heads per CTA (divides H / G); 0 = chosen at launch
   unsigned long long timeout_ns;
 };
 

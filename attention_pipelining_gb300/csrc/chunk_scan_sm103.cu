@@ -9,22 +9,24 @@
 //   out[m, :] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k] x[k, :]
 //
 // One CTA = (batch, chunk, 128-row tile of the chunk, block of HB heads of
-// one group), 640 threads:
-//   warps 0-15 four elementwise warpgroups, thread = row of the tile; for
-//              each head and each 64-key slice, warpgroup w scales keys
-//              16w .. 16w + 15 of its row of cb (kept in shared memory for
-//              all the CTA's heads) by exp2 of the decay and dt into bf16,
-//              written into a ring of 128-byte-swizzled K-major A slices;
-//              after each head they also store the previous head's output;
-//   warp 16    tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
-//              N = 64, K = 16) of the A slice with the x slice (MN-major)
-//              into one of two 128 x 64 fp32 accumulators in tensor memory
-//              (heads alternate between them);
-//   warp 17    TMA producer: the tile's cb once (3-D map, 32-key boxes), then
-//              per head its dA_cs and dt vectors (1-D bulk copies) and its x
-//              slices (4-D map over [B, L, H, P]) through rings.
-// The rings and the two accumulators let the next head's loads and scaling
-// overlap the current head's products and the previous head's output.
+// one group), 704 threads.  The CTA's slices (64 keys of one head) are
+// numbered gs = 0, 1, ... head by head:
+//   warps 0-15  four scaling warpgroups; warpgroup w takes slices gs = w,
+//               w + 4, ...: thread = row of the tile, it scales its row's 64
+//               keys of cb (kept in shared memory for all the CTA's heads)
+//               by the decay and dt, rounds to bf16 and stores them into a
+//               ring of A slices in tensor memory;
+//   warps 16-19 output warpgroup: per head, reads the accumulator from tensor
+//               memory, rounds to bf16 into a staging tile in shared memory
+//               and writes it with one TMA store;
+//   warp 20     tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
+//               N = 64, K = 16) of the A slice (tensor memory) with the x
+//               slice (shared memory, MN-major) into one of four 128 x 64
+//               fp32 accumulators (heads rotate over them);
+//   warp 21     TMA producer: the tile's cb once (3-D map, 32-key boxes),
+//               then per head its dA_cs and dt vectors (1-D bulk copies) and
+//               its x slices (4-D map over [B, L, H, P]) through rings, with
+//               the head two ahead prefetched into L2.
 // Every wait is bounded; a timeout raises a CTA-wide abort flag and the
 // device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
@@ -40,36 +42,46 @@ __device__ int g_cs_status = 0;
 
 namespace {
 
-constexpr int kCsThreads = 640;
-constexpr int kCsEwGroups = 4;     // elementwise warpgroups
+constexpr int kCsScaleGroups = 4;  // scaling warpgroups
+constexpr int kCsOutWarp0 = 4 * kCsScaleGroups;  // first warp of the output warpgroup
+constexpr int kCsMmaWarp = kCsOutWarp0 + 4;
+constexpr int kCsProdWarp = kCsMmaWarp + 1;
+constexpr int kCsThreads = (kCsProdWarp + 1) * 32;
 constexpr int kCsRows = 128;       // rows of a CTA's tile
 constexpr int kCsSlice = 64;       // keys per slice of the reduction axis
-constexpr int kCsEwKeys = kCsSlice / kCsEwGroups;  // keys of a slice per thread
+constexpr int kCsPortion = 16;     // keys per portion (one decay pivot)
 constexpr int kCsP = 64;           // head width
 constexpr int kCsMaxQ = 256;       // longest chunk
 constexpr int kCsBox = 32;         // keys per cb box (128 bytes of fp32)
-constexpr int kCsRingA = 3;        // A slices in flight
-constexpr int kCsRingX = 3;        // x slices in flight
-constexpr int kCsRingV = 2;        // heads' vectors in flight
+constexpr int kCsRingA = 8;        // A slices in tensor memory
+constexpr int kCsRingX = 6;        // x slices in shared memory
+constexpr int kCsRingV = 6;        // heads' vectors in shared memory
+constexpr int kCsAcc = 4;          // accumulators in tensor memory
 constexpr uint32_t kCsAll = 0xffffffffu;
 
 // shared memory, offsets from a 1024-byte aligned base
 constexpr int kCsBoxBytes = kCsRows * kCsBox * 4;                    // 16 KB
 constexpr int kCsOffCb = 0;                                          // [Q / 32 boxes]
-constexpr int kCsSliceBytesA = kCsRows * kCsSlice * 2;               // 16 KB
-constexpr int kCsOffA = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
 constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;                  // 8 KB
-constexpr int kCsOffX = kCsOffA + kCsRingA * kCsSliceBytesA;         // [ring]
+constexpr int kCsOffX = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
+constexpr int kCsStageBytes = kCsRows * kCsP * 2;                    // 16 KB
+constexpr int kCsOffStage = kCsOffX + kCsRingX * kCsSliceBytesX;     // [2]
 constexpr int kCsVecBytes = 2 * kCsMaxQ * 4;                         // dA_cs, dt of one head
-constexpr int kCsOffVec = kCsOffX + kCsRingX * kCsSliceBytesX;       // [ring]
-constexpr int kCsOffBar = kCsOffVec + kCsRingV * kCsVecBytes;
+constexpr int kCsOffVec = kCsOffStage + 2 * kCsStageBytes;           // [ring]
+constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [A ring][64] key factors
+constexpr int kCsOffBar = kCsOffKf + kCsRingA * kCsSlice * 4;
 // cb_full, a_full[RA], a_free[RA], x_full[RX], x_free[RX], v_full[RV],
-// v_free[RV], acc_full[2], acc_free[2], drain
-constexpr int kCsNumBars = 1 + 2 * kCsRingA + 2 * kCsRingX + 2 * kCsRingV + 4 + 1;
+// v_free[RV], acc_full[ACC], acc_free[ACC], drain
+constexpr int kCsNumBars = 1 + 2 * kCsRingA + 2 * kCsRingX + 2 * kCsRingV + 2 * kCsAcc + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
-constexpr uint32_t kCsTmemCols = 128;                                // two accumulators
 static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
+// tensor memory: accumulators in columns [0, 256), A slices (64 bf16 keys =
+// 32 columns each) in [256, 512)
+constexpr uint32_t kCsTmemCols = 512;
+constexpr uint32_t kCsTmemA = kCsAcc * kCsP;
+static_assert(kCsTmemA + kCsRingA * (kCsSlice / 2) <= kCsTmemCols, "tensor memory budget");
+constexpr uint32_t kCsBarOut = 1 + kCsScaleGroups;  // named barrier of the output warpgroup
 
 __device__ __forceinline__ bool cs_warp_wait(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, uint64_t budget) {
@@ -88,9 +100,10 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   extern __shared__ uint8_t smem_raw_cs[];
   uint8_t* smem = align_smem_1024(smem_raw_cs);
   uint8_t* sCb = smem + kCsOffCb;
-  uint8_t* sA = smem + kCsOffA;
   uint8_t* sX = smem + kCsOffX;
+  uint8_t* sStage = smem + kCsOffStage;
   uint8_t* sVec = smem + kCsOffVec;
+  float* sKfAll = reinterpret_cast<float*>(smem + kCsOffKf);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCsOffBar);
   uint64_t* cb_full = bars;
   uint64_t* a_full = bars + 1;
@@ -99,9 +112,9 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   uint64_t* x_free = x_full + kCsRingX;
   uint64_t* v_full = x_free + kCsRingX;
   uint64_t* v_free = v_full + kCsRingV;
-  uint64_t* acc_full = v_free + kCsRingV;   // [2]
-  uint64_t* acc_free = acc_full + 2;        // [2]
-  uint64_t* drain = acc_free + 2;
+  uint64_t* acc_full = v_free + kCsRingV;
+  uint64_t* acc_free = acc_full + kCsAcc;
+  uint64_t* drain = acc_free + kCsAcc;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + kCsOffMisc);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + kCsOffMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -109,7 +122,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   const uint64_t budget = p.timeout_ns;
 
   // CTA -> (b, c, tile, head block): the head blocks and tiles of one chunk
-  // are adjacent, so the CTAs of a chunk read its cb from L2
+  // are adjacent, so the CTAs of a chunk read its cb and x from L2
   const int tiles = p.Q / kCsRows;
   const int hblocks = p.H / p.HB;
   int idx = blockIdx.x;
@@ -124,11 +137,12 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   const int m0 = mt * kCsRows;                 // first row of the tile within the chunk
   const int n_slices = (m0 + kCsRows) / kCsSlice;  // keys 0 .. m0 + 127 are visible to some row
   const int n_boxes = 2 * n_slices;
+  const int total = p.HB * n_slices;           // slices of the CTA
 
   if (threadIdx.x == 0) {
     mbar_init(cb_full, 1);
     for (int i = 0; i < kCsRingA; ++i) {
-      mbar_init(&a_full[i], kCsEwGroups * 128);
+      mbar_init(&a_full[i], 128);
       mbar_init(&a_free[i], 1);
     }
     for (int i = 0; i < kCsRingX; ++i) {
@@ -137,17 +151,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     }
     for (int i = 0; i < kCsRingV; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_free[i], kCsEwGroups * 128);
+      mbar_init(&v_free[i], 128 * n_slices);  // every slice's warpgroup
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kCsAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_free[i], kCsEwGroups * 128);
+      mbar_init(&acc_free[i], 128);
     }
     mbar_init(drain, 1);
     *sAbort = 0;
     fence_mbar_init();
   }
-  if (warp == 16) {
+  if (warp == kCsMmaWarp) {
     tmem_alloc(sTmemBase, kCsTmemCols);
     tmem_relinquish();
   }
@@ -156,136 +170,203 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   tc_fence_after_sync();
   const uint32_t tmem = *sTmemBase;
 
-  if (warp < 4 * kCsEwGroups) {
-    // ---------------------------------------------------------- elementwise
-    const int w = warp >> 2;
-    const int r = (warp & 3) * 32 + lane;      // row of the tile
+  if (warp < kCsOutWarp0) {
+    // ---------------------------------------------------------- scaling
+    const int w = warp >> 2;                   // warpgroup
+    const int t = threadIdx.x & 127;           // thread of the warpgroup
+    const int r = (warp & 3) * 32 + lane;      // row of the tile = tensor-memory lane
     const int m = m0 + r;                      // row of the chunk
+    const int row0 = m0 + (warp & 3) * 32;     // the warp's first row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float l2e = 1.4426950408889634f;
     const uint64_t nl2e2 = f2_pack(-l2e, -l2e);
     bool ok = cs_warp_wait(cb_full, 0, sAbort, budget);
-    // stores the output rows of head j from accumulator j & 1
-    auto epilogue = [&](int j) -> bool {
-      if (!cs_warp_wait(&acc_full[j & 1], (j >> 1) & 1, sAbort, budget)) return false;
-      tc_fence_after_sync();
-      uint32_t v[16];
-      tmem_ld_x16(tmem + lane_base + (j & 1) * kCsP + kCsEwKeys * w, v);
-      tmem_ld_wait();
-      reg_after_wait(v);
-      tc_fence_before_sync();
-      mbar_arrive(&acc_free[j & 1]);           // the accumulator may take head j + 2
-      uint4* dst = reinterpret_cast<uint4*>(
-          static_cast<uint16_t*>(p.out) +
-          ((((size_t)b * p.L + (size_t)c * p.Q + m) * p.H + h0 + j) * kCsP) + kCsEwKeys * w);
-#pragma unroll
-      for (int q = 0; q < kCsEwKeys / 8; ++q) {
-        uint4 val;
-        val.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-        val.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-        val.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-        val.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-        dst[q] = val;
-      }
-      return true;
-    };
-    int gs = 0;                                // A slices produced so far
-    for (int j = 0; j < p.HB && ok; ++j) {
+    for (int gs = w; gs < total; gs += kCsScaleGroups) {
+      const int j = gs / n_slices;             // head of the block
+      const int s = gs - j * n_slices;         // slice of the head
       const int vs = j % kCsRingV;
-      if (!cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget)) { ok = false; break; }
+      const int slot = gs % kCsRingA;
+      ok = ok && cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget);
+      ok = ok && (gs < kCsRingA ||
+                  cs_warp_wait(&a_free[slot], ((gs / kCsRingA) - 1) & 1, sAbort, budget));
+      tc_fence_after_sync();                   // the slot's last products are done before it is rewritten
       const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
       const float* sDT = sDA + kCsMaxQ;
-      const float da_m = sDA[m] * l2e;
-      const uint64_t dam2 = f2_pack(da_m, da_m);
-      for (int s = 0; s < n_slices; ++s, ++gs) {
-        const int slot = gs % kCsRingA;
-        if (gs >= kCsRingA &&
-            !cs_warp_wait(&a_free[slot], ((gs / kCsRingA) - 1) & 1, sAbort, budget)) {
-          ok = false;
-          break;
-        }
-        const int k0 = s * kCsSlice + kCsEwKeys * w;  // first key of this thread's 16
-        const bool diag = (k0 + kCsEwKeys - 1 > m0);   // keys after some row of the tile
-        // row r of the cb box holding these keys: 16-byte chunks in the
-        // 128-byte swizzle, this thread's 4 chunks from (w % 2) * 4
-        const uint8_t* cb_row = sCb + (2 * s + (w >> 1)) * kCsBoxBytes + r * 128;
-        uint32_t pk[kCsEwKeys / 2];
-#pragma unroll
-        for (int q = 0; q < kCsEwKeys / 4; ++q) {
-          const int k = k0 + 4 * q;
-          const int cq = (w & 1) * 4 + q;
-          const float4 cv = *reinterpret_cast<const float4*>(cb_row + ((cq ^ (r & 7)) << 4));
-          const float4 da = *reinterpret_cast<const float4*>(sDA + k);
-          const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
-          float e0, e1, e2, e3;
-          f2_unpack(f2_fma(f2_pack(da.x, da.y), nl2e2, dam2), e0, e1);
-          f2_unpack(f2_fma(f2_pack(da.z, da.w), nl2e2, dam2), e2, e3);
-          const uint64_t w01 = f2_mul(f2_mul(f2_pack(ex2_approx(e0), ex2_approx(e1)),
-                                             f2_pack(cv.x, cv.y)), f2_pack(dtv.x, dtv.y));
-          const uint64_t w23 = f2_mul(f2_mul(f2_pack(ex2_approx(e2), ex2_approx(e3)),
-                                             f2_pack(cv.z, cv.w)), f2_pack(dtv.z, dtv.w));
-          float v0, v1, v2, v3;
-          f2_unpack(w01, v0, v1);
-          f2_unpack(w23, v2, v3);
-          if (diag) {  // keys after the row drop out (select: the decay may be inf there)
-            v0 = (k + 0 <= m) ? v0 : 0.f;
-            v1 = (k + 1 <= m) ? v1 : 0.f;
-            v2 = (k + 2 <= m) ? v2 : 0.f;
-            v3 = (k + 3 <= m) ? v3 : 0.f;
-          }
-          pk[2 * q] = pack_bf16x2(v0, v1);
-          pk[2 * q + 1] = pack_bf16x2(v2, v3);
-        }
-        uint8_t* row_base = sA + slot * kCsSliceBytesA + r * 128;
-#pragma unroll
-        for (int q = 0; q < kCsEwKeys / 8; ++q) {
-          const int chunk = ((kCsEwKeys / 8) * w + q) ^ (r & 7);
-          *reinterpret_cast<uint4*>(row_base + chunk * 16) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
-        fence_proxy_async_smem();  // generic-proxy writes before the tensor core reads them
-        mbar_arrive(&a_full[slot]);
+      float* sKf = sKfAll + slot * kCsSlice;
+      // Key factors of the slice, kf[k] = exp(dA_cs[k | 15] - dA_cs[k]) dt[k]
+      // (k | 15 is the last key of k's 16-key portion).  For a row m at or
+      // after k | 15,
+      //   exp(dA_cs[m] - dA_cs[k]) = exp(dA_cs[m] - dA_cs[k | 15]) exp(dA_cs[k | 15] - dA_cs[k]),
+      // and where both exponents are <= 0 (dA_cs does not rise, as with
+      // dt > 0 and A < 0) both factors lie in [0, 1]: a portion wholly at or
+      // before a row then costs one exponential per row and one per key
+      // instead of one per (row, key).  `rises` flags a key whose factor
+      // would exceed 1; the slice then keeps one exponential per (row, key).
+      bool rises = false;
+      if (ok && t < kCsSlice) {
+        const int k = s * kCsSlice + t;
+        const float dak = sDA[k];
+        const float dap = sDA[k | (kCsPortion - 1)];
+        sKf[t] = ex2_approx((dap - dak) * l2e) * sDT[k];
+        rises = !(dap <= dak);
       }
-      if (!ok) break;
-      mbar_arrive(&v_free[vs]);                // this head's vectors are no longer read
-      // the previous head's output, while the tensor core works on this one
-      if (j > 0 && !epilogue(j - 1)) { ok = false; break; }
+      // every thread of the warpgroup passes this barrier once per slice,
+      // also after a failed wait, so none is left waiting on it
+      const bool factor = !barrier_or(1 + w, 128, rises || !ok);
+      if (ok) {
+        const float da_raw = sDA[m];
+        const float da_m = da_raw * l2e;
+        const uint64_t dam2 = f2_pack(da_m, da_m);
+        const uint32_t a_col = tmem + lane_base + kCsTmemA + slot * (kCsSlice / 2);
+#pragma unroll 1
+        for (int pi = 0; pi < kCsSlice / kCsPortion; ++pi) {
+          const int k0 = s * kCsSlice + pi * kCsPortion;   // first key of the portion
+          const float* cb_row = reinterpret_cast<const float*>(
+              sCb + (2 * s + (pi >> 1)) * kCsBoxBytes + r * 128);
+          uint32_t pk[kCsPortion / 2];
+          const float dap = sDA[k0 + kCsPortion - 1];
+          if (k0 > row0 + 31) {
+            // every key after every row of the warp
+#pragma unroll
+            for (int q = 0; q < kCsPortion / 2; ++q) pk[q] = 0u;
+          } else if (factor && k0 + kCsPortion - 1 <= row0 && da_raw <= dap) {
+            // every key at or before the row: row factor times key factors
+            const float rowf = ex2_approx((da_raw - dap) * l2e);
+            const uint64_t rf2 = f2_pack(rowf, rowf);
+#pragma unroll
+            for (int q = 0; q < kCsPortion / 4; ++q) {
+              const int cq = (pi & 1) * 4 + q;  // 16-byte chunk of the 128-byte cb row
+              const float4 cv = *reinterpret_cast<const float4*>(
+                  reinterpret_cast<const uint8_t*>(cb_row) + ((cq ^ (r & 7)) << 4));
+              const float4 kv = *reinterpret_cast<const float4*>(sKf + pi * kCsPortion + 4 * q);
+              float v0, v1, v2, v3;
+              f2_unpack(f2_mul(f2_mul(f2_pack(kv.x, kv.y), rf2), f2_pack(cv.x, cv.y)), v0, v1);
+              f2_unpack(f2_mul(f2_mul(f2_pack(kv.z, kv.w), rf2), f2_pack(cv.z, cv.w)), v2, v3);
+              pk[2 * q] = pack_bf16x2(v0, v1);
+              pk[2 * q + 1] = pack_bf16x2(v2, v3);
+            }
+          } else {
+            // the diagonal band, or a decay that rises: one exponential per
+            // (row, key); keys after the row drop out by a select, since the
+            // decay may be inf there
+            const bool diag = (k0 + kCsPortion - 1 > row0);
+#pragma unroll
+            for (int q = 0; q < kCsPortion / 4; ++q) {
+              const int k = k0 + 4 * q;
+              const int cq = (pi & 1) * 4 + q;
+              const float4 cv = *reinterpret_cast<const float4*>(
+                  reinterpret_cast<const uint8_t*>(cb_row) + ((cq ^ (r & 7)) << 4));
+              const float4 da = *reinterpret_cast<const float4*>(sDA + k);
+              const float4 dtv = *reinterpret_cast<const float4*>(sDT + k);
+              float e0, e1, e2, e3;
+              f2_unpack(f2_fma(f2_pack(da.x, da.y), nl2e2, dam2), e0, e1);
+              f2_unpack(f2_fma(f2_pack(da.z, da.w), nl2e2, dam2), e2, e3);
+              const uint64_t w01 = f2_mul(f2_mul(f2_pack(ex2_approx(e0), ex2_approx(e1)),
+                                                 f2_pack(cv.x, cv.y)), f2_pack(dtv.x, dtv.y));
+              const uint64_t w23 = f2_mul(f2_mul(f2_pack(ex2_approx(e2), ex2_approx(e3)),
+                                                 f2_pack(cv.z, cv.w)), f2_pack(dtv.z, dtv.w));
+              float v0, v1, v2, v3;
+              f2_unpack(w01, v0, v1);
+              f2_unpack(w23, v2, v3);
+              if (diag) {
+                v0 = (k + 0 <= m) ? v0 : 0.f;
+                v1 = (k + 1 <= m) ? v1 : 0.f;
+                v2 = (k + 2 <= m) ? v2 : 0.f;
+                v3 = (k + 3 <= m) ? v3 : 0.f;
+              }
+              pk[2 * q] = pack_bf16x2(v0, v1);
+              pk[2 * q + 1] = pack_bf16x2(v2, v3);
+            }
+          }
+          // keys 2i, 2i + 1 of the portion in column i
+          tmem_st_x8(a_col + pi * (kCsPortion / 2), pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&a_full[slot]);
+        mbar_arrive(&v_free[vs]);              // this slice no longer reads the head's vectors
+      }
     }
-    if (ok && p.HB > 0) epilogue(p.HB - 1);
-  } else if (warp == 16) {
+  } else if (warp < kCsMmaWarp) {
+    // ---------------------------------------------------------- output
+    const int r = (warp & 3) * 32 + lane;      // row of the tile = tensor-memory lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool issuer = (warp == kCsOutWarp0) && elect_one();
+    bool ok = true;
+    for (int j = 0; j < p.HB; ++j) {
+      const int a = j % kCsAcc;
+      ok = ok && cs_warp_wait(&acc_full[a], (j / kCsAcc) & 1, sAbort, budget);
+      uint8_t* stage = sStage + (j & 1) * kCsStageBytes;
+      // the store that last read this staging tile (head j - 2) is done reading
+      if (issuer) tma_store_wait_read<1>();
+      __syncwarp();
+      named_barrier_sync(kCsBarOut, 128);
+      if (ok) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_base + a * kCsP + half * 32, v);
+          tmem_ld_wait();
+          reg_after_wait(v);
+          if (half == 1) {
+            tc_fence_before_sync();
+            mbar_arrive(&acc_free[a]);         // the accumulator may take head j + 4
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {        // 16-byte chunks 4 * half + q of the row
+            const int chunk = (4 * half + q) ^ (r & 7);
+            *reinterpret_cast<uint4*>(stage + r * 128 + chunk * 16) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+          }
+        }
+        fence_proxy_async_smem();              // the staging writes before the TMA store reads them
+      }
+      named_barrier_sync(kCsBarOut, 128);
+      if (issuer && ok) {
+        tma_store_4d(&p.tm_out, stage, 0, h0 + j, c * p.Q + m0, b);
+        tma_store_commit();
+      }
+    }
+    if (issuer) tma_store_wait_all();
+  } else if (warp == kCsMmaWarp) {
     // ---------------------------------------------------------- tensor-core issuer
     const bool leader = elect_one();
     constexpr uint32_t idesc = make_idesc_bf16_f32(128, kCsP, false, true);
     bool ok = true;
-    int gs = 0;                                // slices consumed (A and x rings advance together)
-    for (int j = 0; j < p.HB && ok; ++j) {
-      // accumulator j & 1 must have been read out (head j - 2)
-      if (j >= 2 && !cs_warp_wait(&acc_free[j & 1], ((j >> 1) - 1) & 1, sAbort, budget)) {
+    for (int gs = 0; gs < total && ok; ++gs) {
+      const int j = gs / n_slices;
+      const int s = gs - j * n_slices;
+      const int a = j % kCsAcc;
+      const int sa = gs % kCsRingA, sx = gs % kCsRingX;
+      // accumulator a must have been read out (head j - 4)
+      if (s == 0 && j >= kCsAcc &&
+          !cs_warp_wait(&acc_free[a], ((j / kCsAcc) - 1) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
-      for (int s = 0; s < n_slices; ++s, ++gs) {
-        const int sa = gs % kCsRingA, sx = gs % kCsRingX;
-        if (!cs_warp_wait(&a_full[sa], (gs / kCsRingA) & 1, sAbort, budget) ||
-            !cs_warp_wait(&x_full[sx], (gs / kCsRingX) & 1, sAbort, budget)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (leader) {
-          const uint64_t a_desc = make_smem_desc_sw128(smem_u32(sA + sa * kCsSliceBytesA), 16, 1024);
-          // the x slice is a single 64-wide slab: the leading offset is unused
-          const uint64_t b_desc =
-              make_smem_desc_sw128(smem_u32(sX + sx * kCsSliceBytesX), 1024, 1024);
+      if (!cs_warp_wait(&a_full[sa], (gs / kCsRingA) & 1, sAbort, budget) ||
+          !cs_warp_wait(&x_full[sx], (gs / kCsRingX) & 1, sAbort, budget)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (leader) {
+        const uint32_t a_tmem = tmem + kCsTmemA + sa * (kCsSlice / 2);
+        // the x slice is a single 64-wide slab: the leading offset is unused
+        const uint64_t b_desc =
+            make_smem_desc_sw128(smem_u32(sX + sx * kCsSliceBytesX), 1024, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kCsSlice / 16; ++kk) {
-            mma_ss(tmem + (j & 1) * kCsP, a_desc + (uint64_t)((kk * 32) >> 4),
-                   b_desc + (uint64_t)((kk * 2048) >> 4), idesc, (s > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&a_free[sa]);
-          tc_commit(&x_free[sx]);
-          if (s + 1 == n_slices) tc_commit(&acc_full[j & 1]);
+        for (int kk = 0; kk < kCsSlice / 16; ++kk) {
+          mma_ts(tmem + a * kCsP, a_tmem + kk * 8, b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
+                 (s > 0 || kk > 0) ? 1u : 0u);
         }
+        tc_commit(&a_free[sa]);
+        tc_commit(&x_free[sx]);
+        if (s + 1 == n_slices) tc_commit(&acc_full[a]);
       }
     }
     if (leader) {
@@ -293,7 +374,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       cs_drain_wait(drain, 0, budget);
     }
     __syncwarp();
-  } else if (warp == 17) {
+  } else {
     // ---------------------------------------------------------- TMA producer
     const bool leader = elect_one();
     const uint64_t pol_x = l2_policy_evict_first();
@@ -309,6 +390,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     for (int j = 0; j < p.HB && ok; ++j) {
       const int h = h0 + j;
       const int vs = j % kCsRingV;
+      if (leader) {
+        // the x slices and vectors of the head two ahead into L2, so that
+        // their loads into the rings wait on L2 rather than on DRAM
+        for (int jj = (j == 0 ? 1 : j + 2); jj <= j + 2 && jj < p.HB; ++jj) {
+          for (int s = 0; s < n_slices; ++s)
+            tma_prefetch_4d(&p.tm_x, 0, h0 + jj, c * p.Q + s * kCsSlice, b);
+          const size_t off = (((size_t)b * p.H + h0 + jj) * p.nchunks + c) * p.Q;
+          bulk_prefetch_l2(p.dA_cs + off, p.Q * 4);
+          bulk_prefetch_l2(p.dt + off, p.Q * 4);
+        }
+      }
       if (j >= kCsRingV &&
           !cs_warp_wait(&v_free[vs], ((j / kCsRingV) - 1) & 1, sAbort, budget)) {
         ok = false;
@@ -352,29 +444,49 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 16) tmem_dealloc(tmem, kCsTmemCols);
+  if (warp == kCsMmaWarp) tmem_dealloc(tmem, kCsTmemCols);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_cs_status, 0, (int)ATTN_ERR_TIMEOUT);
 }
 
 namespace {
 std::mutex g_cs_mu;
 bool g_cs_attr[64] = {};
+int g_cs_sms[64] = {};
+
+// Heads per CTA: the largest of 32, 16, 8, 4, 2, 1 that divides the group
+// size and still gives every SM at least three CTAs.  A CTA loads its tile's
+// cb once for all its heads, so larger blocks load it less often; too few
+// CTAs leave SMs idle.
+int choose_head_block(const ChunkScanParams& p, int sms) {
+  const int group = p.H / p.G;
+  const long long tiles = (long long)p.B * p.nchunks * (p.Q / kCsRows) * p.G;
+  int hb = 32;
+  while (hb > 1 && (group % hb != 0 || tiles * (group / hb) < 3ll * sms)) hb >>= 1;
+  return hb;
+}
 }  // namespace
 
-cudaError_t launch_chunk_scan(const ChunkScanParams& p, cudaStream_t stream) {
+cudaError_t launch_chunk_scan(const ChunkScanParams& params, cudaStream_t stream) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int sms = 0;
   {
     std::lock_guard<std::mutex> lk(g_cs_mu);
     if (!g_cs_attr[dev]) {
       err = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kCsSmemBytes);
       if (err != cudaSuccess) return err;
+      err = cudaDeviceGetAttribute(&g_cs_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (err != cudaSuccess) return err;
       g_cs_attr[dev] = true;
     }
+    sms = g_cs_sms[dev];
   }
+  ChunkScanParams p = params;
+  if (p.HB <= 0) p.HB = choose_head_block(p, sms);
+  if ((p.H / p.G) % p.HB != 0) return cudaErrorInvalidValue;
   const long long ctas = (long long)p.B * p.nchunks * (p.Q / kCsRows) * (p.H / p.HB);
   if (ctas <= 0 || ctas >= (1ll << 31)) return cudaErrorInvalidValue;
   chunk_scan_kernel<<<(unsigned)ctas, kCsThreads, kCsSmemBytes, stream>>>(p);

@@ -98,3 +98,51 @@ def test_chunk_scan_rejects_bad_arguments():
     with pytest.raises(ap.AttnError):   # P = 32 is not supported
         ap.chunk_scan(cb, dA_cs, dt, x[..., :32].contiguous())
     assert ap.device_status(reset=True) == 0
+
+
+def test_chunk_scan_rising_decay():
+    """dA_cs that rises somewhere in a chunk (not Mamba2's case, where dt > 0
+    and A < 0 make it fall) next to heads where it falls, in one launch:
+    where it rises the kernel keeps one exponential per (row, key), where it
+    falls it splits the decay into a row and a key factor."""
+    B, L, H, P, G, Q = 2, 512, 8, 64, 2, 256
+    cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=35)
+    g = torch.Generator().manual_seed(36)
+    walk = torch.cumsum(0.05 * torch.randn(B, H, L // Q, Q, generator=g), dim=-1)
+    dA_cs[:, 1] = walk[:, 1]                     # a random walk: rises and falls
+    dA_cs[0, 2, 1, 100:] += 0.3                  # one step up at key 100 of one chunk
+    dA_cs[1, 6, 0, 255] += 1e-3                  # a rise at the chunk's last key only
+    got = run(cb, dA_cs, dt, x)
+    ref = oracle.chunk_scan_default().chunk_scan(cb, dA_cs, dt, x)
+    assert_close("out", got, ref)
+
+
+@pytest.mark.parametrize("shape", [(4, 8192, 64, 64, 1, 256)], ids=["b4_s8192"])
+def test_chunk_scan_large_head_blocks_sampled_rows(shape):
+    """Enough row tiles that a CTA takes 32 heads; sampled rows."""
+    B, L, H, P, G, Q = shape
+    cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=37)
+    got = run(cb, dA_cs, dt, x)
+    rng = np.random.default_rng(38)
+    total = B * L * H
+    rows = np.unique(np.concatenate([[0, total - 1], rng.integers(0, total, 400)]))
+    ref = oracle.chunk_scan_default().rows(cb, dA_cs, dt, x, rows)
+    assert_close("rows", got.reshape(-1, P)[rows], ref)
+
+
+def test_chunk_scan_headline_workload_sampled_rows():
+    """The 64 x 8192 workload as the benchmark times it (inputs drawn on the
+    device): sampled rows against the oracle."""
+    w = CHUNK_SCAN_WORKLOADS["chunkscan_b64_s8192"]
+    cb, dA_cs, dt, x = make_chunk_scan_workload(w, device="cuda")
+    out = ap.chunk_scan(cb, dA_cs, dt, x)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    rng = np.random.default_rng(39)
+    total = w.B * w.L * w.H
+    rows = np.unique(np.concatenate([[0, total - 1], rng.integers(0, total, 300)]))
+    got = out.reshape(-1, w.P)[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    cpu = [t.cpu() for t in (cb, dA_cs, dt, x)]
+    del cb, dA_cs, dt, x, out
+    ref = oracle.chunk_scan_default().rows(*cpu, rows)
+    assert_close("rows", got, ref)
