@@ -14,8 +14,10 @@
 //   warps 0-15  four scaling warpgroups; warpgroup w takes slices gs = w,
 //               w + 4, ...: thread = row of the tile, it scales its row's 64
 //               keys of cb (kept in shared memory for all the CTA's heads)
-//               by the decay and dt, rounds to bf16 and stores them into a
-//               ring of A slices in tensor memory;
+//               by the decay and dt, rounds to bf16 and stores them into the
+//               slice's A slot in tensor memory (a ring of six slots, each
+//               paired with an x slot in shared memory and one full/free
+//               barrier pair);
 //   warps 16-19 output warpgroup: per head, reads the accumulator from tensor
 //               memory, rounds to bf16 into a staging tile in shared memory
 //               and writes it with one TMA store;
@@ -53,8 +55,7 @@ constexpr int kCsPortion = 16;     // keys per portion (one decay pivot)
 constexpr int kCsP = 64;           // head width
 constexpr int kCsMaxQ = 256;       // longest chunk
 constexpr int kCsBox = 32;         // keys per cb box (128 bytes of fp32)
-constexpr int kCsRingA = 8;        // A slices in tensor memory
-constexpr int kCsRingX = 6;        // x slices in shared memory
+constexpr int kCsRing = 6;         // slices in flight: A in tensor memory, x in shared memory
 constexpr int kCsRingV = 6;        // heads' vectors in shared memory
 constexpr int kCsAcc = 4;          // accumulators in tensor memory
 constexpr uint32_t kCsAll = 0xffffffffu;
@@ -65,14 +66,14 @@ constexpr int kCsOffCb = 0;                                          // [Q / 32 
 constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;                  // 8 KB
 constexpr int kCsOffX = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
 constexpr int kCsStageBytes = kCsRows * kCsP * 2;                    // 16 KB
-constexpr int kCsOffStage = kCsOffX + kCsRingX * kCsSliceBytesX;     // [2]
+constexpr int kCsOffStage = kCsOffX + kCsRing * kCsSliceBytesX;      // [2]
 constexpr int kCsVecBytes = 2 * kCsMaxQ * 4;                         // dA_cs, dt of one head
 constexpr int kCsOffVec = kCsOffStage + 2 * kCsStageBytes;           // [ring]
-constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [A ring][64] key factors
-constexpr int kCsOffBar = kCsOffKf + kCsRingA * kCsSlice * 4;
-// cb_full, a_full[RA], a_free[RA], x_full[RX], x_free[RX], v_full[RV],
-// v_free[RV], acc_full[ACC], acc_free[ACC], drain
-constexpr int kCsNumBars = 1 + 2 * kCsRingA + 2 * kCsRingX + 2 * kCsRingV + 2 * kCsAcc + 1;
+constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [ring][64] key factors
+constexpr int kCsOffBar = kCsOffKf + kCsRing * kCsSlice * 4;
+// cb_full, slot_full[R], slot_free[R], v_full[RV], v_free[RV],
+// acc_full[ACC], acc_free[ACC], drain
+constexpr int kCsNumBars = 1 + 2 * kCsRing + 2 * kCsRingV + 2 * kCsAcc + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
 static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
@@ -80,7 +81,7 @@ static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
 // 32 columns each) in [256, 512)
 constexpr uint32_t kCsTmemCols = 512;
 constexpr uint32_t kCsTmemA = kCsAcc * kCsP;
-static_assert(kCsTmemA + kCsRingA * (kCsSlice / 2) <= kCsTmemCols, "tensor memory budget");
+static_assert(kCsTmemA + kCsRing * (kCsSlice / 2) <= kCsTmemCols, "tensor memory budget");
 constexpr uint32_t kCsBarOut = 1 + kCsScaleGroups;  // named barrier of the output warpgroup
 
 __device__ __forceinline__ bool cs_warp_wait(uint64_t* bar, uint32_t parity,
@@ -106,11 +107,12 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   float* sKfAll = reinterpret_cast<float*>(smem + kCsOffKf);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCsOffBar);
   uint64_t* cb_full = bars;
-  uint64_t* a_full = bars + 1;
-  uint64_t* a_free = a_full + kCsRingA;
-  uint64_t* x_full = a_free + kCsRingA;
-  uint64_t* x_free = x_full + kCsRingX;
-  uint64_t* v_full = x_free + kCsRingX;
+  // slot_full[i]: the A slice written (128 arrivals of its warpgroup) and
+  // the x slice landed (one arrival with its bytes); slot_free[i]: the
+  // products that read both are done
+  uint64_t* slot_full = bars + 1;
+  uint64_t* slot_free = slot_full + kCsRing;
+  uint64_t* v_full = slot_free + kCsRing;
   uint64_t* v_free = v_full + kCsRingV;
   uint64_t* acc_full = v_free + kCsRingV;
   uint64_t* acc_free = acc_full + kCsAcc;
@@ -141,13 +143,9 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     mbar_init(cb_full, 1);
-    for (int i = 0; i < kCsRingA; ++i) {
-      mbar_init(&a_full[i], 128);
-      mbar_init(&a_free[i], 1);
-    }
-    for (int i = 0; i < kCsRingX; ++i) {
-      mbar_init(&x_full[i], 1);
-      mbar_init(&x_free[i], 1);
+    for (int i = 0; i < kCsRing; ++i) {
+      mbar_init(&slot_full[i], 128 + 1);
+      mbar_init(&slot_free[i], 1);
     }
     for (int i = 0; i < kCsRingV; ++i) {
       mbar_init(&v_full[i], 1);
@@ -185,10 +183,10 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       const int j = gs / n_slices;             // head of the block
       const int s = gs - j * n_slices;         // slice of the head
       const int vs = j % kCsRingV;
-      const int slot = gs % kCsRingA;
+      const int slot = gs % kCsRing;
       ok = ok && cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget);
-      ok = ok && (gs < kCsRingA ||
-                  cs_warp_wait(&a_free[slot], ((gs / kCsRingA) - 1) & 1, sAbort, budget));
+      ok = ok && (gs < kCsRing ||
+                  cs_warp_wait(&slot_free[slot], ((gs / kCsRing) - 1) & 1, sAbort, budget));
       tc_fence_after_sync();                   // the slot's last products are done before it is rewritten
       const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
       const float* sDT = sDA + kCsMaxQ;
@@ -283,7 +281,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&a_full[slot]);
+        mbar_arrive(&slot_full[slot]);
         mbar_arrive(&v_free[vs]);              // this slice no longer reads the head's vectors
       }
     }
@@ -341,31 +339,29 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       const int j = gs / n_slices;
       const int s = gs - j * n_slices;
       const int a = j % kCsAcc;
-      const int sa = gs % kCsRingA, sx = gs % kCsRingX;
+      const int slot = gs % kCsRing;
       // accumulator a must have been read out (head j - 4)
       if (s == 0 && j >= kCsAcc &&
           !cs_warp_wait(&acc_free[a], ((j / kCsAcc) - 1) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
-      if (!cs_warp_wait(&a_full[sa], (gs / kCsRingA) & 1, sAbort, budget) ||
-          !cs_warp_wait(&x_full[sx], (gs / kCsRingX) & 1, sAbort, budget)) {
+      if (!cs_warp_wait(&slot_full[slot], (gs / kCsRing) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       if (leader) {
-        const uint32_t a_tmem = tmem + kCsTmemA + sa * (kCsSlice / 2);
+        const uint32_t a_tmem = tmem + kCsTmemA + slot * (kCsSlice / 2);
         // the x slice is a single 64-wide slab: the leading offset is unused
         const uint64_t b_desc =
-            make_smem_desc_sw128(smem_u32(sX + sx * kCsSliceBytesX), 1024, 1024);
+            make_smem_desc_sw128(smem_u32(sX + slot * kCsSliceBytesX), 1024, 1024);
 #pragma unroll
         for (int kk = 0; kk < kCsSlice / 16; ++kk) {
           mma_ts(tmem + a * kCsP, a_tmem + kk * 8, b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
                  (s > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&a_free[sa]);
-        tc_commit(&x_free[sx]);
+        tc_commit(&slot_free[slot]);
         if (s + 1 == n_slices) tc_commit(&acc_full[a]);
       }
     }
@@ -415,28 +411,32 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       }
       ++issued_v;
       for (int s = 0; s < n_slices; ++s, ++gs) {
-        const int sx = gs % kCsRingX;
-        if (gs >= kCsRingX &&
-            !cs_warp_wait(&x_free[sx], ((gs / kCsRingX) - 1) & 1, sAbort, budget)) {
+        const int slot = gs % kCsRing;
+        if (gs >= kCsRing &&
+            !cs_warp_wait(&slot_free[slot], ((gs / kCsRing) - 1) & 1, sAbort, budget)) {
           ok = false;
           break;
         }
         if (leader) {
-          mbar_arrive_expect_tx(&x_full[sx], kCsSliceBytesX);
-          tma_load_4d(sX + sx * kCsSliceBytesX, &p.tm_x, &x_full[sx], 0, h,
+          mbar_arrive_expect_tx(&slot_full[slot], kCsSliceBytesX);
+          tma_load_4d(sX + slot * kCsSliceBytesX, &p.tm_x, &slot_full[slot], 0, h,
                       c * p.Q + s * kCsSlice, b, pol_x);
         }
       }
     }
-    // every copy issued lands before the CTA exits
+    // every copy issued lands before the CTA exits.  An x slice's phase
+    // also needs its warpgroup's arrivals: after an abort those may never
+    // come, so the wait for them is cut short (the copies themselves land
+    // within microseconds)
     if (leader) {
       cs_drain_wait(cb_full, 0, budget);
       const int first_v = issued_v > kCsRingV ? issued_v - kCsRingV : 0;
       for (int j = first_v; j < issued_v; ++j)
         cs_drain_wait(&v_full[j % kCsRingV], (j / kCsRingV) & 1, budget);
-      const int first_x = gs > kCsRingX ? gs - kCsRingX : 0;
+      const uint64_t x_budget = *sAbort ? (budget < 1000000ull ? budget : 1000000ull) : budget;
+      const int first_x = gs > kCsRing ? gs - kCsRing : 0;
       for (int t = first_x; t < gs; ++t)
-        cs_drain_wait(&x_full[t % kCsRingX], (t / kCsRingX) & 1, budget);
+        cs_drain_wait(&slot_full[t % kCsRing], (t / kCsRing) & 1, x_budget);
     }
     __syncwarp();
   }
