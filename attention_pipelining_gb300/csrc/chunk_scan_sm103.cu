@@ -9,26 +9,29 @@
 //   out[m, :] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k] x[k, :]
 //
 // One CTA = (batch, chunk, 128-row tile of the chunk, block of HB heads of
-// one group), 704 threads.  The CTA's slices (64 keys of one head) are
+// one group), 736 threads.  The CTA's slices (64 keys of one head) are
 // numbered gs = 0, 1, ... head by head:
 //   warps 0-15  four scaling warpgroups; warpgroup w takes slices gs = w,
 //               w + 4, ...: thread = row of the tile, it scales its row's 64
 //               keys of cb (kept in shared memory for all the CTA's heads)
 //               by the decay and dt, rounds to bf16 and stores them into the
-//               slice's A slot in tensor memory (a ring of six slots, each
-//               paired with an x slot in shared memory and one full/free
-//               barrier pair);
+//               slice's A slot in tensor memory (a ring of six slots; two
+//               consecutive slices share one full/free barrier pair);
 //   warps 16-19 output warpgroup: per head, reads the accumulator from tensor
 //               memory, rounds to bf16 into a staging tile in shared memory
 //               and writes it with one TMA store;
-//   warp 20     tensor-core issuer: per slice, 4 tcgen05.mma (M = 128,
-//               N = 64, K = 16) of the A slice (tensor memory) with the x
-//               slice (shared memory, MN-major) into one of four 128 x 64
+//   warp 20     tensor-core issuer: per pair of slices, 8 tcgen05.mma (M = 128,
+//               N = 64, K = 16) of the A slices (tensor memory) with the x
+//               slices (shared memory, MN-major) into one of four 128 x 64
 //               fp32 accumulators (heads rotate over them);
+//   warp 22     vectors and key factors: per head, loads dA_cs and dt (1-D
+//               bulk copies, ahead as far as its ring allows) and computes the per-key
+//               factors of the decay and the mask of portions where dA_cs
+//               rises (see below);
 //   warp 21     TMA producer: the tile's cb once (3-D map, 32-key boxes),
-//               then per head its dA_cs and dt vectors (1-D bulk copies) and
-//               its x slices (4-D map over [B, L, H, P]) through rings, with
-//               the head two ahead prefetched into L2.
+//               then per head its x slices (4-D map over [B, L, H, P])
+//               through a ring of eight slots (two slices per full/free
+//               barrier pair), with the head two ahead prefetched into L2.
 // Every wait is bounded; a timeout raises a CTA-wide abort flag and the
 // device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
@@ -48,15 +51,19 @@ constexpr int kCsScaleGroups = 4;  // scaling warpgroups
 constexpr int kCsOutWarp0 = 4 * kCsScaleGroups;  // first warp of the output warpgroup
 constexpr int kCsMmaWarp = kCsOutWarp0 + 4;
 constexpr int kCsProdWarp = kCsMmaWarp + 1;
-constexpr int kCsThreads = (kCsProdWarp + 1) * 32;
+constexpr int kCsVecWarp = kCsProdWarp + 1;
+constexpr int kCsThreads = (kCsVecWarp + 1) * 32;
 constexpr int kCsRows = 128;       // rows of a CTA's tile
 constexpr int kCsSlice = 64;       // keys per slice of the reduction axis
 constexpr int kCsPortion = 16;     // keys per portion (one decay pivot)
 constexpr int kCsP = 64;           // head width
 constexpr int kCsMaxQ = 256;       // longest chunk
 constexpr int kCsBox = 32;         // keys per cb box (128 bytes of fp32)
-constexpr int kCsRing = 6;         // slices in flight: A in tensor memory, x in shared memory
-constexpr int kCsRingV = 6;        // heads' vectors in shared memory
+constexpr int kCsRing = 8;         // A slices in tensor memory
+constexpr int kCsPairs = kCsRing / 2;  // slices go in pairs (gs, gs + 1), gs even
+constexpr int kCsRingX = 8;        // x slices in shared memory
+constexpr int kCsPairsX = kCsRingX / 2;
+constexpr int kCsRingV = 4;        // heads' vectors in shared memory
 constexpr int kCsAcc = 4;          // accumulators in tensor memory
 constexpr uint32_t kCsAll = 0xffffffffu;
 
@@ -66,14 +73,16 @@ constexpr int kCsOffCb = 0;                                          // [Q / 32 
 constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;                  // 8 KB
 constexpr int kCsOffX = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
 constexpr int kCsStageBytes = kCsRows * kCsP * 2;                    // 16 KB
-constexpr int kCsOffStage = kCsOffX + kCsRing * kCsSliceBytesX;      // [2]
+constexpr int kCsOffStage = kCsOffX + kCsRingX * kCsSliceBytesX;     // one tile
 constexpr int kCsVecBytes = 2 * kCsMaxQ * 4;                         // dA_cs, dt of one head
-constexpr int kCsOffVec = kCsOffStage + 2 * kCsStageBytes;           // [ring]
-constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [ring][64] key factors
-constexpr int kCsOffBar = kCsOffKf + kCsRing * kCsSlice * 4;
-// cb_full, slot_full[R], slot_free[R], v_full[RV], v_free[RV],
-// acc_full[ACC], acc_free[ACC], drain
-constexpr int kCsNumBars = 1 + 2 * kCsRing + 2 * kCsRingV + 2 * kCsAcc + 1;
+constexpr int kCsOffVec = kCsOffStage + kCsStageBytes;               // [ring]
+constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [vector ring][Q] key factors
+constexpr int kCsOffMask = kCsOffKf + kCsRingV * kCsMaxQ * 4;        // [vector ring] rise masks
+constexpr int kCsOffBar = kCsOffMask + kCsRingV * 4;
+// cb_full, pair_full[R / 2], pair_free[R / 2], xp_full[RX / 2],
+// xp_free[RX / 2], v_full[RV], v_free[RV], kf_full[RV], acc_full[ACC],
+// acc_free[ACC], drain
+constexpr int kCsNumBars = 1 + 2 * kCsPairs + 2 * kCsPairsX + 3 * kCsRingV + 2 * kCsAcc + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
 static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
@@ -82,7 +91,7 @@ static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kCsTmemCols = 512;
 constexpr uint32_t kCsTmemA = kCsAcc * kCsP;
 static_assert(kCsTmemA + kCsRing * (kCsSlice / 2) <= kCsTmemCols, "tensor memory budget");
-constexpr uint32_t kCsBarOut = 1 + kCsScaleGroups;  // named barrier of the output warpgroup
+constexpr uint32_t kCsBarOut = 1;  // named barrier of the output warpgroup
 
 __device__ __forceinline__ bool cs_warp_wait(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, uint64_t budget) {
@@ -105,16 +114,23 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   uint8_t* sStage = smem + kCsOffStage;
   uint8_t* sVec = smem + kCsOffVec;
   float* sKfAll = reinterpret_cast<float*>(smem + kCsOffKf);
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + kCsOffMask);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCsOffBar);
   uint64_t* cb_full = bars;
-  // slot_full[i]: the A slice written (128 arrivals of its warpgroup) and
-  // the x slice landed (one arrival with its bytes); slot_free[i]: the
-  // products that read both are done
-  uint64_t* slot_full = bars + 1;
-  uint64_t* slot_free = slot_full + kCsRing;
-  uint64_t* v_full = slot_free + kCsRing;
+  // Slices gs and gs + 1 (gs even, the same head: a head has an even
+  // number of slices) share the barriers of pair gs / 2: its A slices in
+  // slot pair (gs / 2) % kCsPairs (pair_full: 128 arrivals of each slice's
+  // warpgroup), its x slices in x slot pair (gs / 2) % kCsPairsX (xp_full:
+  // one arrival with its bytes per slice); the matching _free barriers say
+  // the products that read them are done.
+  uint64_t* pair_full = bars + 1;
+  uint64_t* pair_free = pair_full + kCsPairs;
+  uint64_t* xp_full = pair_free + kCsPairs;
+  uint64_t* xp_free = xp_full + kCsPairsX;
+  uint64_t* v_full = xp_free + kCsPairsX;
   uint64_t* v_free = v_full + kCsRingV;
-  uint64_t* acc_full = v_free + kCsRingV;
+  uint64_t* kf_full = v_free + kCsRingV;    // the head's key factors and rise mask written
+  uint64_t* acc_full = kf_full + kCsRingV;
   uint64_t* acc_free = acc_full + kCsAcc;
   uint64_t* drain = acc_free + kCsAcc;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + kCsOffMisc);
@@ -138,18 +154,24 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   const int g = h0 / (p.H / p.G);              // the block's group (HB divides H / G)
   const int m0 = mt * kCsRows;                 // first row of the tile within the chunk
   const int n_slices = (m0 + kCsRows) / kCsSlice;  // keys 0 .. m0 + 127 are visible to some row
+  const int log_ns = (n_slices == 4) ? 2 : 1;      // n_slices is 2 or 4 (Q = 128 or 256)
   const int n_boxes = 2 * n_slices;
   const int total = p.HB * n_slices;           // slices of the CTA
 
   if (threadIdx.x == 0) {
     mbar_init(cb_full, 1);
-    for (int i = 0; i < kCsRing; ++i) {
-      mbar_init(&slot_full[i], 128 + 1);
-      mbar_init(&slot_free[i], 1);
+    for (int i = 0; i < kCsPairs; ++i) {
+      mbar_init(&pair_full[i], 2 * 128);
+      mbar_init(&pair_free[i], 1);
+    }
+    for (int i = 0; i < kCsPairsX; ++i) {
+      mbar_init(&xp_full[i], 2);
+      mbar_init(&xp_free[i], 1);
     }
     for (int i = 0; i < kCsRingV; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_free[i], 128 * n_slices);  // every slice's warpgroup
+      mbar_init(&kf_full[i], 32);
     }
     for (int i = 0; i < kCsAcc; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -171,46 +193,31 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   if (warp < kCsOutWarp0) {
     // ---------------------------------------------------------- scaling
     const int w = warp >> 2;                   // warpgroup
-    const int t = threadIdx.x & 127;           // thread of the warpgroup
-    const int r = (warp & 3) * 32 + lane;      // row of the tile = tensor-memory lane
-    const int m = m0 + r;                      // row of the chunk
-    const int row0 = m0 + (warp & 3) * 32;     // the warp's first row
+    // Tensor-memory lanes 32q .. 32q + 31 (q = warp % 4, the warp's
+    // scheduler) hold the tile's row block (q + j) % 4 for head j: the rows
+    // near the diagonal cost the most, and rotating the blocks over the
+    // heads spreads them over the four schedulers.
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float l2e = 1.4426950408889634f;
     const uint64_t nl2e2 = f2_pack(-l2e, -l2e);
     bool ok = cs_warp_wait(cb_full, 0, sAbort, budget);
-    for (int gs = w; gs < total; gs += kCsScaleGroups) {
-      const int j = gs / n_slices;             // head of the block
-      const int s = gs - j * n_slices;         // slice of the head
+    for (int gs = w; gs < total && ok; gs += kCsScaleGroups) {
+      const int j = gs >> log_ns;              // head of the block
+      const int s = gs & (n_slices - 1);       // slice of the head
       const int vs = j % kCsRingV;
       const int slot = gs % kCsRing;
-      ok = ok && cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget);
-      ok = ok && (gs < kCsRing ||
-                  cs_warp_wait(&slot_free[slot], ((gs / kCsRing) - 1) & 1, sAbort, budget));
+      const int pr = gs >> 1;                  // pair
+      ok = ok && cs_warp_wait(&kf_full[vs], (j / kCsRingV) & 1, sAbort, budget);
+      ok = ok && (pr < kCsPairs || cs_warp_wait(&pair_free[pr % kCsPairs],
+                                                ((pr / kCsPairs) - 1) & 1, sAbort, budget));
       tc_fence_after_sync();                   // the slot's last products are done before it is rewritten
       const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
       const float* sDT = sDA + kCsMaxQ;
-      float* sKf = sKfAll + slot * kCsSlice;
-      // Key factors of the slice, kf[k] = exp(dA_cs[k | 15] - dA_cs[k]) dt[k]
-      // (k | 15 is the last key of k's 16-key portion).  For a row m at or
-      // after k | 15,
-      //   exp(dA_cs[m] - dA_cs[k]) = exp(dA_cs[m] - dA_cs[k | 15]) exp(dA_cs[k | 15] - dA_cs[k]),
-      // and where both exponents are <= 0 (dA_cs does not rise, as with
-      // dt > 0 and A < 0) both factors lie in [0, 1]: a portion wholly at or
-      // before a row then costs one exponential per row and one per key
-      // instead of one per (row, key).  `rises` flags a key whose factor
-      // would exceed 1; the slice then keeps one exponential per (row, key).
-      bool rises = false;
-      if (ok && t < kCsSlice) {
-        const int k = s * kCsSlice + t;
-        const float dak = sDA[k];
-        const float dap = sDA[k | (kCsPortion - 1)];
-        sKf[t] = ex2_approx((dap - dak) * l2e) * sDT[k];
-        rises = !(dap <= dak);
-      }
-      // every thread of the warpgroup passes this barrier once per slice,
-      // also after a failed wait, so none is left waiting on it
-      const bool factor = !barrier_or(1 + w, 128, rises || !ok);
+      const float* sKf = sKfAll + vs * kCsMaxQ + s * kCsSlice;
+      const uint32_t rises = sMask[vs] >> (s * (kCsSlice / kCsPortion));
+      const int r = ((warp + j) & 3) * 32 + lane;  // row of the tile
+      const int m = m0 + r;                      // row of the chunk
+      const int row0 = m0 + ((warp + j) & 3) * 32;  // the warp's first row
       if (ok) {
         const float da_raw = sDA[m];
         const float da_m = da_raw * l2e;
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
             // every key after every row of the warp
 #pragma unroll
             for (int q = 0; q < kCsPortion / 2; ++q) pk[q] = 0u;
-          } else if (factor && k0 + kCsPortion - 1 <= row0 && da_raw <= dap) {
+          } else if (!((rises >> pi) & 1u) && k0 + kCsPortion - 1 <= row0 && da_raw <= dap) {
             // every key at or before the row: row factor times key factors
             const float rowf = ex2_approx((da_raw - dap) * l2e);
             const uint64_t rf2 = f2_pack(rowf, rowf);
@@ -281,22 +288,22 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&slot_full[slot]);
+        mbar_arrive(&pair_full[pr % kCsPairs]);
         mbar_arrive(&v_free[vs]);              // this slice no longer reads the head's vectors
       }
     }
   } else if (warp < kCsMmaWarp) {
     // ---------------------------------------------------------- output
-    const int r = (warp & 3) * 32 + lane;      // row of the tile = tensor-memory lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool issuer = (warp == kCsOutWarp0) && elect_one();
     bool ok = true;
     for (int j = 0; j < p.HB; ++j) {
       const int a = j % kCsAcc;
       ok = ok && cs_warp_wait(&acc_full[a], (j / kCsAcc) & 1, sAbort, budget);
-      uint8_t* stage = sStage + (j & 1) * kCsStageBytes;
-      // the store that last read this staging tile (head j - 2) is done reading
-      if (issuer) tma_store_wait_read<1>();
+      const int r = ((warp + j) & 3) * 32 + lane;  // the tile row in this lane for head j
+      uint8_t* stage = sStage;
+      // the store of head j - 1 is done reading the staging tile
+      if (issuer) tma_store_wait_read<0>();
       __syncwarp();
       named_barrier_sync(kCsBarOut, 128);
       if (ok) {
@@ -335,39 +342,118 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     const bool leader = elect_one();
     constexpr uint32_t idesc = make_idesc_bf16_f32(128, kCsP, false, true);
     bool ok = true;
-    for (int gs = 0; gs < total && ok; ++gs) {
-      const int j = gs / n_slices;
-      const int s = gs - j * n_slices;
+    for (int pr = 0; 2 * pr < total && ok; ++pr) {
+      const int j = (2 * pr) >> log_ns;
+      const int s0 = (2 * pr) & (n_slices - 1);  // first slice of the pair within its head
       const int a = j % kCsAcc;
-      const int slot = gs % kCsRing;
+      const int ps = pr % kCsPairs, px = pr % kCsPairsX;
       // accumulator a must have been read out (head j - 4)
-      if (s == 0 && j >= kCsAcc &&
+      if (s0 == 0 && j >= kCsAcc &&
           !cs_warp_wait(&acc_free[a], ((j / kCsAcc) - 1) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
-      if (!cs_warp_wait(&slot_full[slot], (gs / kCsRing) & 1, sAbort, budget)) {
+      if (!cs_warp_wait(&pair_full[ps], (pr / kCsPairs) & 1, sAbort, budget) ||
+          !cs_warp_wait(&xp_full[px], (pr / kCsPairsX) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       if (leader) {
-        const uint32_t a_tmem = tmem + kCsTmemA + slot * (kCsSlice / 2);
-        // the x slice is a single 64-wide slab: the leading offset is unused
-        const uint64_t b_desc =
-            make_smem_desc_sw128(smem_u32(sX + slot * kCsSliceBytesX), 1024, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kCsSlice / 16; ++kk) {
-          mma_ts(tmem + a * kCsP, a_tmem + kk * 8, b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
-                 (s > 0 || kk > 0) ? 1u : 0u);
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t a_tmem = tmem + kCsTmemA + (2 * ps + i) * (kCsSlice / 2);
+          // the x slice is a single 64-wide slab: the leading offset is unused
+          const uint64_t b_desc =
+              make_smem_desc_sw128(smem_u32(sX + (2 * px + i) * kCsSliceBytesX), 1024, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kCsSlice / 16; ++kk) {
+            mma_ts(tmem + a * kCsP, a_tmem + kk * 8, b_desc + (uint64_t)((kk * 2048) >> 4),
+                   idesc, (s0 + i > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        tc_commit(&slot_free[slot]);
-        if (s + 1 == n_slices) tc_commit(&acc_full[a]);
+        tc_commit(&pair_free[ps]);
+        tc_commit(&xp_free[px]);
+        if (s0 + 2 == n_slices) tc_commit(&acc_full[a]);
       }
     }
     if (leader) {
       tc_commit(drain);
       cs_drain_wait(drain, 0, budget);
+    }
+    __syncwarp();
+  } else if (warp == kCsVecWarp) {
+    // ---------------------------------------------------------- key factors
+    // Per head, kf[k] = exp(dA_cs[k | 15] - dA_cs[k]) dt[k] (k | 15 is the
+    // last key of k's 16-key portion) and a mask with bit i set where
+    // portion i has a key whose factor would exceed 1.  For a row m at or
+    // after k | 15,
+    //   exp(dA_cs[m] - dA_cs[k]) = exp(dA_cs[m] - dA_cs[k | 15]) exp(dA_cs[k | 15] - dA_cs[k]),
+    // and where both exponents are <= 0 (dA_cs does not rise, as with
+    // dt > 0 and A < 0) both factors lie in [0, 1]: a portion wholly at or
+    // before a row then costs one exponential per row and one per key
+    // instead of one per (row, key).
+    // It also loads each head's dA_cs and dt (1-D bulk copies) into a ring of
+    // kCsRingV slots, as far ahead of the head it works on as the slots
+    // allow.
+    const float l2e = 1.4426950408889634f;
+    const bool leader = elect_one();
+    bool ok = true;
+    int issued = 0;
+    auto issue = [&](int jn) {
+      const int vs = jn % kCsRingV;
+      if (leader) {
+        const size_t off = (((size_t)b * p.H + h0 + jn) * p.nchunks + c) * p.Q;
+        float* dst = reinterpret_cast<float*>(sVec + vs * kCsVecBytes);
+        mbar_arrive_expect_tx(&v_full[vs], 2 * p.Q * 4);
+        bulk_load(dst, p.dA_cs + off, p.Q * 4, &v_full[vs]);
+        bulk_load(dst + kCsMaxQ, p.dt + off, p.Q * 4, &v_full[vs]);
+      }
+      __syncwarp();
+    };
+    for (int j = 0; j < p.HB && ok; ++j) {
+      const int vs = j % kCsRingV;
+      // issue every later head whose slot is free (without waiting), and
+      // head j itself in any case (waiting for its slot if need be)
+      while (ok && issued < p.HB) {
+        const int jn = issued;
+        if (jn >= kCsRingV) {
+          bool free_now = mbar_test_wait(&v_free[jn % kCsRingV], ((jn / kCsRingV) - 1) & 1);
+          free_now = __all_sync(kCsAll, free_now);
+          if (!free_now) {
+            if (jn > j) break;
+            ok = cs_warp_wait(&v_free[jn % kCsRingV], ((jn / kCsRingV) - 1) & 1, sAbort, budget);
+            if (!ok) break;
+          }
+        }
+        issue(jn);
+        ++issued;
+      }
+      if (!ok || !cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget)) {
+        ok = false;
+        break;
+      }
+      const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
+      const float* sDT = sDA + kCsMaxQ;
+      float* sKf = sKfAll + vs * kCsMaxQ;
+      uint32_t mask = 0;
+      for (int i = 0; i < p.Q / 32; ++i) {
+        const int k = 32 * i + lane;
+        const float dak = sDA[k];
+        const float dap = sDA[k | (kCsPortion - 1)];
+        sKf[k] = ex2_approx((dap - dak) * l2e) * sDT[k];
+        const uint32_t bal = __ballot_sync(kCsAll, !(dap <= dak));
+        mask |= ((bal & 0xffffu) ? 1u : 0u) << (2 * i);
+        mask |= ((bal >> 16) ? 1u : 0u) << (2 * i + 1);
+      }
+      if (lane == 0) sMask[vs] = mask;
+      __syncwarp();
+      mbar_arrive(&kf_full[vs]);
+    }
+    // every copy issued lands before the CTA exits
+    if (leader) {
+      for (int j = issued > kCsRingV ? issued - kCsRingV : 0; j < issued; ++j)
+        cs_drain_wait(&v_full[j % kCsRingV], (j / kCsRingV) & 1, budget);
     }
     __syncwarp();
   } else {
@@ -376,7 +462,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     const uint64_t pol_x = l2_policy_evict_first();
     const uint64_t pol_cb = l2_policy_evict_last();
     bool ok = true;
-    int gs = 0, issued_v = 0;
+    int gs = 0;
     if (leader) {
       mbar_arrive_expect_tx(cb_full, n_boxes * kCsBoxBytes);
       const int zc = (b * p.nchunks + c) * p.G + g;
@@ -385,7 +471,6 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     }
     for (int j = 0; j < p.HB && ok; ++j) {
       const int h = h0 + j;
-      const int vs = j % kCsRingV;
       if (leader) {
         // the x slices and vectors of the head two ahead into L2, so that
         // their loads into the rings wait on L2 rather than on DRAM
@@ -397,46 +482,28 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
           bulk_prefetch_l2(p.dt + off, p.Q * 4);
         }
       }
-      if (j >= kCsRingV &&
-          !cs_warp_wait(&v_free[vs], ((j / kCsRingV) - 1) & 1, sAbort, budget)) {
-        ok = false;
-        break;
-      }
-      if (leader) {
-        const size_t vec_off = (((size_t)b * p.H + h) * p.nchunks + c) * p.Q;
-        float* dst = reinterpret_cast<float*>(sVec + vs * kCsVecBytes);
-        mbar_arrive_expect_tx(&v_full[vs], 2 * p.Q * 4);
-        bulk_load(dst, p.dA_cs + vec_off, p.Q * 4, &v_full[vs]);
-        bulk_load(dst + kCsMaxQ, p.dt + vec_off, p.Q * 4, &v_full[vs]);
-      }
-      ++issued_v;
       for (int s = 0; s < n_slices; ++s, ++gs) {
-        const int slot = gs % kCsRing;
-        if (gs >= kCsRing &&
-            !cs_warp_wait(&slot_free[slot], ((gs / kCsRing) - 1) & 1, sAbort, budget)) {
+        const int pr = gs >> 1;
+        const int px = pr % kCsPairsX;
+        if ((gs & 1) == 0 && pr >= kCsPairsX &&
+            !cs_warp_wait(&xp_free[px], ((pr / kCsPairsX) - 1) & 1, sAbort, budget)) {
           ok = false;
           break;
         }
         if (leader) {
-          mbar_arrive_expect_tx(&slot_full[slot], kCsSliceBytesX);
-          tma_load_4d(sX + slot * kCsSliceBytesX, &p.tm_x, &slot_full[slot], 0, h,
+          mbar_arrive_expect_tx(&xp_full[px], kCsSliceBytesX);
+          tma_load_4d(sX + (2 * px + (gs & 1)) * kCsSliceBytesX, &p.tm_x, &xp_full[px], 0, h,
                       c * p.Q + s * kCsSlice, b, pol_x);
         }
       }
     }
-    // every copy issued lands before the CTA exits.  An x slice's phase
-    // also needs its warpgroup's arrivals: after an abort those may never
-    // come, so the wait for them is cut short (the copies themselves land
-    // within microseconds)
+    // every copy issued lands before the CTA exits (the producer stops only
+    // before the first slice of a pair, so every x pair it started is whole)
     if (leader) {
       cs_drain_wait(cb_full, 0, budget);
-      const int first_v = issued_v > kCsRingV ? issued_v - kCsRingV : 0;
-      for (int j = first_v; j < issued_v; ++j)
-        cs_drain_wait(&v_full[j % kCsRingV], (j / kCsRingV) & 1, budget);
-      const uint64_t x_budget = *sAbort ? (budget < 1000000ull ? budget : 1000000ull) : budget;
-      const int first_x = gs > kCsRing ? gs - kCsRing : 0;
-      for (int t = first_x; t < gs; ++t)
-        cs_drain_wait(&slot_full[t % kCsRing], (t / kCsRing) & 1, x_budget);
+      const int np = gs / 2;                   // pairs with both x slices issued
+      for (int pr = np > kCsPairsX ? np - kCsPairsX : 0; pr < np; ++pr)
+        cs_drain_wait(&xp_full[pr % kCsPairsX], (pr / kCsPairsX) & 1, budget);
     }
     __syncwarp();
   }
