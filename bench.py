@@ -74,6 +74,46 @@ def load_hbm_peak():
         return 6800.0, "fallback"
 
 
+def flush_bytes_for(in_bytes: int) -> int:
+    """Bytes to write between timed steps: none when the inputs alone are
+    larger than L2 (each step then reads them from DRAM), else a buffer of
+    four times L2."""
+    return 0 if in_bytes > L2_BYTES else 4 * L2_BYTES
+
+
+def l2_note(in_bytes: int, flush_bytes: int) -> str:
+    if flush_bytes == 0:
+        return f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
+    return f"L2 flushed before each timed step ({flush_bytes / 1e6:.0f} MB written, outside the timed events)"
+
+
+def time_steps(step, steps, stream, dev, flush_bytes):
+    """Device seconds of `steps` calls of step() on `stream`.  Without a
+    flush one pair of CUDA events brackets all steps; with one, a buffer of
+    `flush_bytes` is written before each step, outside a pair of events per
+    step, and the per-step times are summed."""
+    import torch
+    if flush_bytes <= 0:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        return start.elapsed_time(end) / 1e3
+    buf = torch.empty(flush_bytes, dtype=torch.uint8, device=dev)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            buf.fill_(i & 0xFF)
+            events[i][0].record(stream)
+            step()
+            events[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in events) / 1e3
+
+
 def load_traffic():
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -318,22 +358,17 @@ def run_ours(args, w):
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
 
+    flush = flush_bytes_for(in_bytes)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
     sampler = ClockSampler(smi_index)
     sampler.start()
     time.sleep(0.2)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    start.record(stream)
-    for _ in range(args.steps):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    t_local = time_steps(step, args.steps, stream, dev, flush)
     barrier(world)
     clocks = sampler.stop()
-    t_local = start.elapsed_time(end) / 1e3
     t = max_over_ranks(t_local, world)
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out in the timed region")
@@ -396,8 +431,7 @@ def run_ours(args, w):
             "workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S_q": w.S_q,
             "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
             "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
-            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
-                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+            "l2": l2_note(in_bytes, flush),
         },
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": ({
@@ -468,27 +502,24 @@ def run_bwd(args, w):
         ap.attn_bwd(q, k, v, o, lse, dout, w.causal, w.scale, workspace=ws, out=(dq, dk, dv),
                     stream=stream)
 
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dout, o, lse))
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
+    flush = flush_bytes_for(in_bytes)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
     sampler = ClockSampler(smi_index)
     sampler.start()
     time.sleep(0.2)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    start.record(stream)
-    for _ in range(args.steps):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    t_local = time_steps(step, args.steps, stream, dev, flush)
     barrier(world)
     clocks = sampler.stop()
-    t_local = start.elapsed_time(end) / 1e3
     t = max_over_ranks(t_local, world)
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out in the timed region")
@@ -527,7 +558,6 @@ def run_bwd(args, w):
     flops = 2.5 * w.flops
     per_launch = t_local / args.steps
     achieved = flops / per_launch / 1e12
-    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dout, o, lse))
     out_bytes = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     line = {
         "metric": "attention bwd TFLOP/s (bf16, fp32 acc; 2.5x the forward's FLOPs)",
@@ -547,8 +577,7 @@ def run_bwd(args, w):
             "workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S_q": w.S_q,
             "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
             "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
-            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
-                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+            "l2": l2_note(in_bytes, flush),
         },
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {
@@ -623,27 +652,24 @@ def run_chunk_scan(args, name):
     def step():
         ap.chunk_scan(cb, dA_cs, dt, x, out=out, stream=stream)
 
+    in_bytes = sum(tt.numel() * tt.element_size() for tt in (cb, dA_cs, dt, x))
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
+    flush = flush_bytes_for(in_bytes)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
     sampler = ClockSampler(smi_index)
     sampler.start()
     time.sleep(0.2)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    start.record(stream)
-    for _ in range(args.steps):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    t_local = time_steps(step, args.steps, stream, dev, flush)
     barrier(world)
     clocks = sampler.stop()
-    t_local = start.elapsed_time(end) / 1e3
     t = max_over_ranks(t_local, world)
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out in the timed region")
@@ -676,7 +702,6 @@ def run_chunk_scan(args, name):
         return
     hbm_peak = load_hbm_peak()
     per_launch = t_local / args.steps
-    in_bytes = sum(tt.numel() * tt.element_size() for tt in dev_in)
     line = {
         "metric": "Mamba2 chunk scan TFLOP/s (bf16 products, fp32 acc; 2 P per visible key)",
         "value": world * w.flops * args.steps / t / 1e12,
@@ -694,8 +719,7 @@ def run_chunk_scan(args, name):
         "config": {
             "workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P, "G": w.G, "Q": w.Q,
             "seed": w.seed, "parallelism": f"replicas x{world}",
-            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB), no flush"
-                  if in_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+            "l2": l2_note(in_bytes, flush),
         },
         "roofline": {
             "bound": "hbm",
