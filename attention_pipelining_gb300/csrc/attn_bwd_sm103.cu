@@ -29,6 +29,7 @@
 // CTA-wide abort flag and the device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 #include <mutex>
 
 #include "attn_internal.h"
@@ -134,6 +135,31 @@ __device__ __forceinline__ bool qblock_sees(const BwdParams& p, int r0, int kv0)
   return last % p.S_q >= kv0;
 }
 
+// Causal grids: CTA idx -> (cost rank, row group), the costliest ranks first,
+// in bands of kRankBand ranks; within a band the CTAs of one row group are
+// adjacent.  The CTAs that run at once (one per SM) then cover a few row
+// groups and share those groups' tiles in L2, instead of every group's (a
+// rank-major order over 32 groups at 16K rows reads 256 MB of Q and dO per
+// sweep, twice the L2).
+constexpr int kRankBand = 16;
+
+__device__ __forceinline__ void banded_rank(int idx, int n_ranks, int groups, int& rank,
+                                            int& zkv) {
+  const int full = n_ranks / kRankBand;  // whole bands
+  const int per_band = groups * kRankBand;
+  if (idx < full * per_band) {
+    const int band = idx / per_band;
+    const int rem = idx - band * per_band;
+    zkv = rem / kRankBand;
+    rank = band * kRankBand + (rem - zkv * kRankBand);
+  } else {
+    const int tail = n_ranks - full * kRankBand;  // ranks of the last, partial band
+    const int rem = idx - full * per_band;
+    zkv = rem / tail;
+    rank = full * kRankBand + (rem - zkv * tail);
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- prep
@@ -205,14 +231,13 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   const uint64_t budget = p.timeout_ns;
 
   // CTA -> (key block, row group): with the causal mask the first key
-  // blocks carry the most query blocks, so all groups' first blocks go
-  // first; without it the blocks of one group are adjacent (they share
-  // their Q and dO tiles in L2)
+  // blocks carry the most query blocks, so they go first (in bands, see
+  // banded_rank); without it the blocks of one group are adjacent (they
+  // share their Q and dO tiles in L2)
   const int n_kvb = (p.S_kv + kRows - 1) / kRows;
   int kvb, zkv;
   if (p.causal) {
-    kvb = blockIdx.x / p.groups;
-    zkv = blockIdx.x - kvb * p.groups;
+    banded_rank((int)blockIdx.x, n_kvb, p.groups, kvb, zkv);
   } else {
     zkv = blockIdx.x / n_kvb;
     kvb = blockIdx.x - zkv * n_kvb;
@@ -301,40 +326,49 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         reg_after_wait(sv);
         reg_after_wait(dp);
         uint32_t pk[16], dk[16];
+        // The masked and unmasked bodies are separate code paths, so the
+        // common (unmasked) one carries no per-element mask arithmetic.
+        auto body = [&](auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = lse4[i4];
-          const float4 d4 = dl4[i4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], dsr[4];
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 l4 = lse4[i4];
+            const float4 d4 = dl4[i4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pr[4], dsr[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * i4 + e;                // element of the slice
-            float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lv[e]);
-            if (masked) {
-              const int rho = r0 + col0 + c;
-              bool vis = (rho < p.R) && (key < p.S_kv);
-              if (p.causal) {
-                int pos;
-                if (p.S_q >= kRows) {
-                  pos = base_pos + col0 + c;
-                  if (pos >= p.S_q) pos -= p.S_q;
-                } else {
-                  pos = rho % p.S_q;
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * i4 + e;                // element of the slice
+              float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lv[e]);
+              if constexpr (kMasked) {
+                const int rho = r0 + col0 + c;
+                bool vis = (rho < p.R) && (key < p.S_kv);
+                if (p.causal) {
+                  int pos;
+                  if (p.S_q >= kRows) {
+                    pos = base_pos + col0 + c;
+                    if (pos >= p.S_q) pos -= p.S_q;
+                  } else {
+                    pos = rho % p.S_q;
+                  }
+                  vis = vis && (key <= pos);
                 }
-                vis = vis && (key <= pos);
+                pv = vis ? pv : 0.f;
               }
-              pv = vis ? pv : 0.f;
+              pr[e] = pv;
+              dsr[e] = pv * (u2f_b(dp[c]) - dv4[e]);
             }
-            pr[e] = pv;
-            dsr[e] = pv * (u2f_b(dp[c]) - dv4[e]);
+            pk[2 * i4] = pack_bf16x2(pr[0], pr[1]);
+            pk[2 * i4 + 1] = pack_bf16x2(pr[2], pr[3]);
+            dk[2 * i4] = pack_bf16x2(dsr[0], dsr[1]);
+            dk[2 * i4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
           }
-          pk[2 * i4] = pack_bf16x2(pr[0], pr[1]);
-          pk[2 * i4 + 1] = pack_bf16x2(pr[2], pr[3]);
-          dk[2 * i4] = pack_bf16x2(dsr[0], dsr[1]);
-          dk[2 * i4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
-        }
+        };
+        if (masked)
+          body(std::true_type{});
+        else
+          body(std::false_type{});
         // P^T and dS^T of the slice: 16 columns from col0 in the S^T and
         // dP^T regions (this warpgroup's own, already-read columns)
         tmem_st_x16(tmem + lane_base + C::kTmS + col0, pk);
@@ -514,13 +548,13 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
 
   // CTA -> (query block, row group): with the causal mask by cost rank,
   // longest first (with S_q a multiple of 128 a rank is one position block
-  // of one head of the group, so the group's heads interleave), then group;
-  // without it group-major, query blocks last to first
+  // of one head of the group, so the group's heads interleave), in bands
+  // (see banded_rank); without it group-major, query blocks last to first
   const int n_qb = (p.R + kRows - 1) / kRows;
   int qb, zkv;
   if (p.causal) {
-    const int rank = blockIdx.x / p.groups;
-    zkv = blockIdx.x - rank * p.groups;
+    int rank;
+    banded_rank((int)blockIdx.x, n_qb, p.groups, rank, zkv);
     const int hr = p.R / p.S_q;  // heads per group
     if (p.S_q % kRows == 0) {
       const int nh = p.S_q / kRows;
