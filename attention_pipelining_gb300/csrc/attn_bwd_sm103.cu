@@ -633,18 +633,26 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
         reg_after_wait(sv);
         reg_after_wait(dp);
         uint32_t dk[16];
+        // separate masked and unmasked code paths, as in the dK/dV kernel
+        auto body = [&](auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float dsr[2];
+          for (int i = 0; i < 16; ++i) {
+            float dsr[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 2 * i + e;
-            float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lse2);
-            if (masked) pv = (row_ok && kb0 + col0 + c < key_limit) ? pv : 0.f;
-            dsr[e] = pv * (u2f_b(dp[c]) - dl);
+            for (int e = 0; e < 2; ++e) {
+              const int c = 2 * i + e;
+              float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lse2);
+              if constexpr (kMasked) pv = (row_ok && kb0 + col0 + c < key_limit) ? pv : 0.f;
+              dsr[e] = pv * (u2f_b(dp[c]) - dl);
+            }
+            dk[i] = pack_bf16x2(dsr[0], dsr[1]);
           }
-          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
-        }
+        };
+        if (masked)
+          body(std::true_type{});
+        else
+          body(std::false_type{});
         // dS of the slice: 16 columns from col0 of the S region (this
         // warpgroup's own, already-read columns)
         tmem_st_x16(tmem + lane_base + C::kTmS + col0, dk);
