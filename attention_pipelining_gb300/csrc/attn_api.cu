@@ -285,8 +285,8 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   p.dk = dk;
   p.dv = dv;
   const int64_t Rp = bwd_padded_rows(H_q, H_kv, S_q);
-  p.lse2 = static_cast<float*>(workspace);
-  p.delta = p.lse2 + (size_t)B * H_kv * Rp;
+  p.nlse2 = static_cast<float*>(workspace);
+  p.ndelta = p.nlse2 + (size_t)B * H_kv * Rp;
   p.B = B;
   p.H_q = H_q;
   p.H_kv = H_kv;

@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
   const int rho = (int)(row - z * p.Rp);
   if (rho >= p.R) {
     if (lane == 0) {
-      p.delta[row] = 0.f;
-      p.lse2[row] = 0.f;
+      p.ndelta[row] = 0.f;
+      p.nlse2[row] = 0.f;
     }
     return;
   }
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kAll, acc, off);
   if (lane == 0) {
-    p.delta[row] = acc;
-    p.lse2[row] = lse[z * p.R + rho] * 1.4426950408889634f;
+    p.ndelta[row] = -acc;
+    p.nlse2[row] = -(lse[z * p.R + rho] * 1.4426950408889634f);
   }
 }
 
@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kv0 + r;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
     int n = 0;
     for (int qb = 0; qb < n_qb && ok; ++qb) {
@@ -332,22 +333,26 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
           constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 l4 = lse4[i4];
-            const float4 d4 = dl4[i4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pr[4], dsr[4];
+            const float4 l4 = lse4[i4];              // -LSE * log2(e) of 4 queries
+            const float4 d4 = dl4[i4];               // -D of the same queries
+            const int c = 4 * i4;                    // first element of the four
+            // x = s * scale * log2(e) - LSE * log2(e), two lanes per instruction
+            float x[4];
+            f2_unpack(f2_fma(f2_pack(u2f_b(sv[c]), u2f_b(sv[c + 1])), sl2x2, f2_pack(l4.x, l4.y)),
+                      x[0], x[1]);
+            f2_unpack(f2_fma(f2_pack(u2f_b(sv[c + 2]), u2f_b(sv[c + 3])), sl2x2,
+                             f2_pack(l4.z, l4.w)), x[2], x[3]);
+            float pr[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int c = 4 * i4 + e;                // element of the slice
-              float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lv[e]);
+              float pv = ex2_approx(x[e]);
               if constexpr (kMasked) {
-                const int rho = r0 + col0 + c;
+                const int rho = r0 + col0 + c + e;
                 bool vis = (rho < p.R) && (key < p.S_kv);
                 if (p.causal) {
                   int pos;
                   if (p.S_q >= kRows) {
-                    pos = base_pos + col0 + c;
+                    pos = base_pos + col0 + c + e;
                     if (pos >= p.S_q) pos -= p.S_q;
                   } else {
                     pos = rho % p.S_q;
@@ -357,12 +362,21 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
                 pv = vis ? pv : 0.f;
               }
               pr[e] = pv;
-              dsr[e] = pv * (u2f_b(dp[c]) - dv4[e]);
             }
+            // dS = P (dP - D)
+            const uint64_t ds01 = f2_mul(f2_pack(pr[0], pr[1]),
+                                         f2_add(f2_pack(u2f_b(dp[c]), u2f_b(dp[c + 1])),
+                                                f2_pack(d4.x, d4.y)));
+            const uint64_t ds23 = f2_mul(f2_pack(pr[2], pr[3]),
+                                         f2_add(f2_pack(u2f_b(dp[c + 2]), u2f_b(dp[c + 3])),
+                                                f2_pack(d4.z, d4.w)));
+            float d0, d1, d2, d3;
+            f2_unpack(ds01, d0, d1);
+            f2_unpack(ds23, d2, d3);
             pk[2 * i4] = pack_bf16x2(pr[0], pr[1]);
             pk[2 * i4 + 1] = pack_bf16x2(pr[2], pr[3]);
-            dk[2 * i4] = pack_bf16x2(dsr[0], dsr[1]);
-            dk[2 * i4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
+            dk[2 * i4] = pack_bf16x2(d0, d1);
+            dk[2 * i4 + 1] = pack_bf16x2(d2, d3);
           }
         };
         if (masked)
@@ -504,8 +518,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         tma_load_tile<D>(stage_q(s), &p.tm_q, &q_full[s], r0, zkv, pol_q);
         tma_load_tile<D>(stage_do(s), &p.tm_do, &q_full[s], r0, zkv, pol_q);
         const size_t vo = (size_t)zkv * p.Rp + r0;
-        bulk_load(stage_lse(s), p.lse2 + vo, C::kVecBytes, &q_full[s]);
-        bulk_load(stage_delta(s), p.delta + vo, C::kVecBytes, &q_full[s]);
+        bulk_load(stage_lse(s), p.nlse2 + vo, C::kVecBytes, &q_full[s]);
+        bulk_load(stage_delta(s), p.ndelta + vo, C::kVecBytes, &q_full[s]);
       }
       ++issued;
     }
@@ -610,11 +624,12 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     const int rho = r0 + r;
     const bool row_ok = rho < p.R;
     const size_t vo = (size_t)zkv * p.Rp + rho;    // in the padded layout (rho < Rp)
-    const float lse2 = p.lse2[vo];
-    const float dl = p.delta[vo];
+    const uint64_t nlse2x2 = f2_pack(p.nlse2[vo], p.nlse2[vo]);  // -LSE * log2(e), twice
+    const uint64_t ndl2 = f2_pack(p.ndelta[vo], p.ndelta[vo]);    // -D_i, twice
     const int pos = rho % p.S_q;
     const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
     for (int j = 0; j < n_kb && ok; ++j) {
       const int kb0 = j * kRows;
@@ -638,15 +653,18 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
           constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float dsr[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = 2 * i + e;
-              float pv = ex2_approx(u2f_b(sv[c]) * sl2 - lse2);
-              if constexpr (kMasked) pv = (row_ok && kb0 + col0 + c < key_limit) ? pv : 0.f;
-              dsr[e] = pv * (u2f_b(dp[c]) - dl);
+            const int c = 2 * i;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(u2f_b(sv[c]), u2f_b(sv[c + 1])), sl2x2, nlse2x2), x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if constexpr (kMasked) {
+              p0 = (row_ok && kb0 + col0 + c < key_limit) ? p0 : 0.f;
+              p1 = (row_ok && kb0 + col0 + c + 1 < key_limit) ? p1 : 0.f;
             }
-            dk[i] = pack_bf16x2(dsr[0], dsr[1]);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(u2f_b(dp[c]), u2f_b(dp[c + 1])), ndl2)), d0, d1);
+            dk[i] = pack_bf16x2(d0, d1);
           }
         };
         if (masked)

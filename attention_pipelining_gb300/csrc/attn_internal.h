@@ -70,8 +70,9 @@ struct BwdParams {
   void* dq;           // [B, H_q, S_q, D] bf16
   void* dk;           // [B, H_kv, S_kv, D] bf16
   void* dv;           // [B, H_kv, S_kv, D] bf16
-  float* lse2;        // [groups, Rp]: LSE * log2(e) (workspace)
-  float* delta;       // [groups, Rp]: D_i = dO_i . O_i (workspace)
+  float* nlse2;       // [groups, Rp]: -LSE * log2(e) (workspace; negated so the
+                      // kernels' products and sums map onto packed fma / add)
+  float* ndelta;      // [groups, Rp]: -D_i = -(dO_i . O_i) (workspace)
   int B, H_q, H_kv, S_q, S_kv, causal;
   int R, Rp, groups;
   float scale, scale_log2;
