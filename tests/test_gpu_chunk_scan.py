@@ -102,9 +102,10 @@ def test_chunk_scan_rejects_bad_arguments():
 
 def test_chunk_scan_rising_decay():
     """dA_cs that rises somewhere in a chunk (not Mamba2's case, where dt > 0
-    and A < 0 make it fall) next to heads where it falls, in one launch:
-    where it rises the kernel keeps one exponential per (row, key), where it
-    falls it splits the decay into a row and a key factor."""
+    and A < 0 make it fall), or falls by 100 within 16 keys, next to heads
+    where it falls gently, in one launch: where it rises the kernel keeps one
+    exponential per (row, key), elsewhere it splits the decay into a row and a
+    key factor."""
     B, L, H, P, G, Q = 2, 512, 8, 64, 2, 256
     cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=35)
     g = torch.Generator().manual_seed(36)
@@ -112,6 +113,7 @@ def test_chunk_scan_rising_decay():
     dA_cs[:, 1] = walk[:, 1]                     # a random walk: rises and falls
     dA_cs[0, 2, 1, 100:] += 0.3                  # one step up at key 100 of one chunk
     dA_cs[1, 6, 0, 255] += 1e-3                  # a rise at the chunk's last key only
+    dA_cs[1, 3, 0, 40:] -= 100.0                 # a fall of 100 inside one 16-key portion
     got = run(cb, dA_cs, dt, x)
     ref = oracle.chunk_scan_default().chunk_scan(cb, dA_cs, dt, x)
     assert_close("out", got, ref)
