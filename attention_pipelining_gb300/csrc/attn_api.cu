@@ -304,6 +304,126 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   return ATTN_OK;
 }
 
+// ---------------------------------------------------------------- host entry
+//
+// attn_fwd_host: the row groups (b, h_kv) are cut into up to kHostChunks
+// chunks of consecutive groups; a chunk is a contiguous slice of every
+// tensor and a problem of its own (B = 1, its groups' heads).  Its inputs go
+// up on one stream, its kernel runs on one of two compute streams (so one
+// chunk's last tiles overlap the next chunk's first), and its outputs come
+// back on a third: the copies of the other chunks overlap each kernel.  The
+// streams start after, and the caller's stream continues after, the whole.
+constexpr int kHostChunks = 8;
+constexpr size_t kHostPipeMinBytes = size_t(32) << 20;  // smaller inputs: one chunk
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t up = nullptr, down = nullptr, comp[2] = {nullptr, nullptr};
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t loaded[kHostChunks] = {}, computed[kHostChunks] = {};
+};
+static std::mutex g_pipe_mu;
+static HostPipe g_pipe[64];
+
+// The device's streams and events, made on first use (call with g_pipe_mu held).
+static HostPipe* host_pipe(int dev) {
+  HostPipe& hp = g_pipe[dev];
+  if (hp.ready) return &hp;
+  const unsigned sf = cudaStreamNonBlocking;
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&hp.up, sf) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.down, sf) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.comp[0], sf) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.comp[1], sf) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.done, ef) == cudaSuccess;
+  for (int c = 0; ok && c < kHostChunks; ++c)
+    ok = cudaEventCreateWithFlags(&hp.loaded[c], ef) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.computed[c], ef) == cudaSuccess;
+  if (!ok) return nullptr;  // (what was made stays cached for the process)
+  hp.ready = true;
+  return &hp;
+}
+
+static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const void* v_host,
+                                   void* o_host, float* lse_host, void* q_dev, void* k_dev,
+                                   void* v_dev, void* o_dev, float* lse_dev, int B, int H_q,
+                                   int H_kv, int S_q, int S_kv, int D, int causal, float scale,
+                                   cudaStream_t s) {
+  const size_t q_bytes = (size_t)B * H_q * S_q * D * 2;
+  const size_t kv_bytes = (size_t)B * H_kv * S_kv * D * 2;
+  const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
+  const int groups = B * H_kv;
+  const int chunks = (q_bytes + 2 * kv_bytes >= kHostPipeMinBytes)
+                         ? (groups < kHostChunks ? groups : kHostChunks)
+                         : 1;
+  if (chunks <= 1) {
+    if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev, v_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attn_status_t st = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H_q, H_kv, S_q, S_kv, D,
+                                causal, scale, nullptr, 0, 0, -1, kDefaultTimeoutNs, s);
+    if (st != ATTN_OK) return st;
+    if (cudaMemcpyAsync(o_host, o_dev, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(lse_host, lse_dev, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  // queued under the lock, so concurrent callers' chunks do not interleave
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = host_pipe(dev);
+  if (!hp) return ATTN_ERR_CUDA;
+  if (cudaEventRecord(hp->start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->up, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp[0], hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp[1], hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->down, hp->start, 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const int r = H_q / H_kv;
+  const size_t q_group = (size_t)r * S_q * D * 2;     // bytes of one group's Q (and O)
+  const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (and V)
+  const size_t lse_group = (size_t)r * S_q;           // floats of one group's LSE
+  for (int c = 0; c < chunks; ++c) {
+    const int z0 = (int)((long long)groups * c / chunks);
+    const int z1 = (int)((long long)groups * (c + 1) / chunks);
+    const int ng = z1 - z0;
+    const size_t qo = z0 * q_group, qn = ng * q_group;
+    const size_t ko = z0 * kv_group, kn = ng * kv_group;
+    const size_t lo = z0 * lse_group, ln = ng * lse_group;
+    auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+    auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+    if (cudaMemcpyAsync(db(q_dev, qo), hb(q_host, qo), qn, cudaMemcpyHostToDevice, hp->up) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(db(k_dev, ko), hb(k_host, ko), kn, cudaMemcpyHostToDevice, hp->up) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(db(v_dev, ko), hb(v_host, ko), kn, cudaMemcpyHostToDevice, hp->up) !=
+            cudaSuccess ||
+        cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    cudaStream_t cs = hp->comp[c & 1];
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_status_t st =
+        fwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo), lse_dev + lo, 1,
+                 ng * r, ng, S_q, S_kv, D, causal, scale, nullptr, 0, 0, -1, kDefaultTimeoutNs, cs);
+    if (st != ATTN_OK) return st;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(db(o_host, qo), db(o_dev, qo), qn, cudaMemcpyDeviceToHost, hp->down) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(lse_host + lo, lse_dev + lo, ln * sizeof(float), cudaMemcpyDeviceToHost,
+                        hp->down) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  // every chunk's outputs are back (and so its kernel and inputs done)
+  if (cudaEventRecord(hp->done, hp->down) != cudaSuccess ||
+      cudaStreamWaitEvent(s, hp->done, 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const float* dt,
                                      const void* x, void* out, int B, int L, int H, int G, int P,
                                      int Q, attn_stream_t stream) {
@@ -427,21 +547,9 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
   if (st != ATTN_OK) return st;
   st = check_device();
   if (st != ATTN_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t q_bytes = (size_t)B * H_q * S_q * D * 2;
-  const size_t kv_bytes = (size_t)B * H_kv * S_kv * D * 2;
-  const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
-  if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(v_dev, v_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  st = attn_fwd(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H_q, H_kv, S_q, S_kv, D, causal, scale,
-                stream);
-  if (st != ATTN_OK) return st;
-  if (cudaMemcpyAsync(o_host, o_dev, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(lse_host, lse_dev, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  return attnpipe::fwd_host_impl(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
+                                 o_dev, lse_dev, B, H_q, H_kv, S_q, S_kv, D, causal, scale,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 const char* attn_status_string(attn_status_t status) {

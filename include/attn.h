@@ -74,13 +74,22 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        float scale, attn_stream_t stream);
 
 /*
- * The same computation with host inputs and outputs: on `stream`, copies
- * q/k/v from host memory into the caller's device buffers q_dev/k_dev/v_dev,
- * runs attn_fwd into o_dev/lse_dev, and copies o/lse back to host memory.
- * Host buffers should be page-locked for the copies to be asynchronous.
- * Returns once everything is queued; the host outputs are valid after the
- * stream is synchronised.  Same argument rules as attn_fwd for the device
- * buffers; host pointers must be non-null.
+ * The same computation with host inputs and outputs: copies q/k/v from host
+ * memory into the caller's device buffers q_dev/k_dev/v_dev, runs attn_fwd
+ * into o_dev/lse_dev, and copies o/lse back to host memory, ordered after
+ * the work already queued on `stream` and before the work queued on it
+ * afterwards.  Inputs of 32 MiB or more are split into up to 8 chunks of
+ * consecutive (batch, kv-head) row groups, each a contiguous slice of every
+ * tensor: a chunk's inputs go up on one internal stream, its kernel runs on
+ * one of two internal compute streams and its outputs come back on another,
+ * so each chunk's copies overlap the other chunks' kernels.  The internal
+ * streams and events are created on first use, once per device, and kept;
+ * concurrent callers on one device queue their chunks one call at a time.
+ * Every row is computed by the same tiles as in one attn_fwd call, so the
+ * results are bit-identical to it.  Host buffers should be page-locked for
+ * the copies to be asynchronous.  Returns once everything is queued; the
+ * host outputs are valid once `stream` has been synchronised.  Same argument
+ * rules as attn_fwd for the device buffers; host pointers must be non-null.
  */
 attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
                             void *o_host, float *lse_host, void *q_dev, void *k_dev,
