@@ -78,3 +78,15 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_l2_flush_only_when_inputs_fit_in_l2():
+    """Timing rule: between timed steps either the inputs alone exceed L2, or
+    L2 is flushed by writing a buffer larger than it (outside the events)."""
+    big = bench.L2_BYTES + 1
+    assert bench.flush_bytes_for(big) == 0
+    assert "no flush" in bench.l2_note(big, 0)
+    small = bench.L2_BYTES // 4
+    fb = bench.flush_bytes_for(small)
+    assert fb > bench.L2_BYTES
+    assert "flushed" in bench.l2_note(small, fb)
