@@ -306,14 +306,20 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
 
 // ---------------------------------------------------------------- host entry
 //
-// attn_fwd_host: the row groups (b, h_kv) are cut into up to kHostChunks
-// chunks of consecutive groups; a chunk is a contiguous slice of every
-// tensor and a problem of its own (B = 1, its groups' heads).  Its inputs go
-// up on one stream, its kernel runs on one of two compute streams (so one
-// chunk's last tiles overlap the next chunk's first), and its outputs come
-// back on a third: the copies of the other chunks overlap each kernel.  The
-// streams start after, and the caller's stream continues after, the whole.
-constexpr int kHostChunks = 8;
+// attn_fwd_host: the row groups (b, h_kv) are cut into chunks of consecutive
+// groups; a chunk is a contiguous slice of every tensor and a problem of its
+// own (B = 1, its groups' heads).  Its inputs go up on one stream, its kernel
+// runs on one of two compute streams (so one chunk's last tiles overlap the
+// next chunk's first), and its outputs come back on a third: the copies of
+// the other chunks overlap each kernel.  The streams start after, and the
+// caller's stream continues after, the whole.  When the kernels take longer
+// than the copies, 16 chunks (the first chunk's inputs and the last chunk's
+// outputs, which nothing overlaps, are then small); when the copies take
+// longer, 8 (fewer, larger copies).
+constexpr int kHostChunks = 16;
+// Rates on GB300 that decide which side is longer: the forward kernel's
+// dense rate and the host link's copy rate (measured, both directions).
+constexpr double kHostKernelFlops = 1.5e15, kHostLinkBytes = 1.9e11;
 constexpr size_t kHostPipeMinBytes = size_t(32) << 20;  // smaller inputs: one chunk
 
 struct HostPipe {
@@ -354,9 +360,12 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   const size_t kv_bytes = (size_t)B * H_kv * S_kv * D * 2;
   const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
   const int groups = B * H_kv;
-  const int chunks = (q_bytes + 2 * kv_bytes >= kHostPipeMinBytes)
-                         ? (groups < kHostChunks ? groups : kHostChunks)
-                         : 1;
+  const double flops = 4.0 * B * H_q * (double)S_q * S_kv * D * (causal ? 0.5 : 1.0);
+  const bool kernel_longer =
+      flops / kHostKernelFlops > (double)(2 * q_bytes + 2 * kv_bytes) / kHostLinkBytes;
+  const int want = kernel_longer ? kHostChunks : kHostChunks / 2;
+  const int chunks =
+      (q_bytes + 2 * kv_bytes >= kHostPipeMinBytes) ? (groups < want ? groups : want) : 1;
   if (chunks <= 1) {
     if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||

@@ -78,7 +78,8 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * memory into the caller's device buffers q_dev/k_dev/v_dev, runs attn_fwd
  * into o_dev/lse_dev, and copies o/lse back to host memory, ordered after
  * the work already queued on `stream` and before the work queued on it
- * afterwards.  Inputs of 32 MiB or more are split into up to 8 chunks of
+ * afterwards.  Inputs of 32 MiB or more are split into 8 or 16 chunks (16
+ * when the kernels are expected to take longer than the copies) of
  * consecutive (batch, kv-head) row groups, each a contiguous slice of every
  * tensor: a chunk's inputs go up on one internal stream, its kernel runs on
  * one of two internal compute streams and its outputs come back on another,

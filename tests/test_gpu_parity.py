@@ -114,13 +114,22 @@ def test_side_stream_and_host_entry():
     assert_parity(oh, lh, o64, lse64, "host entry")
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_host_entry_pipelined_matches_device(causal):
-    """Inputs of 34 MB: the host entry splits the 8 row groups into chunks
-    whose copies overlap the other chunks' kernels (on the caller's side
-    stream here); every row is computed by the same tiles as in one attn_fwd
-    call, so the outputs are bit-identical to it."""
-    B, Hq, Hkv, S, D = 2, 8, 4, 4096, 128
+HOST_PIPE_SHAPES = [
+    # B, H_q, H_kv, S, D, causal: copies longer than the kernels (8 chunks)
+    (2, 8, 4, 4096, 128, False),
+    (2, 8, 4, 4096, 128, True),
+    # kernels longer than the copies: 16 chunks of one row group each
+    (1, 16, 16, 16384, 128, False),
+]
+
+
+@pytest.mark.parametrize("shape", HOST_PIPE_SHAPES, ids=[str(c) for c in HOST_PIPE_SHAPES])
+def test_host_entry_pipelined_matches_device(shape):
+    """Inputs of 32 MiB or more: the host entry splits the row groups into
+    chunks whose copies overlap the other chunks' kernels (on the caller's
+    side stream here); every row is computed by the same tiles as in one
+    attn_fwd call, so the outputs are bit-identical to it."""
+    B, Hq, Hkv, S, D, causal = shape
     q, k, v = make_qkv(B, Hq, Hkv, S, S, D, seed=7)
     scale = 1 / math.sqrt(D)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
