@@ -108,7 +108,8 @@ def test_bwd_k_scaled_by_3():
     assert_close("dv", dv, rv)
 
 
-@pytest.mark.parametrize("name", ["batched_b4_h16_s2048_d128", "gqa_b8_hq32_hkv8_s4096_d64_k3"])
+@pytest.mark.parametrize("name", ["batched_b4_h16_s2048_d128", "gqa_b8_hq32_hkv8_s4096_d64_k3",
+                                  "long_b1_h32_s16384_d128", "long_causal_b1_h32_s16384_d128"])
 def test_bwd_workload_sampled_rows(name):
     """Workload-size run: sampled query rows (dQ) and key rows (dK, dV) against
     the oracle, plus identities that hold at any size."""
