@@ -1,7 +1,9 @@
 """Benchmark of the fused attention forward on GB300.
 
 One step = one fused attention forward over the whole workload (one kernel
-launch), inputs resident in HBM.  Prints ONE JSON line on rank 0.
+launch), inputs resident in HBM.  Prints ONE JSON line on rank 0.  Without
+``--steps`` the timed region is sized from the warm-up to about 5 s of device
+time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference]
@@ -112,6 +114,34 @@ def time_steps(step, steps, stream, dev, flush_bytes):
             events[i][1].record(stream)
     torch.cuda.synchronize(dev)
     return sum(a.elapsed_time(b) for a, b in events) / 1e3
+
+
+MIN_TIMED_SECONDS = 5.0     # default length of the timed region (device time)
+MIN_DEFAULT_STEPS = 20
+MAX_DEFAULT_STEPS = 20000
+
+
+def warm_up(step, warmup, stream, dev, world):
+    """Runs the untimed warm-up steps and returns their mean device seconds
+    per step (max over ranks), which sizes the timed region when no step
+    count is given."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(warmup):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    return max_over_ranks(start.elapsed_time(end) / 1e3 / warmup, world)
+
+
+def timed_steps(requested, per_step_s):
+    """The step count to time: the one asked for, else enough steps for
+    MIN_TIMED_SECONDS of device time (within MIN/MAX_DEFAULT_STEPS)."""
+    if requested is not None:
+        return requested
+    want = math.ceil(MIN_TIMED_SECONDS / max(per_step_s, 1e-9))
+    return int(min(MAX_DEFAULT_STEPS, max(MIN_DEFAULT_STEPS, want)))
 
 
 def load_traffic():
@@ -290,6 +320,8 @@ def run_reference(args, w):
     oracle.build()
     q, k, v = make_workload(w)
     budget = 150.0
+    if args.steps is None:
+        args.steps = 5
     n = calibrate_oracle(q, k, v, w, budget / max(1, args.steps + args.warmup))
     for s in range(args.warmup):
         time_oracle_rows(q, k, v, w, sample_rows(w, n, seed=100 + s))
@@ -352,9 +384,7 @@ def run_ours(args, w):
         def step():
             ap.attn_fwd_out(q, k, v, o, lse, w.causal, w.scale, stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    args.steps = timed_steps(args.steps, warm_up(step, args.warmup, stream, dev, world))
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
 
@@ -504,9 +534,7 @@ def run_bwd(args, w):
 
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dout, o, lse))
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    args.steps = timed_steps(args.steps, warm_up(step, args.warmup, stream, dev, world))
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
     flush = flush_bytes_for(in_bytes)
@@ -654,9 +682,7 @@ def run_chunk_scan(args, name):
 
     in_bytes = sum(tt.numel() * tt.element_size() for tt in (cb, dA_cs, dt, x))
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    args.steps = timed_steps(args.steps, warm_up(step, args.warmup, stream, dev, world))
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out during warm-up")
     flush = flush_bytes_for(in_bytes)
@@ -799,7 +825,8 @@ def main(argv=None):
     from attention_pipelining_gb300.synthetic import HEADLINE, WORKLOADS
     ap_ = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap_.add_argument("--gpus", type=int, default=1)
-    ap_.add_argument("--steps", type=int, default=300)
+    ap_.add_argument("--steps", type=int, default=None,
+                     help="timed steps (default: enough for %g s of device time)" % MIN_TIMED_SECONDS)
     ap_.add_argument("--warmup", type=int, default=10)
     ap_.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap_.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -817,6 +844,8 @@ def main(argv=None):
     args = ap_.parse_args(argv)
     if args.warmup < 3:
         ap_.error("--warmup must be >= 3")
+    if args.steps is not None and args.steps < 1:
+        ap_.error("--steps must be >= 1")
     w = WORKLOADS[args.workload]
     if args.trace > 0:
         run_trace(args, w)

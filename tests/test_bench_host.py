@@ -90,3 +90,13 @@ def test_l2_flush_only_when_inputs_fit_in_l2():
     fb = bench.flush_bytes_for(small)
     assert fb > bench.L2_BYTES
     assert "flushed" in bench.l2_note(small, fb)
+
+
+def test_timed_steps_default_covers_five_seconds():
+    """An explicit step count is kept; without one, enough steps for the
+    minimum timed duration, within the default bounds."""
+    assert bench.timed_steps(7, 1e-3) == 7
+    n = bench.timed_steps(None, 2.8e-3)
+    assert n * 2.8e-3 >= bench.MIN_TIMED_SECONDS and (n - 1) * 2.8e-3 < bench.MIN_TIMED_SECONDS
+    assert bench.timed_steps(None, 1.0) == bench.MIN_DEFAULT_STEPS
+    assert bench.timed_steps(None, 1e-7) == bench.MAX_DEFAULT_STEPS
