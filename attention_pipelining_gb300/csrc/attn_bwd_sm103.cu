@@ -22,10 +22,13 @@
 // so the elementwise work splits over columns with no exchange.  Every GEMM
 // has the forward's shapes (M = 128, N = 128 or D, K = D or 128).
 //
-// 384 threads: warps 0-7 elementwise (warpgroup w takes columns 64w..64w+63
-// of every 128 x 128 block, thread = TMEM lane = the tile's row), warp 8
-// tensor-core issuer and warp 9 TMA producer (warp-wide, one elected lane
-// issues), warps 10-11 idle.  Every wait is bounded; a timeout raises a
+// Each 128 x 128 block runs as two halves of 64 columns, so the elementwise
+// warps work on one half while the tensor core computes the other.
+//
+// 384 threads: warps 0-7 elementwise (warpgroup w takes columns 32w..32w+31
+// of each half, thread = TMEM lane = the tile's row), warp 8 tensor-core
+// issuer and warp 9 TMA producer (warp-wide, one elected lane issues),
+// warps 10-11 idle.  Every wait is bounded; a timeout raises a
 // CTA-wide abort flag and the device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
 #include <cstdint>
