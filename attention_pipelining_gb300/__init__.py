@@ -18,8 +18,10 @@ import os
 
 from ._build import LIB as _LIB_PATH, build as _build_lib
 
-__all__ = ["attn_fwd", "attn_fwd_out", "attn_fwd_host", "selftest_qk", "selftest_pv",
-           "device_status", "status_string", "lib_path", "AttnError", "STATUS"]
+__all__ = ["attn_fwd", "attn_fwd_out", "attn_fwd_host", "attn_fwd_trace", "attn_fwd_splitkv",
+           "splitkv_default_splits", "attn_bwd", "attn_bwd_host", "bwd_workspace_bytes",
+           "chunk_scan", "selftest_qk", "selftest_pv", "device_status", "status_string",
+           "lib_path", "build", "AttnError", "STATUS"]
 
 STATUS = {
     0: "ATTN_OK",
@@ -36,7 +38,7 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
            "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes",
-           "chunk_scan_fwd"]
+           "attn_bwd_host", "chunk_scan_fwd"]
 
 
 class AttnError(RuntimeError):
@@ -95,6 +97,8 @@ def _load():
     lib.attn_splitkv_noalloc_capacity.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
     lib.attn_bwd.restype = ci
+    lib.attn_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
+    lib.attn_bwd_host.restype = ci
     lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.chunk_scan_fwd.argtypes = [vp] * 5 + [ci] * 6 + [vp]
@@ -263,6 +267,22 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, 
                             B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
                             _stream_handle(stream)), "attn_bwd")
     return dq, dk, dv
+
+
+def attn_bwd_host(q_host, k_host, v_host, o_host, lse_host, dout_host, dq_host, dk_host, dv_host,
+                  q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev, dq_dev, dk_dev, dv_dev,
+                  causal: bool, scale: float, workspace, stream=None) -> None:
+    """Host-buffer backward: copies q, k, v, o, lse, dout (host, ideally
+    pinned) into the device buffers, runs attn_bwd with ``workspace`` (a uint8
+    CUDA tensor of at least bwd_workspace_bytes(...) bytes), copies dq, dk, dv
+    back, all queued on ``stream``."""
+    B, Hq, Sq, D = q_host.shape
+    Hkv, Skv = k_host.shape[1], k_host.shape[2]
+    ts = (q_host, k_host, v_host, o_host, lse_host, dout_host, dq_host, dk_host, dv_host,
+          q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev, dq_dev, dk_dev, dv_dev)
+    _check(_load().attn_bwd_host(*(t.data_ptr() for t in ts), workspace.data_ptr(),
+                                 workspace.numel(), B, Hq, Hkv, Sq, Skv, D, int(bool(causal)),
+                                 float(scale), _stream_handle(stream)), "attn_bwd_host")
 
 
 def chunk_scan(cb, dA_cs, dt, x, out=None, stream=None):

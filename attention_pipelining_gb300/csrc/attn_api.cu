@@ -254,11 +254,12 @@ size_t bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q) {
   return 2 * (size_t)B * H_kv * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
 }
 
-static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
-                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                              void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
-                              int S_q, int S_kv, int D, int causal, float scale,
-                              attn_stream_t stream) {
+// Every check of attn_bwd's arguments, the device's included.
+static attn_status_t bwd_validate(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, const void* dq,
+                                  const void* dk, const void* dv, const void* workspace,
+                                  size_t workspace_bytes, int B, int H_q, int H_kv, int S_q,
+                                  int S_kv, int D, int causal, float scale) {
   attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
   if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
@@ -271,7 +272,16 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   if (((S_kv + 127) / 128) * (int64_t)B * H_kv >= (1ll << 31) ||
       ((R64 + 127) / 128) * (int64_t)B * H_kv >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
-  st = check_device();
+  return check_device();
+}
+
+static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                              int S_q, int S_kv, int D, int causal, float scale,
+                              attn_stream_t stream) {
+  attn_status_t st = bwd_validate(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+                                  B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -306,20 +316,21 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
 
 // ---------------------------------------------------------------- host entry
 //
-// attn_fwd_host: the row groups (b, h_kv) are cut into chunks of consecutive
-// groups; a chunk is a contiguous slice of every tensor and a problem of its
-// own (B = 1, its groups' heads).  Its inputs go up on one stream, its kernel
-// runs on one of two compute streams (so one chunk's last tiles overlap the
-// next chunk's first), and its outputs come back on a third: the copies of
-// the other chunks overlap each kernel.  The streams start after, and the
-// caller's stream continues after, the whole.  When the kernels take longer
-// than the copies, 16 chunks (the first chunk's inputs and the last chunk's
-// outputs, which nothing overlaps, are then small); when the copies take
-// longer, 8 (fewer, larger copies).
+// attn_fwd_host and attn_bwd_host: the row groups (b, h_kv) are cut into
+// chunks of consecutive groups; a chunk is a contiguous slice of every tensor
+// and a problem of its own (B = 1, its groups' heads).  Its inputs go up on
+// one stream, its kernels run on one of two compute streams (so one chunk's
+// last tiles overlap the next chunk's first), and its outputs come back on a
+// third: the copies of the other chunks overlap each chunk's kernels.  The
+// streams start after, and the caller's stream continues after, the whole.
+// When the kernels take longer than the copies, 16 chunks (the first chunk's
+// inputs and the last chunk's outputs, which nothing overlaps, are then
+// small); when the copies take longer, 8 (fewer, larger copies).
 constexpr int kHostChunks = 16;
-// Rates on GB300 that decide which side is longer: the forward kernel's
-// dense rate and the host link's copy rate (measured, both directions).
-constexpr double kHostKernelFlops = 1.5e15, kHostLinkBytes = 1.9e11;
+// Rates on GB300 that decide which side is longer: the forward's and the
+// backward's dense rates and the host link's copy rate (measured, both
+// directions).
+constexpr double kHostKernelFlops = 1.5e15, kHostBwdFlops = 1.0e15, kHostLinkBytes = 1.9e11;
 constexpr size_t kHostPipeMinBytes = size_t(32) << 20;  // smaller inputs: one chunk
 
 struct HostPipe {
@@ -330,6 +341,15 @@ struct HostPipe {
 };
 static std::mutex g_pipe_mu;
 static HostPipe g_pipe[64];
+
+// Chunks for a host call: one below kHostPipeMinBytes of inputs, else 16 or
+// 8 as above, never more than the row groups.
+static int host_chunks(size_t in_bytes, size_t out_bytes, double kernel_s, int groups) {
+  if (in_bytes < kHostPipeMinBytes) return 1;
+  const bool kernel_longer = kernel_s > (double)(in_bytes + out_bytes) / kHostLinkBytes;
+  const int want = kernel_longer ? kHostChunks : kHostChunks / 2;
+  return groups < want ? groups : want;
+}
 
 // The device's streams and events, made on first use (call with g_pipe_mu held).
 static HostPipe* host_pipe(int dev) {
@@ -351,6 +371,22 @@ static HostPipe* host_pipe(int dev) {
   return &hp;
 }
 
+// The pipe's streams start after the work queued on `s` so far ...
+static bool pipe_fork(HostPipe* hp, cudaStream_t s) {
+  return cudaEventRecord(hp->start, s) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->up, hp->start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->comp[0], hp->start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->comp[1], hp->start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->down, hp->start, 0) == cudaSuccess;
+}
+
+// ... and `s` continues once every chunk's outputs are back (and so its
+// kernels and inputs are done).
+static bool pipe_join(HostPipe* hp, cudaStream_t s) {
+  return cudaEventRecord(hp->done, hp->down) == cudaSuccess &&
+         cudaStreamWaitEvent(s, hp->done, 0) == cudaSuccess;
+}
+
 static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const void* v_host,
                                    void* o_host, float* lse_host, void* q_dev, void* k_dev,
                                    void* v_dev, void* o_dev, float* lse_dev, int B, int H_q,
@@ -361,11 +397,8 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
   const int groups = B * H_kv;
   const double flops = 4.0 * B * H_q * (double)S_q * S_kv * D * (causal ? 0.5 : 1.0);
-  const bool kernel_longer =
-      flops / kHostKernelFlops > (double)(2 * q_bytes + 2 * kv_bytes) / kHostLinkBytes;
-  const int want = kernel_longer ? kHostChunks : kHostChunks / 2;
   const int chunks =
-      (q_bytes + 2 * kv_bytes >= kHostPipeMinBytes) ? (groups < want ? groups : want) : 1;
+      host_chunks(q_bytes + 2 * kv_bytes, q_bytes, flops / kHostKernelFlops, groups);
   if (chunks <= 1) {
     if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
@@ -384,13 +417,7 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   // queued under the lock, so concurrent callers' chunks do not interleave
   std::lock_guard<std::mutex> lk(g_pipe_mu);
   HostPipe* hp = host_pipe(dev);
-  if (!hp) return ATTN_ERR_CUDA;
-  if (cudaEventRecord(hp->start, s) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->up, hp->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->comp[0], hp->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->comp[1], hp->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->down, hp->start, 0) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
   const int r = H_q / H_kv;
   const size_t q_group = (size_t)r * S_q * D * 2;     // bytes of one group's Q (and O)
   const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (and V)
@@ -426,11 +453,88 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
                         hp->down) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
-  // every chunk's outputs are back (and so its kernel and inputs done)
-  if (cudaEventRecord(hp->done, hp->down) != cudaSuccess ||
-      cudaStreamWaitEvent(s, hp->done, 0) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const void* v_host,
+                                   const void* o_host, const float* lse_host,
+                                   const void* dout_host, void* dq_host, void* dk_host,
+                                   void* dv_host, void* q_dev, void* k_dev, void* v_dev,
+                                   void* o_dev, float* lse_dev, void* dout_dev, void* dq_dev,
+                                   void* dk_dev, void* dv_dev, void* workspace,
+                                   size_t workspace_bytes, int B, int H_q, int H_kv, int S_q,
+                                   int S_kv, int D, int causal, float scale, cudaStream_t s) {
+  const size_t q_bytes = (size_t)B * H_q * S_q * D * 2;
+  const size_t kv_bytes = (size_t)B * H_kv * S_kv * D * 2;
+  const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
+  const int groups = B * H_kv;
+  const double flops = 2.5 * 4.0 * B * H_q * (double)S_q * S_kv * D * (causal ? 0.5 : 1.0);
+  const int chunks = host_chunks(3 * q_bytes + 2 * kv_bytes + lse_bytes, q_bytes + 2 * kv_bytes,
+                                 flops / kHostBwdFlops, groups);
+  auto up = [](void* dst, const void* src, size_t n, cudaStream_t st) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  auto down = [](void* dst, const void* src, size_t n, cudaStream_t st) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  if (chunks <= 1) {
+    if (!up(q_dev, q_host, q_bytes, s) || !up(k_dev, k_host, kv_bytes, s) ||
+        !up(v_dev, v_host, kv_bytes, s) || !up(o_dev, o_host, q_bytes, s) ||
+        !up(lse_dev, lse_host, lse_bytes, s) || !up(dout_dev, dout_host, q_bytes, s))
+      return ATTN_ERR_CUDA;
+    attn_status_t st = bwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev, dq_dev, dk_dev,
+                                dv_dev, workspace, workspace_bytes, B, H_q, H_kv, S_q, S_kv, D,
+                                causal, scale, s);
+    if (st != ATTN_OK) return st;
+    if (!down(dq_host, dq_dev, q_bytes, s) || !down(dk_host, dk_dev, kv_bytes, s) ||
+        !down(dv_host, dv_dev, kv_bytes, s))
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = host_pipe(dev);
+  if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
+  const int r = H_q / H_kv;
+  const size_t q_group = (size_t)r * S_q * D * 2;     // bytes of one group's Q (O, dO, dQ)
+  const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (V, dK, dV)
+  const size_t lse_group = (size_t)r * S_q;           // floats of one group's LSE
+  // a chunk's workspace is its own slice: the per-group layout of a call on
+  // ng groups takes 2 * ng padded row vectors (a multiple of 1024 bytes)
+  const size_t ws_group = 2 * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
+  auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+  for (int c = 0; c < chunks; ++c) {
+    const int z0 = (int)((long long)groups * c / chunks);
+    const int z1 = (int)((long long)groups * (c + 1) / chunks);
+    const int ng = z1 - z0;
+    const size_t qo = z0 * q_group, qn = ng * q_group;
+    const size_t ko = z0 * kv_group, kn = ng * kv_group;
+    const size_t lo = z0 * lse_group, ln = ng * lse_group;
+    if (!up(db(q_dev, qo), hb(q_host, qo), qn, hp->up) ||
+        !up(db(k_dev, ko), hb(k_host, ko), kn, hp->up) ||
+        !up(db(v_dev, ko), hb(v_host, ko), kn, hp->up) ||
+        !up(db(o_dev, qo), hb(o_host, qo), qn, hp->up) ||
+        !up(lse_dev + lo, lse_host + lo, ln * sizeof(float), hp->up) ||
+        !up(db(dout_dev, qo), hb(dout_host, qo), qn, hp->up) ||
+        cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    cudaStream_t cs = hp->comp[c & 1];
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_status_t st = bwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo),
+                                lse_dev + lo, db(dout_dev, qo), db(dq_dev, qo), db(dk_dev, ko),
+                                db(dv_dev, ko), db(workspace, z0 * ws_group), ng * ws_group, 1,
+                                ng * r, ng, S_q, S_kv, D, causal, scale, cs);
+    if (st != ATTN_OK) return st;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
+        !down(db(dq_host, qo), db(dq_dev, qo), qn, hp->down) ||
+        !down(db(dk_host, ko), db(dk_dev, ko), kn, hp->down) ||
+        !down(db(dv_host, ko), db(dv_dev, ko), kn, hp->down))
+      return ATTN_ERR_CUDA;
+  }
+  return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const float* dt,
@@ -559,6 +663,26 @@ attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* 
   return attnpipe::fwd_host_impl(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
                                  o_dev, lse_dev, B, H_q, H_kv, S_q, S_kv, D, causal, scale,
                                  static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_bwd_host(const void* q_host, const void* k_host, const void* v_host,
+                            const void* o_host, const float* lse_host, const void* dout_host,
+                            void* dq_host, void* dk_host, void* dv_host, void* q_dev, void* k_dev,
+                            void* v_dev, void* o_dev, float* lse_dev, void* dout_dev,
+                            void* dq_dev, void* dk_dev, void* dv_dev, void* workspace,
+                            size_t workspace_bytes, int B, int H_q, int H_kv, int S_q, int S_kv,
+                            int D, int causal, float scale, attn_stream_t stream) {
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host || !dout_host || !dq_host ||
+      !dk_host || !dv_host)
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = bwd_validate(q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev, dq_dev, dk_dev,
+                                  dv_dev, workspace, workspace_bytes, B, H_q, H_kv, S_q, S_kv, D,
+                                  causal, scale);
+  if (st != ATTN_OK) return st;
+  return attnpipe::bwd_host_impl(q_host, k_host, v_host, o_host, lse_host, dout_host, dq_host,
+                                 dk_host, dv_host, q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev,
+                                 dq_dev, dk_dev, dv_dev, workspace, workspace_bytes, B, H_q, H_kv,
+                                 S_q, S_kv, D, causal, scale, static_cast<cudaStream_t>(stream));
 }
 
 const char* attn_status_string(attn_status_t status) {

@@ -552,21 +552,16 @@ def run_bwd(args, w):
     if ap.device_status(reset=True) != 0:
         raise RuntimeError("a kernel wait timed out in the timed region")
 
-    # end to end: pinned host inputs in, gradients back, copies timed
+    # end to end through the host-buffer backward (attn_bwd_host): pinned
+    # host inputs in, gradients back, copies inside the timed region
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    host_in = [t.pin_memory() for t in (q_cpu, k_cpu, v_cpu, do_cpu)]
-    o_h, lse_h = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    host_in = [t.pin_memory() for t in (q_cpu, k_cpu, v_cpu)] + \
+        [o.cpu().pin_memory(), lse.cpu().pin_memory(), do_cpu.pin_memory()]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
-    dev_in = [q, k, v, dout]
 
     def e2e_step():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        o.copy_(o_h, non_blocking=True)
-        lse.copy_(lse_h, non_blocking=True)
-        step()
-        for h_, d_ in zip(host_out, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
+        ap.attn_bwd_host(*host_in, *host_out, q, k, v, o, lse, dout, dq, dk, dv, w.causal,
+                         w.scale, ws, stream=stream)
 
     for _ in range(2):
         e2e_step()

@@ -205,6 +205,35 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
 /* Workspace bytes attn_bwd needs (0 if the arguments are invalid). */
 size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
 
+/*
+ * attn_bwd with host inputs and outputs, pipelined as attn_fwd_host is:
+ * copies q, k, v, o, lse and dout from host memory into the caller's device
+ * buffers (the *_dev arguments, same shapes as attn_bwd's), runs the backward
+ * and copies dq, dk and dv back to host memory, ordered after the work
+ * already queued on `stream` and before the work queued on it afterwards.
+ * Inputs of 32 MiB or more are split into 8 or 16 chunks of consecutive
+ * (batch, kv-head) row groups; a chunk's inputs go up on one internal
+ * stream, its three kernels run on one of two internal compute streams with
+ * its own slice of `workspace`, and its gradients come back on another, so
+ * each chunk's copies overlap the other chunks' kernels.  Every gradient
+ * element is computed by the same tiles in the same order as in one
+ * attn_bwd call, so the results are bit-identical to it.  Host buffers
+ * should be page-locked for the copies to be asynchronous.  Returns once
+ * everything is queued; the host gradients are valid once `stream` has
+ * been synchronised.  Argument rules and errors as attn_bwd for the device
+ * buffers and the workspace (the same size, attn_bwd_workspace_bytes);
+ * ATTN_ERR_INVALID_ARG for a null host pointer.  Nothing is queued when a
+ * check fails.
+ */
+attn_status_t attn_bwd_host(const void *q_host, const void *k_host, const void *v_host,
+                            const void *o_host, const float *lse_host, const void *dout_host,
+                            void *dq_host, void *dk_host, void *dv_host, void *q_dev,
+                            void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
+                            void *dout_dev, void *dq_dev, void *dk_dev, void *dv_dev,
+                            void *workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
+                            int S_q, int S_kv, int D, int causal, float scale,
+                            attn_stream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char *attn_status_string(attn_status_t status);
 

@@ -84,6 +84,36 @@ def test_host_entry_rejects_null_host_buffers(lib):
         assert lib.attn_fwd_host(*bad) == 1
 
 
+def test_bwd_host_entry_rejects_before_queuing(lib):
+    """attn_bwd_host: a null host buffer, then the device-side rules of
+    attn_bwd (fake, never-dereferenced device addresses), all on the host."""
+    dims = [1, 4, 2, 128, 128, 128, 0, ctypes.c_float(0.1), None]
+    ws_bytes = lib.attn_bwd_workspace_bytes(1, 4, 2, 128)
+    assert ws_bytes > 0
+
+    def call(host=None, dev=None, ws=A, nbytes=ws_bytes, d=dims):
+        host = host or [A] * 9
+        dev = dev or [A] * 9
+        return lib.attn_bwd_host(*host, *dev, ws, nbytes, *d)
+
+    for i in range(9):
+        host = [A] * 9
+        host[i] = None
+        assert call(host=host) == 1                   # null host buffer
+    for i in range(9):
+        dev = [A] * 9
+        dev[i] = None
+        assert call(dev=dev) == 1                     # null device buffer
+    assert call(ws=None) == 1                         # no workspace
+    assert call(nbytes=ws_bytes - 1) == 1             # too small a workspace
+    assert call(ws=A + 16) == 3                       # workspace not 256-byte aligned
+    dev = [A] * 9
+    dev[5] = A + 8
+    assert call(dev=dev) == 3                         # misaligned dout
+    assert call(d=[1, 4, 2, 128, 128, 96, 0, ctypes.c_float(0.1), None]) == 2   # D = 96
+    assert call(d=[1, 3, 2, 128, 128, 128, 0, ctypes.c_float(0.1), None]) == 1  # H_q % H_kv
+
+
 def test_selftest_entry_validation(lib):
     assert lib.attn_selftest_qk(None, A, A, 128, None) == 1
     assert lib.attn_selftest_qk(A, A, A, 96, None) == 2

@@ -155,3 +155,40 @@ def test_bwd_deterministic_and_rejects_bad_workspace():
     with pytest.raises(ap.AttnError):
         ap.attn_bwd(q, k, v, o, lse, dout, True, scale, workspace=small)
     assert ap.device_status(reset=True) == 0
+
+
+HOST_BWD_SHAPES = [
+    # B, H_q, H_kv, S, D, causal: the first two are cut into chunks (inputs >= 32 MiB)
+    (1, 16, 16, 8192, 128, False),
+    (4, 8, 2, 4096, 64, True),
+    (1, 2, 2, 256, 128, True),      # one chunk
+]
+
+
+@pytest.mark.parametrize("shape", HOST_BWD_SHAPES, ids=[str(s) for s in HOST_BWD_SHAPES])
+def test_bwd_host_entry_matches_device_entry(shape):
+    """attn_bwd_host (pinned host buffers, chunked copies and kernels on its
+    own streams) gives the same bits as attn_bwd on device buffers, called
+    twice in a row on a side stream."""
+    B, Hq, Hkv, S, D, causal = shape
+    q, k, v = make_qkv(B, Hq, Hkv, S, S, D, seed=21)
+    dout = make_dout(q.shape, 22)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, dout))
+    o, lse = ap.attn_fwd(qd, kd, vd, causal, scale)
+    ref = ap.attn_bwd(qd, kd, vd, o, lse, dod, causal, scale)
+    torch.cuda.synchronize()
+    host_in = [t.pin_memory() for t in (q, k, v, o.cpu(), lse.cpu(), dout)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in ref]
+    dev_in = [torch.empty_like(t) for t in (qd, kd, vd, o, lse, dod)]
+    dev_out = [torch.empty_like(t) for t in ref]
+    ws = torch.empty(ap.bwd_workspace_bytes(B, Hq, Hkv, S), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    for _ in range(2):
+        for t in host_out:
+            t.fill_(0)
+        ap.attn_bwd_host(*host_in, *host_out, *dev_in, *dev_out, causal, scale, ws, stream=side)
+        side.synchronize()
+        assert ap.device_status(reset=True) == 0
+        for name, got, want in zip(("dq", "dk", "dv"), host_out, ref):
+            assert torch.equal(got, want.cpu()), name
