@@ -20,7 +20,7 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = ["attn_fwd", "attn_fwd_out", "attn_fwd_host", "attn_fwd_trace", "attn_fwd_splitkv",
            "splitkv_default_splits", "attn_bwd", "attn_bwd_host", "bwd_workspace_bytes",
-           "chunk_scan", "selftest_qk", "selftest_pv", "device_status", "status_string",
+           "chunk_scan", "chunk_scan_host", "selftest_qk", "selftest_pv", "device_status", "status_string",
            "lib_path", "build", "AttnError", "STATUS"]
 
 STATUS = {
@@ -38,7 +38,7 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
            "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes",
-           "attn_bwd_host", "chunk_scan_fwd"]
+           "attn_bwd_host", "chunk_scan_fwd", "chunk_scan_fwd_host"]
 
 
 class AttnError(RuntimeError):
@@ -103,6 +103,8 @@ def _load():
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.chunk_scan_fwd.argtypes = [vp] * 5 + [ci] * 6 + [vp]
     lib.chunk_scan_fwd.restype = ci
+    lib.chunk_scan_fwd_host.argtypes = [vp] * 10 + [ci] * 6 + [vp]
+    lib.chunk_scan_fwd_host.restype = ci
     _lib = lib
     return lib
 
@@ -306,6 +308,19 @@ def chunk_scan(cb, dA_cs, dt, x, out=None, stream=None):
                                   out.data_ptr(), B, L, H, G, P, Q, _stream_handle(stream)),
            "chunk_scan_fwd")
     return out
+
+
+def chunk_scan_host(cb_host, dA_cs_host, dt_host, x_host, out_host, cb_dev, dA_cs_dev, dt_dev,
+                    x_dev, out_dev, stream=None) -> None:
+    """Host-buffer chunk scan: copies cb, dA_cs, dt, x (host, ideally pinned)
+    into the device buffers, runs chunk_scan_fwd, copies out back, all queued
+    on ``stream``."""
+    B, L, H, P = x_host.shape
+    G, Q = cb_host.shape[2], cb_host.shape[3]
+    ts = (cb_host, dA_cs_host, dt_host, x_host, out_host, cb_dev, dA_cs_dev, dt_dev, x_dev,
+          out_dev)
+    _check(_load().chunk_scan_fwd_host(*(t.data_ptr() for t in ts), B, L, H, G, P, Q,
+                                       _stream_handle(stream)), "chunk_scan_fwd_host")
 
 
 def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,

@@ -537,9 +537,10 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
   return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const float* dt,
-                                     const void* x, void* out, int B, int L, int H, int G, int P,
-                                     int Q, attn_stream_t stream) {
+// Every check of chunk_scan_fwd's arguments, the device's included.
+static attn_status_t chunk_scan_validate(const void* cb, const void* dA_cs, const void* dt,
+                                         const void* x, const void* out, int B, int L, int H,
+                                         int G, int P, int Q) {
   if (!cb || !dA_cs || !dt || !x || !out) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || P <= 0 || Q <= 0) return ATTN_ERR_INVALID_ARG;
   if (H % G != 0 || L % Q != 0) return ATTN_ERR_INVALID_ARG;
@@ -549,7 +550,13 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
     return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(cb) || !aligned16(dA_cs) || !aligned16(dt) || !aligned16(x) || !aligned16(out))
     return ATTN_ERR_MISALIGNED;
-  attn_status_t st = check_device();
+  return check_device();
+}
+
+static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const float* dt,
+                                     const void* x, void* out, int B, int L, int H, int G, int P,
+                                     int Q, attn_stream_t stream) {
+  attn_status_t st = chunk_scan_validate(cb, dA_cs, dt, x, out, B, L, H, G, P, Q);
   if (st != ATTN_OK) return st;
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return ATTN_ERR_CUDA;
@@ -598,6 +605,72 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
   return ATTN_OK;
 }
 
+// chunk_scan_fwd_host: the batch is cut into chunks of consecutive batch
+// entries (a contiguous slice of every tensor and a problem of its own),
+// pipelined on the same streams as attn_fwd_host.  The kernel is far shorter
+// than the copies here, so the gain is the uploads of one chunk overlapping
+// the downloads of another (the host link carries both directions at once).
+static attn_status_t chunk_scan_host_impl(const float* cb_host, const float* dA_host,
+                                          const float* dt_host, const void* x_host,
+                                          void* out_host, float* cb_dev, float* dA_dev,
+                                          float* dt_dev, void* x_dev, void* out_dev, int B, int L,
+                                          int H, int G, int P, int Q, cudaStream_t s) {
+  const size_t nch = (size_t)(L / Q);
+  const size_t cb_b = nch * G * Q * Q;     // floats of one batch entry's cb
+  const size_t vec_b = (size_t)H * nch * Q;  // floats of its dA_cs (and of its dt)
+  const size_t x_b = (size_t)L * H * P * 2;  // bytes of its x (and of its out)
+  const size_t in_bytes = (size_t)B * (cb_b * 4 + 2 * vec_b * 4 + x_b);
+  const size_t out_bytes = (size_t)B * x_b;
+  // the kernel moves its bytes at about 4 TB/s: always shorter than the copies
+  const int chunks = host_chunks(in_bytes, out_bytes, (double)(in_bytes + out_bytes) / 4.0e12, B);
+  auto up = [](void* dst, const void* src, size_t n, cudaStream_t st) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  auto down = [](void* dst, const void* src, size_t n, cudaStream_t st) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  if (chunks <= 1) {
+    if (!up(cb_dev, cb_host, B * cb_b * 4, s) || !up(dA_dev, dA_host, B * vec_b * 4, s) ||
+        !up(dt_dev, dt_host, B * vec_b * 4, s) || !up(x_dev, x_host, B * x_b, s))
+      return ATTN_ERR_CUDA;
+    attn_status_t st = chunk_scan_impl(cb_dev, dA_dev, dt_dev, x_dev, out_dev, B, L, H, G, P, Q, s);
+    if (st != ATTN_OK) return st;
+    return down(out_host, out_dev, out_bytes, s) ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = host_pipe(dev);
+  if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
+  auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+  for (int c = 0; c < chunks; ++c) {
+    const int b0 = (int)((long long)B * c / chunks);
+    const int b1 = (int)((long long)B * (c + 1) / chunks);
+    const int nb = b1 - b0;
+    const size_t co = b0 * cb_b * 4, cn = nb * cb_b * 4;
+    const size_t vo = b0 * vec_b * 4, vn = nb * vec_b * 4;
+    const size_t xo = b0 * x_b, xn = nb * x_b;
+    if (!up(db(cb_dev, co), hb(cb_host, co), cn, hp->up) ||
+        !up(db(dA_dev, vo), hb(dA_host, vo), vn, hp->up) ||
+        !up(db(dt_dev, vo), hb(dt_host, vo), vn, hp->up) ||
+        !up(db(x_dev, xo), hb(x_host, xo), xn, hp->up) ||
+        cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    cudaStream_t cs = hp->comp[c & 1];
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_status_t st = chunk_scan_impl(cb_dev + b0 * cb_b, dA_dev + b0 * vec_b,
+                                       dt_dev + b0 * vec_b, db(x_dev, xo), db(out_dev, xo), nb,
+                                       L, H, G, P, Q, cs);
+    if (st != ATTN_OK) return st;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
+        !down(db(out_host, xo), db(out_dev, xo), xn, hp->down))
+      return ATTN_ERR_CUDA;
+  }
+  return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace attnpipe
 
 extern "C" {
@@ -606,6 +679,20 @@ attn_status_t chunk_scan_fwd(const float* cb, const float* dA_cs, const float* d
                              void* out, int B, int L, int H, int G, int P, int Q,
                              attn_stream_t stream) {
   return chunk_scan_impl(cb, dA_cs, dt, x, out, B, L, H, G, P, Q, stream);
+}
+
+attn_status_t chunk_scan_fwd_host(const float* cb_host, const float* dA_cs_host,
+                                  const float* dt_host, const void* x_host, void* out_host,
+                                  float* cb_dev, float* dA_cs_dev, float* dt_dev, void* x_dev,
+                                  void* out_dev, int B, int L, int H, int G, int P, int Q,
+                                  attn_stream_t stream) {
+  if (!cb_host || !dA_cs_host || !dt_host || !x_host || !out_host) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = chunk_scan_validate(cb_dev, dA_cs_dev, dt_dev, x_dev, out_dev, B, L, H, G,
+                                         P, Q);
+  if (st != ATTN_OK) return st;
+  return attnpipe::chunk_scan_host_impl(cb_host, dA_cs_host, dt_host, x_host, out_host, cb_dev,
+                                        dA_cs_dev, dt_dev, x_dev, out_dev, B, L, H, G, P, Q,
+                                        static_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -42,6 +42,29 @@ attn_status_t chunk_scan_fwd(const float *cb, const float *dA_cs, const float *d
                              void *out, int B, int L, int H, int G, int P, int Q,
                              attn_stream_t stream);
 
+/*
+ * chunk_scan_fwd with host inputs and output: copies cb, dA_cs, dt and x from
+ * host memory into the caller's device buffers (the *_dev arguments, same
+ * shapes as chunk_scan_fwd's), runs the scan and copies out back to host
+ * memory, ordered after the work already queued on `stream` and before the
+ * work queued on it afterwards.  Inputs of 32 MiB or more are split into 8
+ * or 16 chunks of consecutive batch entries, pipelined on the internal
+ * streams attn_fwd_host uses: one chunk's inputs go up while another's
+ * output comes back, so the host link carries both directions at once.
+ * Every output element is computed the same way as in one chunk_scan_fwd
+ * call, so the results are bit-identical to it.  Host buffers should be
+ * page-locked for the copies to be asynchronous.  Returns once everything
+ * is queued; the host output is valid once `stream` has been synchronised.
+ * Argument rules and errors as chunk_scan_fwd for the device buffers;
+ * ATTN_ERR_INVALID_ARG for a null host pointer.  Nothing is queued when a
+ * check fails.
+ */
+attn_status_t chunk_scan_fwd_host(const float *cb_host, const float *dA_cs_host,
+                                  const float *dt_host, const void *x_host, void *out_host,
+                                  float *cb_dev, float *dA_cs_dev, float *dt_dev, void *x_dev,
+                                  void *out_dev, int B, int L, int H, int G, int P, int Q,
+                                  attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

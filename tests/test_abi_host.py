@@ -177,3 +177,18 @@ def test_chunk_scan_rejects_bad_arguments_on_host(lib):
     assert call(P=128) == 2                     # head width other than 64
     assert call(Q=64, L=256) == 2               # chunk other than 128 or 256
     assert call(x=A + 8) == 3                   # misaligned
+
+
+def test_chunk_scan_host_entry_rejects_before_queuing(lib):
+    """chunk_scan_fwd_host: null host buffers, then chunk_scan_fwd's rules on
+    the device buffers (fake pointers), all on the host."""
+    f = lib.chunk_scan_fwd_host
+    dims = [1, 256, 4, 1, 64, 256, None]
+    for i in range(5):
+        host = [A] * 5
+        host[i] = None
+        assert f(*host, *([A] * 5), *dims) == 1
+    assert f(*([A] * 5), A, A, None, A, A, *dims) == 1                  # null device buffer
+    assert f(*([A] * 5), *([A] * 5), 1, 300, 4, 1, 64, 256, None) == 1  # L not a multiple of Q
+    assert f(*([A] * 5), *([A] * 5), 1, 256, 4, 1, 128, 256, None) == 2  # P = 128
+    assert f(*([A] * 5), A, A, A, A + 8, A, *dims) == 3                 # misaligned x

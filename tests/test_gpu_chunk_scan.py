@@ -148,3 +148,27 @@ def test_chunk_scan_headline_workload_sampled_rows():
     del cb, dA_cs, dt, x, out
     ref = oracle.chunk_scan_default().rows(*cpu, rows)
     assert_close("rows", got, ref)
+
+
+@pytest.mark.parametrize("shape", [(4, 8192, 64, 64, 1, 256), (1, 512, 4, 64, 1, 256)],
+                         ids=["b4_s8192_chunked", "b1_s512_one_chunk"])
+def test_chunk_scan_host_entry_matches_device_entry(shape):
+    """chunk_scan_fwd_host (pinned host buffers; the first shape is cut into
+    chunks of batch entries on the entry's own streams) gives the same bits
+    as chunk_scan_fwd, called twice in a row on a side stream."""
+    B, L, H, P, G, Q = shape
+    cb, dA_cs, dt, x = make_chunk_scan(B, L, H, P, G, Q, seed=51)
+    dev = [t.cuda() for t in (cb, dA_cs, dt, x)]
+    ref = ap.chunk_scan(*dev)
+    torch.cuda.synchronize()
+    host_in = [t.pin_memory() for t in (cb, dA_cs, dt, x)]
+    host_out = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    dev_in = [torch.empty_like(t) for t in dev]
+    dev_out = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    for _ in range(2):
+        host_out.fill_(0)
+        ap.chunk_scan_host(*host_in, host_out, *dev_in, dev_out, stream=side)
+        side.synchronize()
+        assert ap.device_status(reset=True) == 0
+        assert torch.equal(host_out, ref.cpu())
