@@ -28,8 +28,10 @@
 //               bulk copies, ahead as far as its ring allows) and computes the per-key
 //               factors of the decay and the mask of portions where dA_cs
 //               rises (see below);
-//   warp 21     TMA producer: the tile's cb once (3-D map, 32-key boxes),
-//               then per head its x slices (4-D map over [B, L, H, P])
+//   warp 21     TMA producer: the tile's cb once (3-D map, 32-key boxes;
+//               one barrier per 64-key slice, issued along with the first
+//               head's x slices), then per head its x slices (4-D map over
+//               [B, L, H, P])
 //               through a ring of eight slots (two slices per full/free
 //               barrier pair), with the head two ahead prefetched into L2.
 // Every wait is bounded; a timeout raises a CTA-wide abort flag and the
@@ -79,10 +81,12 @@ constexpr int kCsOffVec = kCsOffStage + kCsStageBytes;               // [ring]
 constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [vector ring][Q] key factors
 constexpr int kCsOffMask = kCsOffKf + kCsRingV * kCsMaxQ * 4;        // [vector ring] rise masks
 constexpr int kCsOffBar = kCsOffMask + kCsRingV * 4;
-// cb_full, pair_full[R / 2], pair_free[R / 2], xp_full[RX / 2],
+// cb_full[Q / 64], pair_full[R / 2], pair_free[R / 2], xp_full[RX / 2],
 // xp_free[RX / 2], v_full[RV], v_free[RV], kf_full[RV], acc_full[ACC],
 // acc_free[ACC], drain
-constexpr int kCsNumBars = 1 + 2 * kCsPairs + 2 * kCsPairsX + 3 * kCsRingV + 2 * kCsAcc + 1;
+constexpr int kCsCbSlices = kCsMaxQ / kCsSlice;  // cb arrives slice by slice
+constexpr int kCsNumBars =
+    kCsCbSlices + 2 * kCsPairs + 2 * kCsPairsX + 3 * kCsRingV + 2 * kCsAcc + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
 static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
@@ -116,14 +120,14 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   float* sKfAll = reinterpret_cast<float*>(smem + kCsOffKf);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + kCsOffMask);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCsOffBar);
-  uint64_t* cb_full = bars;
+  uint64_t* cb_full = bars;  // [slice]: the cb boxes of keys 64s .. 64s + 63 landed
   // Slices gs and gs + 1 (gs even, the same head: a head has an even
   // number of slices) share the barriers of pair gs / 2: its A slices in
   // slot pair (gs / 2) % kCsPairs (pair_full: 128 arrivals of each slice's
   // warpgroup), its x slices in x slot pair (gs / 2) % kCsPairsX (xp_full:
   // one arrival with its bytes per slice); the matching _free barriers say
   // the products that read them are done.
-  uint64_t* pair_full = bars + 1;
+  uint64_t* pair_full = bars + kCsCbSlices;
   uint64_t* pair_free = pair_full + kCsPairs;
   uint64_t* xp_full = pair_free + kCsPairs;
   uint64_t* xp_free = xp_full + kCsPairsX;
@@ -155,11 +159,10 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   const int m0 = mt * kCsRows;                 // first row of the tile within the chunk
   const int n_slices = (m0 + kCsRows) / kCsSlice;  // keys 0 .. m0 + 127 are visible to some row
   const int log_ns = (n_slices == 4) ? 2 : 1;      // n_slices is 2 or 4 (Q = 128 or 256)
-  const int n_boxes = 2 * n_slices;
   const int total = p.HB * n_slices;           // slices of the CTA
 
   if (threadIdx.x == 0) {
-    mbar_init(cb_full, 1);
+    for (int i = 0; i < kCsCbSlices; ++i) mbar_init(&cb_full[i], 1);
     for (int i = 0; i < kCsPairs; ++i) {
       mbar_init(&pair_full[i], 2 * 128);
       mbar_init(&pair_free[i], 1);
@@ -200,13 +203,18 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float l2e = 1.4426950408889634f;
     const uint64_t nl2e2 = f2_pack(-l2e, -l2e);
-    bool ok = cs_warp_wait(cb_full, 0, sAbort, budget);
+    bool ok = true;
+    uint32_t cb_seen = 0;                      // cb slices this warp has seen land
     for (int gs = w; gs < total && ok; gs += kCsScaleGroups) {
       const int j = gs >> log_ns;              // head of the block
       const int s = gs & (n_slices - 1);       // slice of the head
       const int vs = j % kCsRingV;
       const int slot = gs % kCsRing;
       const int pr = gs >> 1;                  // pair
+      if (!((cb_seen >> s) & 1u)) {
+        ok = cs_warp_wait(&cb_full[s], 0, sAbort, budget);
+        cb_seen |= 1u << s;
+      }
       ok = ok && cs_warp_wait(&kf_full[vs], (j / kCsRingV) & 1, sAbort, budget);
       ok = ok && (pr < kCsPairs || cs_warp_wait(&pair_free[pr % kCsPairs],
                                                 ((pr / kCsPairs) - 1) & 1, sAbort, budget));
@@ -463,12 +471,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     const uint64_t pol_cb = l2_policy_evict_last();
     bool ok = true;
     int gs = 0;
-    if (leader) {
-      mbar_arrive_expect_tx(cb_full, n_boxes * kCsBoxBytes);
-      const int zc = (b * p.nchunks + c) * p.G + g;
-      for (int i = 0; i < n_boxes; ++i)
-        tma_load_3d(sCb + i * kCsBoxBytes, &p.tm_cb, cb_full, i * kCsBox, m0, zc, pol_cb);
-    }
+    int cb_issued = 0;                         // cb slices whose loads were issued
+    const int zc = (b * p.nchunks + c) * p.G + g;
     for (int j = 0; j < p.HB && ok; ++j) {
       const int h = h0 + j;
       if (leader) {
@@ -490,6 +494,18 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
           ok = false;
           break;
         }
+        if (j == 0) {
+          // the tile's cb for slice s (two 32-key boxes) just ahead of the
+          // first head's x slice s: the first slices can start before the
+          // whole cb has arrived
+          if (leader) {
+            mbar_arrive_expect_tx(&cb_full[s], 2 * kCsBoxBytes);
+            for (int i = 2 * s; i < 2 * s + 2; ++i)
+              tma_load_3d(sCb + i * kCsBoxBytes, &p.tm_cb, &cb_full[s], i * kCsBox, m0, zc,
+                          pol_cb);
+          }
+          ++cb_issued;
+        }
         if (leader) {
           mbar_arrive_expect_tx(&xp_full[px], kCsSliceBytesX);
           tma_load_4d(sX + (2 * px + (gs & 1)) * kCsSliceBytesX, &p.tm_x, &xp_full[px], 0, h,
@@ -500,7 +516,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     // every copy issued lands before the CTA exits (the producer stops only
     // before the first slice of a pair, so every x pair it started is whole)
     if (leader) {
-      cs_drain_wait(cb_full, 0, budget);
+      for (int i = 0; i < cb_issued; ++i) cs_drain_wait(&cb_full[i], 0, budget);
       const int np = gs / 2;                   // pairs with both x slices issued
       for (int pr = np > kCsPairsX ? np - kCsPairsX : 0; pr < np; ++pr)
         cs_drain_wait(&xp_full[pr % kCsPairsX], (pr / kCsPairsX) & 1, budget);
