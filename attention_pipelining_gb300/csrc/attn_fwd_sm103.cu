@@ -41,6 +41,18 @@
 //   fin[2][t]  the final row statistics, double-buffered by tile parity so a
 //              one-block tile cannot overwrite them before they are read.
 //
+// Split tail (the kTail instantiation, launched as clusters of two CTAs):
+// when the grid's last round would leave more than half of the CTAs idle,
+// each of its tiles is split across a CTA pair, half of the KV blocks each.
+// Both halves run as ordinary tiles; at the end the second CTA writes its
+// normalised fp32 partial O and base-2 log-sum-exp into its own idle K/V
+// ring and Q buffer and arrives on the first CTA's xfer_full (remote
+// mbarrier arrivals, release at cluster scope); the first reads them through
+// distributed shared memory, merges them with its own half by the two
+// log-sum-exps, writes O and LSE, and arrives on the second's xfer_free.
+// Cluster barriers at start (barriers initialised) and exit (no CTA leaves
+// while its partner may still touch its shared memory) bracket the kernel.
+//
 // Every wait is bounded (see ptx.cuh); a timeout raises a CTA-wide abort
 // flag, every role unwinds to the teardown, and the device status word
 // records ATTN_ERR_TIMEOUT.  No trap, no assert.
@@ -63,6 +75,10 @@ constexpr int kThreads = 512;
 constexpr int kBlockM = 128;  // rows per query sub-tile
 constexpr int kBlockN = 128;  // keys per KV block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+// Split tail only for tiles of at least this many KV blocks: half a tile must
+// save more than the merge and the cluster start cost (measured on GB300:
+// +5 % at 128 blocks per tile, none at 16, a loss for short causal tiles)
+constexpr int kSplitTailMinBlocks = 32;
 constexpr uint32_t kFull = 0xffffffffu;
 // Register split across the four warpgroups (setmaxnreg): softmax x2,
 // correction, load/MMA.  The kernel launches with 128 registers per thread
@@ -84,8 +100,8 @@ struct Cfg {
   static constexpr int kOffKV = kOffQ + 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // kv_full[P], kv_empty[P], q_full[2], s_full[2], p_full[2], stats[2],
-  // pv_done[2], drain[1], fin[2][2], q_free[2]
-  static constexpr int kNumBars = 2 * kPairs + 17;
+  // pv_done[2], drain[1], fin[2][2], q_free[2], xfer_full, xfer_free
+  static constexpr int kNumBars = 2 * kPairs + 19;
   static constexpr int kOffScale = kOffBar + kNumBars * 8;      // float [2][128]: alpha per row
   static constexpr int kOffRowSum = kOffScale + 2 * 128 * 4;    // float [2][2][128]: fp32 sum of p
   static constexpr int kOffRowSumP = kOffRowSum + 4 * 128 * 4;  // float [2][2][128]: sum of bf16(p)
@@ -98,12 +114,23 @@ struct Cfg {
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // a split tail tile's partial result, [sub-tile][row][D] fp32, fits in
+  // the K/V ring, and its log-sum-exps [sub-tile][row] in the Q buffer
+  static_assert(2 * 128 * D * 4 <= kSlots * kTileBytes && 2 * 128 * 4 <= 2 * kTileBytes,
+                "split-tail partial does not fit");
 };
 
 // Warp-uniform bounded wait: every lane waits, the warp agrees on the result.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t budget) {
   const bool ok = mbar_wait(bar, parity, abort_flag, budget);
+  return __all_sync(kFull, ok);
+}
+
+// The same at cluster scope: for barriers the partner CTA arrives on.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, uint64_t budget) {
+  const bool ok = mbar_wait_cluster(bar, parity, abort_flag, budget);
   return __all_sync(kFull, ok);
 }
 
@@ -125,19 +152,30 @@ struct Tile {
   int jb;         // first KV block the tile visits
   int n_blocks;   // KV blocks it visits (<= 0: a split with no visible key)
   bool has_sub1;  // rows m0 + 128 .. m0 + 255 exist in the row group
+  int pair;       // -1: a whole tile; 0 / 1: the first / second KV half of a
+                  // split tail tile, run by cluster ranks 0 / 1
 };
 
 // Index of the k-th tile of this CTA, or -1 when it has no k-th tile: round
 // k covers list entries [k G, (k + 1) G), taken left to right in even rounds
-// and right to left in odd ones.
-__device__ __forceinline__ int tile_of(const AttnParams& p, int k) {
+// and right to left in odd ones.  With a split tail, the last round's
+// tail_pairs tiles go one per CTA pair (c / 2), half c % 2 each (`pair`).
+template <bool kTail>
+__device__ __forceinline__ int tile_of(const AttnParams& p, int k, int& pair) {
   const long long G = gridDim.x;
   const long long c = blockIdx.x;
-  const long long idx = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+  const long long base = (long long)k * G;
+  pair = -1;
+  if (kTail && base >= p.tail_base) {
+    if (base != p.tail_base || (c >> 1) >= p.tail_pairs) return -1;
+    pair = (int)(c & 1);
+    return (int)(p.tail_base + (c >> 1));
+  }
+  const long long idx = base + ((k & 1) ? (G - 1 - c) : c);
   return idx < (long long)p.num_tiles ? (int)idx : -1;
 }
 
-__device__ __forceinline__ Tile decode_tile(const AttnParams& p, int ti) {
+__device__ __forceinline__ Tile decode_tile(const AttnParams& p, int ti, int pair) {
   const int S = p.kv_splits;
   int m, zkv, split;
   if (p.causal) {
@@ -181,12 +219,25 @@ __device__ __forceinline__ Tile decode_tile(const AttnParams& p, int ti) {
   // (short row groups, e.g. one decoding token per head, or a ragged last
   // tile) every role skips it and the tile costs half
   t.has_sub1 = (t.m0 + kBlockM) < R;
+  // a split tail tile: the first ceil(n / 2) blocks, or the rest
+  t.pair = pair;
+  if (pair >= 0) {
+    const int n0 = (t.n_blocks + 1) >> 1;
+    if (pair == 0) {
+      t.n_blocks = n0;
+    } else {
+      t.jb += n0;
+      t.n_blocks -= n0;
+    }
+  }
   return t;
 }
 
 }  // namespace
 
-template <int D, bool kTrace>
+// kTail: the instantiation with the split tail (launched only when the tail
+// is split; the other one carries none of its code)
+template <int D, bool kTrace, bool kTail>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -204,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* drain = q_full + 10;
   uint64_t* fin = q_full + 11;     // [buffer][sub-tile]
   uint64_t* q_free = q_full + 15;
+  // split tail: the partner's partial result is in its shared memory
+  // (128 remote arrivals), and it has been read (128 remote arrivals)
+  uint64_t* xfer_full = q_full + 17;
+  uint64_t* xfer_free = q_full + 18;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
   float* sRowSum = reinterpret_cast<float*>(smem + C::kOffRowSum);
   float* sRowSumP = reinterpret_cast<float*>(smem + C::kOffRowSumP);
@@ -254,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(xfer_full, kBlockM);
+    mbar_init(xfer_free, kBlockM);
     *sAbort = 0;
     fence_mbar_init();
   }
@@ -269,6 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // the partner CTA's barriers are initialised before any remote arrival
+  if (kTail) cluster_sync_all();
   const uint32_t tmem = *sTmemBase;
   const int wg = warp >> 2;
   const int R = p.rows_per_group;
@@ -285,9 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint32_t ntl = 0;   // tiles with sub-tile t so far: row-stat buffer, fin phase
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int ti = tile_of(p, k);
+      int pr = -1;
+      const int ti = tile_of<kTail>(p, k, pr);
       if (ti < 0) break;
-      const Tile tl = decode_tile(p, ti);
+      const Tile tl = decode_tile(p, ti, pr);
       // (warpgroup 1 has nothing to do when the tile has no sub-tile 1)
       if (tl.n_blocks <= 0 || (t == 1 && !tl.has_sub1)) continue;
       const bool tr = trace_cta && k == 0 && lane == 0 && (warp & 3) == 0;
@@ -425,13 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     bool ok = true;
     // Advances k to the next tile with work and decodes it; a split tile
     // with no visible key on the way gets its empty partial result here
-    // (weight 0 in the merge).
+    // (weight 0 in the merge).  A half of a split tail tile is always
+    // returned: even with no KV block it owes its partner a partial result.
     auto next_work = [&](int& k, Tile& tl) -> bool {
       for (;; ++k) {
-        const int ti = tile_of(p, k);
+        int pr = -1;
+        const int ti = tile_of<kTail>(p, k, pr);
         if (ti < 0) return false;
-        tl = decode_tile(p, ti);
-        if (tl.n_blocks > 0) return true;
+        tl = decode_tile(p, ti, pr);
+        if (tl.n_blocks > 0 || tl.pair >= 0) return true;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           const int rho = tl.m0 + h * kBlockM + r;
@@ -489,6 +551,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int k_next = k + 1;
       Tile nxt;
       const bool have_next = next_work(k_next, nxt);
+      if (cur.pair == 1) {
+        // Second KV half of a split tail tile, the CTA's last tile.  Once its
+        // last PV is done (PV_1 is issued after PV_0, and tensor-core work
+        // runs in issue order) the K/V ring and the Q buffer are idle: the
+        // normalised fp32 partial O_t goes to the ring as [t][row][D], the
+        // 16-byte pieces of a row XOR-swizzled by row % 8, and its base-2
+        // log-sum-exp to the Q buffer as [t][row].  Then every thread arrives
+        // on the partner's xfer_full and waits on this CTA's xfer_free: the
+        // partner has read it all.  A half with no KV block (not produced by
+        // the launch's split rule, which needs long tiles, but handled) leaves
+        // O unset and its log-sum-exp -inf (weight 0 in the merge).
+        float* part = reinterpret_cast<float*>(sKV);
+        float* part_l = reinterpret_cast<float*>(sQ);
+        float lsum[2] = {0.f, 0.f}, lpsum[2] = {0.f, 0.f}, lmax[2] = {0.f, 0.f};
+        if (cur.n_blocks > 0) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (t >= n_sub) break;
+            const int buf = (int)(ntl[t] & 1);
+            if (!warp_wait(&fin[buf * 2 + t], (ntl[t] >> 1) & 1, sAbort, budget) ||
+                !warp_wait(&pv_done[t], ntl[t] & 1, sAbort, budget)) {
+              ok = false;
+              break;
+            }
+            ++ntl[t];
+            const int sb = (buf * 2 + t) * kBlockM + r;
+            lsum[t] = sRowSum[sb];
+            lpsum[t] = sRowSumP[sb];
+            lmax[t] = sRowMax[sb];
+          }
+          tc_fence_after_sync();
+        }
+        if (!ok) break;
+        // the ring and the Q buffer were last written by TMA and read by the
+        // tensor core (both complete): order the plain stores after them
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (t >= n_sub) break;
+          const bool empty = !(lpsum[t] > 0.f);
+          const float inv_l = empty ? 0.f : 1.f / lpsum[t];
+          part_l[t * kBlockM + r] = empty ? -INFINITY : lmax[t] + log2f(lsum[t]);
+          if (cur.n_blocks > 0) {
+            float* row = part + (size_t)(t * kBlockM + r) * D;
+            const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
+#pragma unroll 1
+            for (int ch = 0; ch < D / 16; ++ch) {
+              uint32_t o[16];
+              tmem_ld_x16(tO + ch * 16, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+#pragma unroll
+              for (int qd = 0; qd < 4; ++qd) {
+                const int cc = ch * 4 + qd;  // 16-byte piece of the row
+                *reinterpret_cast<float4*>(row + 4 * (cc ^ (r & 7))) =
+                    make_float4(u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
+                                u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
+              }
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), cluster_ctarank() ^ 1u));
+        if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) ok = false;
+        break;  // the tail round is the last: no tile follows
+      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (t < n_sub) {
@@ -511,7 +639,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int rho = cur.m0 + t * kBlockM + r;
           // The tensor-memory loads are warp-wide; only the stores depend on
           // whether the row exists.
-          if (p.o_part != nullptr) {
+          if (cur.pair == 0) {
+            // First KV half of a split tail tile: merge with the partner's
+            // partial (in its shared memory; see the sender above) by the
+            // two halves' log-sum-exps, then write O and LSE.
+            if (t == 0 && !warp_wait_cluster(xfer_full, 0, sAbort, budget)) {
+              ok = false;
+              break;
+            }
+            const uint32_t peer = cluster_ctarank() ^ 1u;
+            const uint32_t prow =
+                mapa_shared(smem_u32(sKV), peer) + (uint32_t)((t * kBlockM + r) * D * 4);
+            const float l1 =
+                ld_shared_cluster_f32(mapa_shared(smem_u32(sQ), peer) + (uint32_t)((t * kBlockM + r) * 4));
+            const float l0 = empty ? -INFINITY : m + log2f(l);
+            const float mx = fmaxf(l0, l1);
+            float w0 = 0.f, w1 = 0.f, lse_m = -INFINITY;
+            if (mx > -INFINITY) {
+              const float e0 = ex2_approx(l0 - mx), e1 = ex2_approx(l1 - mx);
+              const float inv = 1.f / (e0 + e1);
+              w0 = e0 * inv * inv_l;  // this half's O is unnormalised in tensor memory
+              w1 = e1 * inv;
+              lse_m = (mx + log2f(e0 + e1)) * 0.69314718055994530942f;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                  ((size_t)cur.zkv * R + rho) * D);
+            // 16 columns at a time (the correction warpgroup's register budget)
+#pragma unroll 1
+            for (int ch = 0; ch < D / 16; ++ch) {
+              uint32_t o[16];
+              tmem_ld_x16(tO + ch * 16, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+#pragma unroll
+              for (int qd = 0; qd < 4; ++qd) {
+                const int cc = ch * 4 + qd;  // 16-byte piece of the row
+                const float4 pv = ld_shared_cluster_v4(prow + 16u * (uint32_t)(cc ^ (r & 7)));
+                // w1 = 0 (an empty partner half) must not meet its unset values
+                const float a[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float own = u2f(o[qd * 4 + e]) * w0;
+                  o[qd * 4 + e] = f2u(w1 > 0.f ? fmaf(w1, a[e], own) : own);
+                }
+              }
+              if (rho < R) {
+#pragma unroll
+                for (int qd = 0; qd < 2; ++qd) {
+                  uint4 val;
+                  val.x = pack_bf16x2(u2f(o[qd * 8 + 0]), u2f(o[qd * 8 + 1]));
+                  val.y = pack_bf16x2(u2f(o[qd * 8 + 2]), u2f(o[qd * 8 + 3]));
+                  val.z = pack_bf16x2(u2f(o[qd * 8 + 4]), u2f(o[qd * 8 + 5]));
+                  val.w = pack_bf16x2(u2f(o[qd * 8 + 6]), u2f(o[qd * 8 + 7]));
+                  dst[ch * 2 + qd] = val;
+                }
+              }
+            }
+            if (rho < R) p.lse[(size_t)cur.zkv * R + rho] = lse_m;
+          } else if (p.o_part != nullptr) {
             // split-KV partial: fp32 O normalised within the split, and its LSE
             const size_t row = (size_t)cur.split * p.total_rows + (size_t)cur.zkv * R + rho;
             float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
@@ -561,6 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // of the next tile may start on sub-tile t
         if (have_next && (t == 0 || nxt.has_sub1)) mbar_arrive(&p_full[t]);
       }
+      // the partner's partial has been read
+      if (cur.pair == 0 && ok) mbar_arrive_remote(mapa_shared(smem_u32(xfer_free), cluster_ctarank() ^ 1u));
       if (!ok) break;
       stamp(tr, kEvEnd, 0);
       k = k_next;
@@ -593,9 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t nb[2] = {0, 0};   // blocks so far per sub-tile: the phase of p_full[t]
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int ti = tile_of(p, k);
+        int pr = -1;
+        const int ti = tile_of<kTail>(p, k, pr);
         if (ti < 0) break;
-        const Tile tl = decode_tile(p, ti);
+        const Tile tl = decode_tile(p, ti, pr);
         const int n = tl.n_blocks;
         if (n <= 0) continue;
         const bool tr = trace_cta && k == 0;
@@ -713,9 +901,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int ti = tile_of(p, k);
+        int pr = -1;
+        const int ti = tile_of<kTail>(p, k, pr);
         if (ti < 0) break;
-        const Tile tl = decode_tile(p, ti);
+        const Tile tl = decode_tile(p, ti, pr);
         if (tl.n_blocks <= 0) continue;
         const bool tr = trace_cta && k == 0;
         for (int j = 0; j < tl.n_blocks; ++j) {
@@ -768,6 +957,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // neither CTA of a pair exits while the other may still touch its shared
+  // memory (every role of both reaches this point, all waits being bounded)
+  if (kTail) cluster_sync_all();
   if (warp == 12) tmem_dealloc(tmem, C::kTmemCols);
   if (threadIdx.x == 0 && *sAbort) atomicCAS(&g_attn_status, 0, (int)ATTN_ERR_TIMEOUT);
   if constexpr (kTrace) {
@@ -784,36 +976,81 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 namespace {
 
 std::mutex g_launch_mu;
-bool g_attr_set[2][2][64] = {};  // [D == 128][trace][device]
+bool g_attr_set[2][2][2][64] = {};  // [D == 128][trace][split tail][device]
 int g_sm_count[64] = {};
 
-template <int D, bool kTrace>
-cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
+// The SM count of the current device and, once per instantiation and
+// device, the kernel's shared-memory attribute.
+template <int D, bool kTrace, bool kTail>
+cudaError_t prepare(int* sms) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int sms = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_launch_mu);
-    bool& attr_set = g_attr_set[D == 128][kTrace][dev];
-    if (!attr_set) {
-      err = cudaFuncSetAttribute(attn_fwd_kernel<D, kTrace>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-      if (err != cudaSuccess) return err;
-      attr_set = true;
-    }
-    if (g_sm_count[dev] == 0) {
-      err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-      if (err != cudaSuccess) return err;
-    }
-    sms = g_sm_count[dev];
+  std::lock_guard<std::mutex> lk(g_launch_mu);
+  bool& attr_set = g_attr_set[D == 128][kTrace][kTail][dev];
+  if (!attr_set) {
+    err = cudaFuncSetAttribute(attn_fwd_kernel<D, kTrace, kTail>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
   }
+  if (g_sm_count[dev] == 0) {
+    err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+  }
+  *sms = g_sm_count[dev];
+  return cudaSuccess;
+}
+
+template <int D, bool kTrace>
+cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
+  int sms = 0;
+  cudaError_t err = prepare<D, kTrace, false>(&sms);
+  if (err != cudaSuccess) return err;
   if (p.num_tiles <= 0 || sms <= 0) return cudaErrorInvalidValue;
   // persistent grid: one CTA per SM (the kernel's shared memory allows no
   // second), fewer when there are fewer tiles
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  attn_fwd_kernel<D, kTrace><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  AttnParams q = p;
+  q.tail_base = 0;
+  q.tail_pairs = 0;
+  if constexpr (!kTrace) {
+    // Split tail: when the last round of whole tiles would leave more than
+    // half of the CTAs idle, each of its tiles goes to a pair of CTAs instead
+    // (half of its KV blocks each), so the round takes about half a tile.
+    // Clusters of two CTAs, one per SM, all fit at once on this part.
+    // Non-causal tiles only (with the causal mask the last round holds the
+    // shortest tiles), and long ones.
+    const int kv_blocks = (p.S_kv + kBlockN - 1) / kBlockN;
+    if (p.kv_splits == 1 && !p.causal && kv_blocks >= kSplitTailMinBlocks &&
+        p.num_tiles > grid && grid % 2 == 0) {
+      const int rounds = p.num_tiles / grid;
+      const int tail = p.num_tiles - rounds * grid;
+      if (tail > 0 && tail <= grid / 2) {
+        q.tail_base = rounds * grid;
+        q.tail_pairs = tail;
+      }
+    }
+    if (q.tail_pairs > 0) {
+      err = prepare<D, false, true>(&sms);
+      if (err != cudaSuccess) return err;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, false, true>, q);
+    }
+  }
+  attn_fwd_kernel<D, kTrace, false><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q);
   return cudaGetLastError();
 }
 

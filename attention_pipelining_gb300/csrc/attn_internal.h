@@ -48,6 +48,14 @@ struct AttnParams {
   int kv_blocks_per_split;
   float* o_part;
   float* lse_part;
+  // Split tail (set at launch; 0 = off): when the last round of the grid
+  // holds tail_pairs <= G / 2 tiles (list entries tail_base = R * G ..),
+  // the grid runs as clusters of two CTAs and cluster i takes tail tile
+  // tail_base + i, each CTA one half of its KV blocks.  The second CTA hands
+  // its partial result to the first through distributed shared memory, and
+  // the first writes the merged O and LSE.  Off with kv_splits > 1.
+  int tail_base;
+  int tail_pairs;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   unsigned long long timeout_ns;  // budget of any single wait inside the kernel
   // Timeline trace (the trace instantiation only): SM clock stamps of the

@@ -68,6 +68,13 @@ typedef enum {
  *
  * All pointers must be 16-byte aligned and must not alias o/lse with inputs.
  * Returns once the kernel is queued; no synchronisation happens inside.
+ *
+ * Scheduling: 256-row tiles on a persistent grid of one CTA per SM.  When
+ * the last round of tiles would leave more than half of the SMs idle, the
+ * grid runs as clusters of two CTAs and each tile of that round is split
+ * across a pair: each CTA takes half of its KV blocks and the first merges
+ * the second's partial result (received through distributed shared memory)
+ * by their log-sum-exps.  The results are deterministic for given sizes.
  */
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
@@ -86,8 +93,10 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * so each chunk's copies overlap the other chunks' kernels.  The internal
  * streams and events are created on first use, once per device, and kept;
  * concurrent callers on one device queue their chunks one call at a time.
- * Every row is computed by the same tiles as in one attn_fwd call, so the
- * results are bit-identical to it.  Host buffers should be page-locked for
+ * The results are those of attn_fwd on each chunk: bit-identical to one
+ * attn_fwd call on the whole, except in the rows of tiles that one of the
+ * two splits across a CTA pair (see attn_fwd), which agree to within the
+ * rounding of that merge.  Host buffers should be page-locked for
  * the copies to be asynchronous.  Returns once everything is queued; the
  * host outputs are valid once `stream` has been synchronised.  Same argument
  * rules as attn_fwd for the device buffers; host pointers must be non-null.

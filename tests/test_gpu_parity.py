@@ -44,6 +44,11 @@ SMALL = [
     (1, 2, 2, 77, 300, 64, False, 1.0),
     (1, 3, 3, 40, 1, 128, False, 1.0),     # a single key
     (1, 3, 3, 40, 1, 64, True, 1.0),
+    # 160 tiles of 32 KV blocks on 152 SMs: the last round's 8 tiles are
+    # split across CTA pairs (each half of the KV blocks, merged through the
+    # cluster); plain heads and grouped heads
+    (1, 40, 40, 1024, 4096, 64, False, 1.0),
+    (10, 8, 2, 512, 4096, 64, False, 1.0),
 ]
 ODD_S = [1, 17, 127, 129, 255, 257, 383, 513]
 
@@ -127,8 +132,10 @@ HOST_PIPE_SHAPES = [
 def test_host_entry_pipelined_matches_device(shape):
     """Inputs of 32 MiB or more: the host entry splits the row groups into
     chunks whose copies overlap the other chunks' kernels (on the caller's
-    side stream here); every row is computed by the same tiles as in one
-    attn_fwd call, so the outputs are bit-identical to it."""
+    side stream here).  In these shapes neither the one call (256 and 1024
+    tiles) nor a chunk (fewer tiles than SMs) splits its last round across
+    CTA pairs, so every row is computed by the same tiles and the outputs
+    are bit-identical to one attn_fwd call."""
     B, Hq, Hkv, S, D, causal = shape
     q, k, v = make_qkv(B, Hq, Hkv, S, S, D, seed=7)
     scale = 1 / math.sqrt(D)
@@ -148,6 +155,35 @@ def test_host_entry_pipelined_matches_device(shape):
     assert ap.device_status(reset=True) == 0
     assert torch.equal(oh, o_ref.cpu())
     assert torch.equal(lh, lse_ref.cpu())
+
+
+def test_host_entry_where_one_call_splits_its_tail():
+    """512 tiles in one call (its last 56 split across CTA pairs) against
+    chunks of 32 tiles (none split): the same result within the rounding of
+    the split tiles' merge, and parity against the oracle on sampled rows."""
+    B, Hq, Hkv, S, D = 1, 32, 32, 4096, 128
+    q, k, v = make_qkv(B, Hq, Hkv, S, S, D, seed=71)
+    scale = 1 / math.sqrt(D)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = ap.attn_fwd(qd, kd, vd, False, scale)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((B, Hq, S), dtype=torch.float32).pin_memory()
+    od, ld = torch.empty_like(qd), torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    ap.attn_fwd_host(qh, kh, vh, oh, lh, torch.empty_like(qd), torch.empty_like(kd),
+                     torch.empty_like(vd), od, ld, False, scale)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    assert (oh.float() - o_ref.cpu().float()).abs().max().item() <= 2e-2
+    assert (lh - lse_ref.cpu()).abs().max().item() <= 1e-4
+    rng = np.random.default_rng(72)
+    rows = np.unique(np.concatenate([rng.integers(0, Hq * S, 48),
+                                     Hq * S - 1 - rng.integers(0, 2048, 16)]))
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, False, scale)
+    idx = torch.from_numpy(rows)
+    assert_parity(oh.reshape(-1, D)[idx], lh.reshape(-1)[idx], o64, lse64, "host, split tail")
+    assert_parity(o_ref.cpu().reshape(-1, D)[idx], lse_ref.cpu().reshape(-1)[idx], o64, lse64,
+                  "device, split tail")
 
 
 def _sample_rows(w, n_heads=6, seed=0):
