@@ -1021,10 +1021,11 @@ cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
     // (half of its KV blocks each), so the round takes about half a tile.
     // Clusters of two CTAs, one per SM, all fit at once on this part.
     // Non-causal tiles only (with the causal mask the last round holds the
-    // shortest tiles), and long ones.
+    // shortest tiles), long ones, and only when the tiles write O and LSE
+    // (a split-KV launch, even of one split, writes partials for its merge).
     const int kv_blocks = (p.S_kv + kBlockN - 1) / kBlockN;
-    if (p.kv_splits == 1 && !p.causal && kv_blocks >= kSplitTailMinBlocks &&
-        p.num_tiles > grid && grid % 2 == 0) {
+    if (p.kv_splits == 1 && p.o_part == nullptr && !p.causal &&
+        kv_blocks >= kSplitTailMinBlocks && p.num_tiles > grid && grid % 2 == 0) {
       const int rounds = p.num_tiles / grid;
       const int tail = p.num_tiles - rounds * grid;
       if (tail > 0 && tail <= grid / 2) {

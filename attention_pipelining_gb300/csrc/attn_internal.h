@@ -53,7 +53,7 @@ struct AttnParams {
   // the grid runs as clusters of two CTAs and cluster i takes tail tile
   // tail_base + i, each CTA one half of its KV blocks.  The second CTA hands
   // its partial result to the first through distributed shared memory, and
-  // the first writes the merged O and LSE.  Off with kv_splits > 1.
+  // the first writes the merged O and LSE.  Off in split-KV launches.
   int tail_base;
   int tail_pairs;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2

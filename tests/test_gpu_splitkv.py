@@ -64,3 +64,19 @@ def test_packed_groups_in_plain_forward():
     torch.cuda.synchronize()
     o64, lse64 = oracle.attn_fwd(q, k, v, False, 0.125)
     assert_parity(o.cpu(), lse.cpu(), o64, lse64, "packed plain")
+
+
+def test_one_split_on_a_grid_whose_plain_forward_splits_its_tail():
+    """160 tiles of 32 KV blocks: the plain forward splits its last round
+    across CTA pairs; the split-KV entry with one split must not (its tiles
+    write partials for the merge kernel).  Both against the oracle."""
+    q, k, v = make_qkv(1, 40, 40, 1024, 4096, 64, seed=33)
+    scale = 1.0 / math.sqrt(64)
+    o64, lse64 = oracle.attn_fwd(q, k, v, False, scale)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = ap.attn_fwd_splitkv(qd, kd, vd, False, scale, num_splits=1)
+    o2, l2 = ap.attn_fwd(qd, kd, vd, False, scale)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    assert_parity(o1.cpu(), l1.cpu(), o64, lse64, "split KV, one split")
+    assert_parity(o2.cpu(), l2.cpu(), o64, lse64, "plain, split tail")
