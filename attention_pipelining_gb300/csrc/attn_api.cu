@@ -418,6 +418,9 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   std::lock_guard<std::mutex> lk(g_pipe_mu);
   HostPipe* hp = host_pipe(dev);
   if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
+  // past this point every exit joins the pipe, so `s` stays ordered after
+  // whatever was already queued on the internal streams
+  auto leave = [&](attn_status_t st) { pipe_join(hp, s); return st; };
   const int r = H_q / H_kv;
   const size_t q_group = (size_t)r * S_q * D * 2;     // bytes of one group's Q (and O)
   const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (and V)
@@ -438,20 +441,20 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
         cudaMemcpyAsync(db(v_dev, ko), hb(v_host, ko), kn, cudaMemcpyHostToDevice, hp->up) !=
             cudaSuccess ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
     cudaStream_t cs = hp->comp[c & 1];
-    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st =
         fwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo), lse_dev + lo, 1,
                  ng * r, ng, S_q, S_kv, D, causal, scale, nullptr, 0, 0, -1, kDefaultTimeoutNs, cs);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK) return leave(st);
     if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
         cudaMemcpyAsync(db(o_host, qo), db(o_dev, qo), qn, cudaMemcpyDeviceToHost, hp->down) !=
             cudaSuccess ||
         cudaMemcpyAsync(lse_host + lo, lse_dev + lo, ln * sizeof(float), cudaMemcpyDeviceToHost,
                         hp->down) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
   }
   return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -496,6 +499,9 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
   std::lock_guard<std::mutex> lk(g_pipe_mu);
   HostPipe* hp = host_pipe(dev);
   if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
+  // past this point every exit joins the pipe, so `s` stays ordered after
+  // whatever was already queued on the internal streams
+  auto leave = [&](attn_status_t st) { pipe_join(hp, s); return st; };
   const int r = H_q / H_kv;
   const size_t q_group = (size_t)r * S_q * D * 2;     // bytes of one group's Q (O, dO, dQ)
   const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (V, dK, dV)
@@ -519,20 +525,20 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
         !up(lse_dev + lo, lse_host + lo, ln * sizeof(float), hp->up) ||
         !up(db(dout_dev, qo), hb(dout_host, qo), qn, hp->up) ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
     cudaStream_t cs = hp->comp[c & 1];
-    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st = bwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo),
                                 lse_dev + lo, db(dout_dev, qo), db(dq_dev, qo), db(dk_dev, ko),
                                 db(dv_dev, ko), db(workspace, z0 * ws_group), ng * ws_group, 1,
                                 ng * r, ng, S_q, S_kv, D, causal, scale, cs);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK) return leave(st);
     if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
         !down(db(dq_host, qo), db(dq_dev, qo), qn, hp->down) ||
         !down(db(dk_host, ko), db(dk_dev, ko), kn, hp->down) ||
         !down(db(dv_host, ko), db(dv_dev, ko), kn, hp->down))
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
   }
   return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -642,6 +648,9 @@ static attn_status_t chunk_scan_host_impl(const float* cb_host, const float* dA_
   std::lock_guard<std::mutex> lk(g_pipe_mu);
   HostPipe* hp = host_pipe(dev);
   if (!hp || !pipe_fork(hp, s)) return ATTN_ERR_CUDA;
+  // past this point every exit joins the pipe, so `s` stays ordered after
+  // whatever was already queued on the internal streams
+  auto leave = [&](attn_status_t st) { pipe_join(hp, s); return st; };
   auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
   auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
   for (int c = 0; c < chunks; ++c) {
@@ -656,17 +665,17 @@ static attn_status_t chunk_scan_host_impl(const float* cb_host, const float* dA_
         !up(db(dt_dev, vo), hb(dt_host, vo), vn, hp->up) ||
         !up(db(x_dev, xo), hb(x_host, xo), xn, hp->up) ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
     cudaStream_t cs = hp->comp[c & 1];
-    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st = chunk_scan_impl(cb_dev + b0 * cb_b, dA_dev + b0 * vec_b,
                                        dt_dev + b0 * vec_b, db(x_dev, xo), db(out_dev, xo), nb,
                                        L, H, G, P, Q, cs);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK) return leave(st);
     if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
         !down(db(out_host, xo), db(out_dev, xo), xn, hp->down))
-      return ATTN_ERR_CUDA;
+      return leave(ATTN_ERR_CUDA);
   }
   return pipe_join(hp, s) ? ATTN_OK : ATTN_ERR_CUDA;
 }
