@@ -327,6 +327,11 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
 // inputs and the last chunk's outputs, which nothing overlaps, are then
 // small); when the copies take longer, 8 (fewer, larger copies).
 constexpr int kHostChunks = 16;
+// The chunk scan's copies always take far longer than its kernel, and its
+// chunks are large (a batch entry of the 64 x 8192 workload is 147 MB): it
+// takes up to kHostChunksMax chunks, so the unoverlapped first upload and
+// last download are short.
+constexpr int kHostChunksMax = 32;
 // Rates on GB300 that decide which side is longer: the forward's and the
 // backward's dense rates and the host link's copy rate (measured, both
 // directions).
@@ -337,7 +342,7 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t up = nullptr, down = nullptr, comp[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t loaded[kHostChunks] = {}, computed[kHostChunks] = {};
+  cudaEvent_t loaded[kHostChunksMax] = {}, computed[kHostChunksMax] = {};
 };
 static std::mutex g_pipe_mu;
 static HostPipe g_pipe[64];
@@ -363,7 +368,7 @@ static HostPipe* host_pipe(int dev) {
             cudaStreamCreateWithFlags(&hp.comp[1], sf) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.done, ef) == cudaSuccess;
-  for (int c = 0; ok && c < kHostChunks; ++c)
+  for (int c = 0; ok && c < kHostChunksMax; ++c)
     ok = cudaEventCreateWithFlags(&hp.loaded[c], ef) == cudaSuccess &&
          cudaEventCreateWithFlags(&hp.computed[c], ef) == cudaSuccess;
   if (!ok) return nullptr;  // (what was made stays cached for the process)
@@ -611,7 +616,7 @@ static attn_status_t chunk_scan_impl(const float* cb, const float* dA_cs, const 
   return ATTN_OK;
 }
 
-// chunk_scan_fwd_host: the batch is cut into chunks of consecutive batch
+// chunk_scan_fwd_host: the batch is cut into up to 32 chunks of consecutive batch
 // entries (a contiguous slice of every tensor and a problem of its own),
 // pipelined on the same streams as attn_fwd_host.  The kernel is far shorter
 // than the copies here, so the gain is the uploads of one chunk overlapping
@@ -627,8 +632,8 @@ static attn_status_t chunk_scan_host_impl(const float* cb_host, const float* dA_
   const size_t x_b = (size_t)L * H * P * 2;  // bytes of its x (and of its out)
   const size_t in_bytes = (size_t)B * (cb_b * 4 + 2 * vec_b * 4 + x_b);
   const size_t out_bytes = (size_t)B * x_b;
-  // the kernel moves its bytes at about 4 TB/s: always shorter than the copies
-  const int chunks = host_chunks(in_bytes, out_bytes, (double)(in_bytes + out_bytes) / 4.0e12, B);
+  const int chunks =
+      in_bytes < kHostPipeMinBytes ? 1 : (B < kHostChunksMax ? B : kHostChunksMax);
   auto up = [](void* dst, const void* src, size_t n, cudaStream_t st) {
     return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
   };

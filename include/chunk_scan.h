@@ -47,10 +47,11 @@ attn_status_t chunk_scan_fwd(const float *cb, const float *dA_cs, const float *d
  * host memory into the caller's device buffers (the *_dev arguments, same
  * shapes as chunk_scan_fwd's), runs the scan and copies out back to host
  * memory, ordered after the work already queued on `stream` and before the
- * work queued on it afterwards.  Inputs of 32 MiB or more are split into 8
- * or 16 chunks of consecutive batch entries, pipelined on the internal
- * streams attn_fwd_host uses: one chunk's inputs go up while another's
- * output comes back, so the host link carries both directions at once.
+ * work queued on it afterwards.  Inputs of 32 MiB or more are split into
+ * chunks of consecutive batch entries (one per entry, at most 32),
+ * pipelined on the internal streams attn_fwd_host uses: one chunk's inputs
+ * go up while another's output comes back, so the host link carries both
+ * directions at once.
  * Every output element is computed the same way as in one chunk_scan_fwd
  * call, so the results are bit-identical to it.  Host buffers should be
  * page-locked for the copies to be asynchronous.  Returns once everything
