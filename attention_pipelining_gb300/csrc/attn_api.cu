@@ -347,13 +347,40 @@ struct HostPipe {
 static std::mutex g_pipe_mu;
 static HostPipe g_pipe[64];
 
-// Chunks for a host call: one below kHostPipeMinBytes of inputs, else 16 or
-// 8 as above, never more than the row groups.
-static int host_chunks(size_t in_bytes, size_t out_bytes, double kernel_s, int groups) {
-  if (in_bytes < kHostPipeMinBytes) return 1;
+// Chunk boundaries of a host call over `units` row groups: chunk c holds
+// units [bound[c], bound[c + 1]).
+struct ChunkPlan {
+  int n = 1;
+  int bound[kHostChunksMax + 1] = {};
+};
+
+// One chunk below kHostPipeMinBytes of inputs, else 16 or 8 as above (never
+// more than the units), evenly sized.  When the kernels are the longer side,
+// the first and the last chunk hold one unit each and the units between keep
+// the even chunks' size: the first upload and the last download are the two
+// copies that nothing overlaps, and chunks that small everywhere would leave
+// each kernel too few tiles.
+static ChunkPlan host_plan(size_t in_bytes, size_t out_bytes, double kernel_s, int units) {
+  ChunkPlan pl;
+  pl.bound[0] = 0;
+  pl.bound[1] = units;
+  if (in_bytes < kHostPipeMinBytes) return pl;
   const bool kernel_longer = kernel_s > (double)(in_bytes + out_bytes) / kHostLinkBytes;
   const int want = kernel_longer ? kHostChunks : kHostChunks / 2;
-  return groups < want ? groups : want;
+  const int even = units < want ? units : want;
+  const int size = units / even;  // units per even chunk
+  const int inner = units - 2;
+  const int n_in = size > 0 ? (inner + size - 1) / size : 0;
+  if (kernel_longer && size >= 2 && n_in >= 1 && n_in + 2 <= kHostChunksMax) {
+    pl.n = n_in + 2;
+    pl.bound[1] = 1;
+    for (int i = 1; i <= n_in; ++i) pl.bound[1 + i] = 1 + (int)((long long)inner * i / n_in);
+    pl.bound[pl.n] = units;
+    return pl;
+  }
+  pl.n = even;
+  for (int c = 0; c <= even; ++c) pl.bound[c] = (int)((long long)units * c / even);
+  return pl;
 }
 
 // The device's streams and events, made on first use (call with g_pipe_mu held).
@@ -402,8 +429,8 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
   const int groups = B * H_kv;
   const double flops = 4.0 * B * H_q * (double)S_q * S_kv * D * (causal ? 0.5 : 1.0);
-  const int chunks =
-      host_chunks(q_bytes + 2 * kv_bytes, q_bytes, flops / kHostKernelFlops, groups);
+  const ChunkPlan plan = host_plan(q_bytes + 2 * kv_bytes, q_bytes, flops / kHostKernelFlops, groups);
+  const int chunks = plan.n;
   if (chunks <= 1) {
     if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
@@ -431,8 +458,8 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
   const size_t kv_group = (size_t)S_kv * D * 2;       // bytes of one group's K (and V)
   const size_t lse_group = (size_t)r * S_q;           // floats of one group's LSE
   for (int c = 0; c < chunks; ++c) {
-    const int z0 = (int)((long long)groups * c / chunks);
-    const int z1 = (int)((long long)groups * (c + 1) / chunks);
+    const int z0 = plan.bound[c];
+    const int z1 = plan.bound[c + 1];
     const int ng = z1 - z0;
     const size_t qo = z0 * q_group, qn = ng * q_group;
     const size_t ko = z0 * kv_group, kn = ng * kv_group;
@@ -477,8 +504,9 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
   const size_t lse_bytes = (size_t)B * H_q * S_q * sizeof(float);
   const int groups = B * H_kv;
   const double flops = 2.5 * 4.0 * B * H_q * (double)S_q * S_kv * D * (causal ? 0.5 : 1.0);
-  const int chunks = host_chunks(3 * q_bytes + 2 * kv_bytes + lse_bytes, q_bytes + 2 * kv_bytes,
-                                 flops / kHostBwdFlops, groups);
+  const ChunkPlan plan = host_plan(3 * q_bytes + 2 * kv_bytes + lse_bytes,
+                                   q_bytes + 2 * kv_bytes, flops / kHostBwdFlops, groups);
+  const int chunks = plan.n;
   auto up = [](void* dst, const void* src, size_t n, cudaStream_t st) {
     return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
   };
@@ -517,8 +545,8 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
   auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
   auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
   for (int c = 0; c < chunks; ++c) {
-    const int z0 = (int)((long long)groups * c / chunks);
-    const int z1 = (int)((long long)groups * (c + 1) / chunks);
+    const int z0 = plan.bound[c];
+    const int z1 = plan.bound[c + 1];
     const int ng = z1 - z0;
     const size_t qo = z0 * q_group, qn = ng * q_group;
     const size_t ko = z0 * kv_group, kn = ng * kv_group;
