@@ -85,10 +85,12 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * memory into the caller's device buffers q_dev/k_dev/v_dev, runs attn_fwd
  * into o_dev/lse_dev, and copies o/lse back to host memory, ordered after
  * the work already queued on `stream` and before the work queued on it
- * afterwards.  Inputs of 32 MiB or more are split into 8 or 16 chunks (16
- * when the kernels are expected to take longer than the copies) of
+ * afterwards.  Inputs of 32 MiB or more are split into chunks of
  * consecutive (batch, kv-head) row groups, each a contiguous slice of every
- * tensor: a chunk's inputs go up on one internal stream, its kernel runs on
+ * tensor: 8 even chunks when the copies are expected to take longer than the
+ * kernels, else about 16, the first and the last of a single row group when
+ * the others hold two or more (those two copies are the ones nothing
+ * overlaps).  A chunk's inputs go up on one internal stream, its kernel runs on
  * one of two internal compute streams and its outputs come back on another,
  * so each chunk's copies overlap the other chunks' kernels.  The internal
  * streams and events are created on first use, once per device, and kept;
@@ -220,8 +222,8 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
  * buffers (the *_dev arguments, same shapes as attn_bwd's), runs the backward
  * and copies dq, dk and dv back to host memory, ordered after the work
  * already queued on `stream` and before the work queued on it afterwards.
- * Inputs of 32 MiB or more are split into 8 or 16 chunks of consecutive
- * (batch, kv-head) row groups; a chunk's inputs go up on one internal
+ * Inputs of 32 MiB or more are split into chunks of consecutive (batch,
+ * kv-head) row groups as in attn_fwd_host; a chunk's inputs go up on one internal
  * stream, its three kernels run on one of two internal compute streams with
  * its own slice of `workspace`, and its gradients come back on another, so
  * each chunk's copies overlap the other chunks' kernels.  Every gradient
