@@ -319,7 +319,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
 // attn_fwd_host and attn_bwd_host: the row groups (b, h_kv) are cut into
 // chunks of consecutive groups; a chunk is a contiguous slice of every tensor
 // and a problem of its own (B = 1, its groups' heads).  Its inputs go up on
-// one stream, its kernels run on one of two compute streams (so one chunk's
+// one stream, its kernels run on one of three compute streams (so one chunk's
 // last tiles overlap the next chunk's first), and its outputs come back on a
 // third: the copies of the other chunks overlap each chunk's kernels.  The
 // streams start after, and the caller's stream continues after, the whole.
@@ -332,6 +332,10 @@ constexpr int kHostChunks = 16;
 // takes up to kHostChunksMax chunks, so the unoverlapped first upload and
 // last download are short.
 constexpr int kHostChunksMax = 32;
+// Compute streams: consecutive chunks' kernels run on different ones, so a
+// chunk kernel that leaves SMs idle (a chunk of fewer tiles than SMs) shares
+// the GPU with the next chunks'.
+constexpr int kHostCompStreams = 3;
 // Rates on GB300 that decide which side is longer: the forward's and the
 // backward's dense rates and the host link's copy rate (measured, both
 // directions).
@@ -340,7 +344,7 @@ constexpr size_t kHostPipeMinBytes = size_t(32) << 20;  // smaller inputs: one c
 
 struct HostPipe {
   bool ready = false;
-  cudaStream_t up = nullptr, down = nullptr, comp[2] = {nullptr, nullptr};
+  cudaStream_t up = nullptr, down = nullptr, comp[kHostCompStreams] = {};
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t loaded[kHostChunksMax] = {}, computed[kHostChunksMax] = {};
 };
@@ -391,10 +395,10 @@ static HostPipe* host_pipe(int dev) {
   const unsigned ef = cudaEventDisableTiming;
   bool ok = cudaStreamCreateWithFlags(&hp.up, sf) == cudaSuccess &&
             cudaStreamCreateWithFlags(&hp.down, sf) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&hp.comp[0], sf) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&hp.comp[1], sf) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.done, ef) == cudaSuccess;
+  for (int i = 0; ok && i < kHostCompStreams; ++i)
+    ok = cudaStreamCreateWithFlags(&hp.comp[i], sf) == cudaSuccess;
   for (int c = 0; ok && c < kHostChunksMax; ++c)
     ok = cudaEventCreateWithFlags(&hp.loaded[c], ef) == cudaSuccess &&
          cudaEventCreateWithFlags(&hp.computed[c], ef) == cudaSuccess;
@@ -405,11 +409,12 @@ static HostPipe* host_pipe(int dev) {
 
 // The pipe's streams start after the work queued on `s` so far ...
 static bool pipe_fork(HostPipe* hp, cudaStream_t s) {
-  return cudaEventRecord(hp->start, s) == cudaSuccess &&
-         cudaStreamWaitEvent(hp->up, hp->start, 0) == cudaSuccess &&
-         cudaStreamWaitEvent(hp->comp[0], hp->start, 0) == cudaSuccess &&
-         cudaStreamWaitEvent(hp->comp[1], hp->start, 0) == cudaSuccess &&
-         cudaStreamWaitEvent(hp->down, hp->start, 0) == cudaSuccess;
+  bool ok = cudaEventRecord(hp->start, s) == cudaSuccess &&
+            cudaStreamWaitEvent(hp->up, hp->start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp->down, hp->start, 0) == cudaSuccess;
+  for (int i = 0; ok && i < kHostCompStreams; ++i)
+    ok = cudaStreamWaitEvent(hp->comp[i], hp->start, 0) == cudaSuccess;
+  return ok;
 }
 
 // ... and `s` continues once every chunk's outputs are back (and so its
@@ -474,7 +479,7 @@ static attn_status_t fwd_host_impl(const void* q_host, const void* k_host, const
             cudaSuccess ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
       return leave(ATTN_ERR_CUDA);
-    cudaStream_t cs = hp->comp[c & 1];
+    cudaStream_t cs = hp->comp[c % kHostCompStreams];
     if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st =
         fwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo), lse_dev + lo, 1,
@@ -559,7 +564,7 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
         !up(db(dout_dev, qo), hb(dout_host, qo), qn, hp->up) ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
       return leave(ATTN_ERR_CUDA);
-    cudaStream_t cs = hp->comp[c & 1];
+    cudaStream_t cs = hp->comp[c % kHostCompStreams];
     if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st = bwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo),
                                 lse_dev + lo, db(dout_dev, qo), db(dq_dev, qo), db(dk_dev, ko),
@@ -699,7 +704,7 @@ static attn_status_t chunk_scan_host_impl(const float* cb_host, const float* dA_
         !up(db(x_dev, xo), hb(x_host, xo), xn, hp->up) ||
         cudaEventRecord(hp->loaded[c], hp->up) != cudaSuccess)
       return leave(ATTN_ERR_CUDA);
-    cudaStream_t cs = hp->comp[c & 1];
+    cudaStream_t cs = hp->comp[c % kHostCompStreams];
     if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return leave(ATTN_ERR_CUDA);
     attn_status_t st = chunk_scan_impl(cb_dev + b0 * cb_b, dA_dev + b0 * vec_b,
                                        dt_dev + b0 * vec_b, db(x_dev, xo), db(out_dev, xo), nb,

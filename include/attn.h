@@ -91,7 +91,7 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * kernels, else about 16, the first and the last of a single row group when
  * the others hold two or more (those two copies are the ones nothing
  * overlaps).  A chunk's inputs go up on one internal stream, its kernel runs on
- * one of two internal compute streams and its outputs come back on another,
+ * one of three internal compute streams and its outputs come back on another,
  * so each chunk's copies overlap the other chunks' kernels.  The internal
  * streams and events are created on first use, once per device, and kept;
  * concurrent callers on one device queue their chunks one call at a time.
@@ -224,7 +224,7 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
  * already queued on `stream` and before the work queued on it afterwards.
  * Inputs of 32 MiB or more are split into chunks of consecutive (batch,
  * kv-head) row groups as in attn_fwd_host; a chunk's inputs go up on one internal
- * stream, its three kernels run on one of two internal compute streams with
+ * stream, its three kernels run on one of three internal compute streams with
  * its own slice of `workspace`, and its gradients come back on another, so
  * each chunk's copies overlap the other chunks' kernels.  Every gradient
  * element is computed by the same tiles in the same order as in one
