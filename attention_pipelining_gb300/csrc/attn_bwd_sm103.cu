@@ -168,47 +168,67 @@ __device__ __forceinline__ void banded_rank(int idx, int n_ranks, int groups, in
 // ---------------------------------------------------------------- prep
 
 // D_i = dO_i . O_i and LSE_i * log2(e), per row of the padded per-group
-// layout [groups, Rp] (rows R..Rp-1 of a group get 0).  One warp per row.
+// layout [groups, Rp] (rows R..Rp-1 of a group get 0).  A warp takes
+// kPrepRowsPerWarp consecutive rows; a lane reads 16 bytes of O and of dO
+// per row, and every load of the warp's rows is issued before any product,
+// so each thread keeps several loads in flight (the kernel streams O and dO
+// from HBM).
+constexpr int kPrepRowsPerWarp = 8;
+
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
                                                             const uint16_t* __restrict__ o,
                                                             const uint16_t* __restrict__ dout,
                                                             const float* __restrict__ lse) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int kLanesPerRow = D * 2 / 16;             // 16-byte pieces of a row
+  constexpr int kRowsPerLoad = 32 / kLanesPerRow;      // rows one warp-wide load covers
+  constexpr int kLoads = kPrepRowsPerWarp / kRowsPerLoad;
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kPrepRowsPerWarp;
   const int lane = threadIdx.x & 31;
-  if (row >= (long long)p.groups * p.Rp) return;
-  const long long z = row / p.Rp;
-  const int rho = (int)(row - z * p.Rp);
-  if (rho >= p.R) {
-    if (lane == 0) {
-      p.ndelta[row] = 0.f;
-      p.nlse2[row] = 0.f;
-    }
-    return;
-  }
-  const long long src = (z * p.R + rho) * D;
-  constexpr int kPer = D / 32;  // elements per lane
-  float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + src + lane * 4);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + src + lane * 4);
-    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+  const int sub = lane / kLanesPerRow;                 // row of a load
+  const int piece = lane % kLanesPerRow;               // 16-byte piece within the row
+  const long long total = (long long)p.groups * p.Rp;
+  uint4 a[kLoads], b[kLoads];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+  for (int i = 0; i < kLoads; ++i) {
+    const long long row = row0 + i * kRowsPerLoad + sub;
+    a[i] = make_uint4(0u, 0u, 0u, 0u);
+    b[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < total) {
+      const long long z = row / p.Rp;
+      const int rho = (int)(row - z * p.Rp);
+      if (rho < p.R) {
+        const long long src = (z * p.R + rho) * D + piece * 8;
+        a[i] = *reinterpret_cast<const uint4*>(o + src);
+        b[i] = *reinterpret_cast<const uint4*>(dout + src);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const uint32_t av[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+    const uint32_t bv[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
       acc += __uint_as_float(av[t] << 16) * __uint_as_float(bv[t] << 16);
       acc += __uint_as_float(av[t] & 0xffff0000u) * __uint_as_float(bv[t] & 0xffff0000u);
     }
-  } else {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + src + lane * 2);
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + src + lane * 2);
-    acc += __uint_as_float(a << 16) * __uint_as_float(b << 16);
-    acc += __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
-  }
+    // sum over the row's lanes (a contiguous group of kLanesPerRow lanes)
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kAll, acc, off);
-  if (lane == 0) {
-    p.ndelta[row] = -acc;
-    p.nlse2[row] = -(lse[z * p.R + rho] * 1.4426950408889634f);
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kAll, acc, off);
+    const long long row = row0 + i * kRowsPerLoad + sub;
+    if (piece == 0 && row < total) {
+      const long long z = row / p.Rp;
+      const int rho = (int)(row - z * p.Rp);
+      if (rho < p.R) {
+        p.ndelta[row] = -acc;
+        p.nlse2[row] = -(lse[z * p.R + rho] * 1.4426950408889634f);
+      } else {
+        p.ndelta[row] = 0.f;
+        p.nlse2[row] = 0.f;
+      }
+    }
   }
 }
 
@@ -827,7 +847,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, co
     }
   }
   const long long prep_rows = (long long)p.groups * p.Rp;
-  attn_bwd_prep_kernel<D><<<(unsigned)((prep_rows + 7) / 8), 256, 0, stream>>>(
+  const long long prep_rows_per_block = 8 * kPrepRowsPerWarp;
+  attn_bwd_prep_kernel<D><<<(unsigned)((prep_rows + prep_rows_per_block - 1) / prep_rows_per_block),
+                            256, 0, stream>>>(
       p, static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
