@@ -3,11 +3,11 @@
 Inputs: seeded q, k, v (synthetic.make_qkv) and dO drawn the same way; the
 GPU backward consumes the GPU forward's O and LSE, the oracle forms its own
 exact softmax.  Tolerance (derived, the pages fix none for the backward):
-each gradient is a sum of products that carry at most three bf16 roundings
-(P or dS before its GEMM, O in D_i, the output), 3 * 2^-9 relative per term;
-dQ and dK also cancel (every row of dS sums to zero), so errors are measured
-against the gradient's norm: relative Frobenius error <= 2^-6 and every
-element within 2^-4 of the tensor's largest magnitude.
+per element, 8 standard deviations of the rounding model of the GPU path (P,
+dS and O rounded to bf16, independent roundings summed over each gradient's
+terms; tests/bwd_bound.py) plus the output's own bf16 rounding, and the RMS
+of the errors in units of that model's deviation at most 1.5.  Every check
+prints the achieved errors.
 """
 import math
 
@@ -18,11 +18,9 @@ import torch
 import attention_pipelining_gb300 as ap
 import oracle
 from attention_pipelining_gb300.synthetic import make_qkv
+from tests import bwd_bound
 
 pytestmark = pytest.mark.gpu
-
-REL_FRO = 2.0 ** -6
-REL_MAX = 2.0 ** -4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,16 +44,19 @@ def gpu_bwd(q, k, v, dout, causal, scale):
     return dq.float().cpu().numpy(), dk.float().cpu().numpy(), dv.float().cpu().numpy()
 
 
-def assert_close(name, got, ref):
-    ref = np.asarray(ref, np.float64)
-    got = np.asarray(got, np.float64)
-    assert np.isfinite(got).all(), f"{name}: non-finite values"
-    err = np.abs(got - ref)
-    fro = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
-    mx = err.max() / max(np.abs(ref).max(), 1e-30)
-    assert fro <= REL_FRO and mx <= REL_MAX, (
-        f"{name}: relative Frobenius error {fro:.3e} (<= {REL_FRO:.3e}), "
-        f"max error / max |ref| {mx:.3e} (<= {REL_MAX:.3e})")
+def check_rows(q, k, v, dout, causal, scale, got, ref, qrows=None, krows=None, what=""):
+    """got / ref: (dq, dk, dv) at the flat rows qrows (dq) and krows (dk, dv),
+    all rows when None; each [n, D] or the full tensors."""
+    D = q.shape[-1]
+    nq = q.numel() // D
+    nk = k.numel() // D
+    qrows = np.arange(nq) if qrows is None else qrows
+    krows = np.arange(nk) if krows is None else krows
+    sq, aq = bwd_bound.dq_sigma(q, k, v, dout, qrows, causal, scale)
+    sk, ak, sv, av = bwd_bound.dkv_sigma(q, k, v, dout, krows, causal, scale)
+    for name, g, r, s_, a_ in (("dq", got[0], ref[0], sq, aq), ("dk", got[1], ref[1], sk, ak),
+                               ("dv", got[2], ref[2], sv, av)):
+        bwd_bound.check(f"{what} {name}", np.reshape(g, (-1, D)), np.reshape(r, (-1, D)), s_, a_)
 
 
 SHAPES = [
@@ -76,11 +77,9 @@ def test_bwd_matches_oracle(shape):
     q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, seed=11)
     dout = make_dout(q.shape, 12)
     scale = 1.0 / math.sqrt(D)
-    dq, dk, dv = gpu_bwd(q, k, v, dout, causal, scale)
-    rq, rk, rv = oracle.attn_bwd(q, k, v, dout, causal, scale)
-    assert_close("dq", dq, rq)
-    assert_close("dk", dk, rk)
-    assert_close("dv", dv, rv)
+    got = gpu_bwd(q, k, v, dout, causal, scale)
+    ref = oracle.attn_bwd(q, k, v, dout, causal, scale)
+    check_rows(q, k, v, dout, causal, scale, got, ref, what=str(shape))
 
 
 def test_bwd_medium_causal_full():
@@ -88,11 +87,9 @@ def test_bwd_medium_causal_full():
     q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, seed=13)
     dout = make_dout(q.shape, 14)
     scale = 1.0 / math.sqrt(D)
-    dq, dk, dv = gpu_bwd(q, k, v, dout, True, scale)
-    rq, rk, rv = oracle.attn_bwd(q, k, v, dout, True, scale)
-    assert_close("dq", dq, rq)
-    assert_close("dk", dk, rk)
-    assert_close("dv", dv, rv)
+    got = gpu_bwd(q, k, v, dout, True, scale)
+    ref = oracle.attn_bwd(q, k, v, dout, True, scale)
+    check_rows(q, k, v, dout, True, scale, got, ref, what=f"{(B, Hq, Hkv, Sq, Skv, D)}")
 
 
 def test_bwd_k_scaled_by_3():
@@ -101,11 +98,20 @@ def test_bwd_k_scaled_by_3():
     q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, k_scale=3.0, seed=15)
     dout = make_dout(q.shape, 16)
     scale = 1.0 / math.sqrt(D)
-    dq, dk, dv = gpu_bwd(q, k, v, dout, True, scale)
-    rq, rk, rv = oracle.attn_bwd(q, k, v, dout, True, scale)
-    assert_close("dq", dq, rq)
-    assert_close("dk", dk, rk)
-    assert_close("dv", dv, rv)
+    got = gpu_bwd(q, k, v, dout, True, scale)
+    ref = oracle.attn_bwd(q, k, v, dout, True, scale)
+    check_rows(q, k, v, dout, True, scale, got, ref, what=f"{(B, Hq, Hkv, Sq, Skv, D)}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_negative_scale(causal):
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 300, 300, 64
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, seed=31)
+    dout = make_dout(q.shape, 32)
+    scale = -0.125
+    got = gpu_bwd(q, k, v, dout, causal, scale)
+    ref = oracle.attn_bwd(q, k, v, dout, causal, scale)
+    check_rows(q, k, v, dout, causal, scale, got, ref, what=f"negative scale causal={causal}")
 
 
 @pytest.mark.parametrize("name", ["batched_b4_h16_s2048_d128", "gqa_b8_hq32_hkv8_s4096_d64_k3",
@@ -123,14 +129,14 @@ def test_bwd_workload_sampled_rows(name):
     qrows = np.unique(np.concatenate([[0, nq - 1], rng.integers(0, nq, 62)]))
     bo = oracle.bwd_default()
     ref_q = bo.dq_rows(q, k, v, dout, qrows, w.causal, w.scale)
-    assert_close("dq rows", dq.reshape(-1, w.D)[qrows], ref_q)
     # key rows of two groups (each needs all of its group's softmax rows)
     groups = [0, w.B * w.H_kv - 1]
     krows = np.concatenate([g * w.S_kv + rng.integers(0, w.S_kv, 8) for g in groups])
     krows = np.unique(np.concatenate([krows, [0, w.B * w.H_kv * w.S_kv - 1]]))
     ref_k, ref_v = bo.dkv_rows(q, k, v, dout, krows, w.causal, w.scale)
-    assert_close("dk rows", dk.reshape(-1, w.D)[krows], ref_k)
-    assert_close("dv rows", dv.reshape(-1, w.D)[krows], ref_v)
+    got = (dq.reshape(-1, w.D)[qrows], dk.reshape(-1, w.D)[krows], dv.reshape(-1, w.D)[krows])
+    check_rows(q, k, v, dout, w.causal, w.scale, got, (ref_q, ref_k, ref_v), qrows=qrows,
+               krows=krows, what=name)
     # sum_j dV_j = sum of dO over the group's rows; sum_j dK_j = 0
     rep = w.H_q // w.H_kv
     do_group = dout.double().numpy().reshape(w.B, w.H_kv, rep, w.S_q, w.D).sum(axis=(2, 3))
