@@ -35,7 +35,8 @@ STATUS = {
 # every entry point of include/attn.h and include/attn_selftest.h
 EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_status",
            "attn_version", "attn_selftest_qk", "attn_selftest_pv", "attn_fwd_trace",
-           "attn_fwd_timeout_test", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
+           "attn_fwd_timeout_test", "attn_fwd_tail_timeout_test", "attn_fwd_tail_pairs",
+           "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
            "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes",
            "attn_bwd_host", "chunk_scan_fwd", "chunk_scan_fwd_host"]
@@ -83,6 +84,11 @@ def _load():
     lib.attn_fwd_timeout_test.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci,
                                           ctypes.c_ulonglong, vp]
     lib.attn_fwd_timeout_test.restype = ci
+    lib.attn_fwd_tail_timeout_test.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                               ctypes.c_ulonglong, vp]
+    lib.attn_fwd_tail_timeout_test.restype = ci
+    lib.attn_fwd_tail_pairs.argtypes = [ci] * 7
+    lib.attn_fwd_tail_pairs.restype = ci
     lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
                                      ci, ci, ci, ci, ci, ci, ci, cf, ci, vp]
     lib.attn_fwd_splitkv.restype = ci
@@ -339,6 +345,32 @@ def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,
                                          float(scale), int(drop_block), int(wait_budget_ns),
                                          _stream_handle(stream)), "attn_fwd_timeout_test")
     return o, lse
+
+
+def fwd_tail_timeout_test(q, k, v, causal: bool, scale: float,
+                          wait_budget_ns: int = 20_000_000, stream=None):
+    """Test hook: runs the forward's split-tail launch with the second CTA of
+    each pair withholding its hand-off, so both CTAs' bounded cluster waits
+    run out (see attn_testing.h).  Returns (o, lse); the device status word
+    then reads ATTN_ERR_TIMEOUT."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(_load().attn_fwd_tail_timeout_test(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              o.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Skv,
+                                              D, int(bool(causal)), float(scale),
+                                              int(wait_budget_ns), _stream_handle(stream)),
+           "attn_fwd_tail_timeout_test")
+    return o, lse
+
+
+def fwd_tail_pairs(B: int, H_q: int, H_kv: int, S_q: int, S_kv: int, D: int, causal: bool) -> int:
+    """Tiles attn_fwd splits across CTA pairs for these sizes on the current
+    device (0: none; -1: invalid sizes or no device)."""
+    return int(_load().attn_fwd_tail_pairs(B, H_q, H_kv, S_q, S_kv, D, int(bool(causal))))
 
 
 def selftest_qk(q, k):

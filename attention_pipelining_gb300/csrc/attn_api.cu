@@ -81,7 +81,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
     return ATTN_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   // R = (H_q / H_kv) * S_q rows per K/V head must fit an int, and so must
   // the number of 256-row work tiles, ceil(R / 256) * B * H_kv
@@ -103,6 +103,19 @@ using namespace attnpipe;
 
 namespace attnpipe {
 
+// scale * log2(e), the factor the kernels apply to the raw scores (their
+// softmax runs in base 2).  It is never zero: the forward's masked scores
+// are infinities whose sign is chosen against the sign of this factor, so
+// it must have one.  A zero (or underflowing) scale runs as the smallest
+// normal float of the same sign: then every scaled score of magnitude below
+// 2^100 is under 2^-26, and its probability rounds to exactly 1, as with a
+// zero scale.
+static float scale_log2_of(float scale) {
+  const float v = (float)((double)scale * 1.4426950408889634);
+  if (v == 0.f) return std::signbit(scale) ? -FLT_MIN : FLT_MIN;
+  return v;
+}
+
 // Fills the kernel parameters (tensor maps over the row-group view).
 static attn_status_t make_params(AttnParams* p, const void* q, const void* k, const void* v,
                                  void* o, float* lse, int B, int H_q, int H_kv, int S_q, int S_kv,
@@ -123,11 +136,7 @@ static attn_status_t make_params(AttnParams* p, const void* q, const void* k, co
   p->causal = causal;
   p->rows_per_group = R;
   p->total_rows = (long long)B * H_q * S_q;
-  // The kernel needs scale_log2 > 0 (a masked score -inf must stay -inf
-  // after scaling).  A zero scale runs as the smallest normal float: then
-  // every scaled score of magnitude below 2^100 is under 2^-26, and its
-  // probability rounds to exactly 1, as with a zero scale.
-  p->scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+  p->scale_log2 = scale_log2_of(scale);
   p->timeout_ns = kDefaultTimeoutNs;
   p->kv_splits = 1;
   p->kv_blocks_per_split = 1 << 30;
@@ -151,7 +160,8 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
                               int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
                               float scale, unsigned long long* trace, int trace_ctas,
                               int trace_blocks, int fault_drop_block,
-                              unsigned long long timeout_ns, attn_stream_t stream) {
+                              unsigned long long timeout_ns, attn_stream_t stream,
+                              int fault_drop_xfer = 0) {
   attn_status_t st = validate(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
   st = check_device();
@@ -164,6 +174,9 @@ static attn_status_t fwd_impl(const void* q, const void* k, const void* v, void*
   p.trace_ctas = trace_ctas;
   p.trace_blocks = trace_blocks;
   p.fault_drop_block = fault_drop_block;
+  p.fault_drop_xfer = fault_drop_xfer;
+  // the hand-off test needs a launch that splits its tail
+  if (fault_drop_xfer && fwd_tail_pairs(p, D) <= 0) return ATTN_ERR_UNSUPPORTED;
   if (launch_attn_fwd(p, D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
@@ -307,7 +320,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   p.Rp = (int)Rp;
   p.groups = B * H_kv;
   p.scale = scale;
-  p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+  p.scale_log2 = scale_log2_of(scale);
   p.timeout_ns = kDefaultTimeoutNs;
   if (launch_attn_bwd(p, D, o, dout, lse, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -782,6 +795,33 @@ attn_status_t attn_fwd_timeout_test(const void* q, const void* k, const void* v,
     return ATTN_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0,
                   drop_block, wait_budget_ns, stream);
+}
+
+attn_status_t attn_fwd_tail_timeout_test(const void* q, const void* k, const void* v, void* o,
+                                         float* lse, int B, int H_q, int H_kv, int S_q, int S_kv,
+                                         int D, int causal, float scale,
+                                         unsigned long long wait_budget_ns,
+                                         attn_stream_t stream) {
+  if (wait_budget_ns < 1000000ull || wait_budget_ns > kDefaultTimeoutNs)
+    return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0, -1,
+                  wait_budget_ns, stream, 1);
+}
+
+int attn_fwd_tail_pairs(int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal) {
+  // the size rules of attn_fwd, with a stand-in address that is never used
+  const void* a = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (validate(a, a, a, a, a, B, H_q, H_kv, S_q, S_kv, D, causal, 1.f) != ATTN_OK) return -1;
+  if (check_device() != ATTN_OK) return -1;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.S_kv = S_kv;
+  p.causal = causal;
+  p.kv_splits = 1;
+  p.n_m_tiles = n_m_tiles_of(H_q, H_kv, S_q);
+  p.groups = B * H_kv;
+  p.num_tiles = p.n_m_tiles * p.groups;
+  return fwd_tail_pairs(p, D);
 }
 
 attn_status_t attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,

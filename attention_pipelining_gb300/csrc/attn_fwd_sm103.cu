@@ -340,6 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::kTmS1 : C::kTmS0);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    // With a negative scale the largest scaled score is the smallest raw
+    // score times the scale, and a masked key is +inf so that its scaled
+    // score is -inf: the row max is then taken over the negated raw scores.
+    const bool neg = sl2 < 0.f;
+    const float sl2_abs = fabsf(sl2);
+    const uint32_t masked_bits = f2u(neg ? INFINITY : -INFINITY);
     uint32_t nblk = 0;  // blocks of sub-tile t so far: the phase of s_full[t]
     uint32_t ntl = 0;   // tiles with sub-tile t so far: row-stat buffer, fin phase
     bool ok = true;
@@ -402,19 +408,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // keys this row may not see drop out of the max
 #pragma unroll
             for (int c = 0; c < 128; ++c)
-              if (c >= lim) s[c] = f2u(-INFINITY);
+              if (c >= lim) s[c] = masked_bits;
           }
-          // row max of the raw scores (4 independent chains of 3-input max)
+          // row max of the raw scores, or of the negated raw scores for a
+          // negative scale (4 independent chains of 3-input max)
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (!neg) {
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
+            for (int c = 0; c < 128; c += 8) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
+              for (int i = 0; i < 4; ++i)
+                mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                mx[i] = max3(mx[i], -u2f(s[c + 2 * i]), -u2f(s[c + 2 * i + 1]));
+            }
           }
           const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          // scale >= 0, so the max of the scaled scores is the scaled max; a
-          // row whose keys are all masked here leaves the running max unchanged
-          const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
+          // the max of the scaled scores is mblk * |scale log2(e)|; a row
+          // whose keys are all masked here leaves the running max unchanged
+          const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2_abs);
           if (j == 0) {
             m_use = m_new;
           } else if (m_new - m_run > kRescaleThreshold) {
@@ -425,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             sScale[t * kBlockM + r] = alpha;
             mbar_arrive(&stats[t]);
           }
-          // A masked score is -inf, and so is its x below (scale_log2 > 0),
-          // so its p is exactly 0 -- unless the row has seen no key yet
+          // A masked score is -inf (+inf for a negative scale), so its x
+          // below is -inf and its p exactly 0 -- unless the row has seen no key yet
           // (m_use = -inf, only possible inside one KV split): then subtract
           // 0 instead, which keeps x = -inf rather than -inf + inf.
           float m_sub = m_use;
@@ -613,7 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
         tc_fence_before_sync();
-        mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), cluster_ctarank() ^ 1u));
+        // (the test of the hand-off's timeout path withholds this arrival)
+        if (!p.fault_drop_xfer)
+          mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), cluster_ctarank() ^ 1u));
         if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) ok = false;
         break;  // the tail round is the last: no tile follows
       }
@@ -978,6 +997,7 @@ namespace {
 std::mutex g_launch_mu;
 bool g_attr_set[2][2][2][64] = {};  // [D == 128][trace][split tail][device]
 int g_sm_count[64] = {};
+int g_tail_clusters[2][64] = {};    // [D == 128][device]: resident clusters of two, + 1 (0: unknown)
 
 // The SM count of the current device and, once per instantiation and
 // device, the kernel's shared-memory attribute.
@@ -1003,6 +1023,71 @@ cudaError_t prepare(int* sms) {
   return cudaSuccess;
 }
 
+// Launch configuration of the split-tail instantiation: clusters of two.
+template <int D>
+cudaLaunchConfig_t tail_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// How many clusters of two CTAs of the split-tail instantiation can be
+// resident at once on the current device (queried once per device).
+template <int D>
+int resident_tail_clusters(int grid) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int sms = 0;
+  if (prepare<D, false, true>(&sms) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_launch_mu);
+  int& cached = g_tail_clusters[D == 128][dev];
+  if (cached == 0) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = tail_config<D>(grid, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_kernel<D, false, true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // a failed query leaves a (non-sticky) error behind: clear it
+      n = 0;
+    }
+    cached = n + 1;
+  }
+  return cached - 1;
+}
+
+// The split-tail plan of a launch of `grid` persistent CTAs: when the last
+// round of whole tiles would leave more than half of the CTAs idle, each of
+// its tiles goes to a pair of CTAs instead (half of its KV blocks each), so
+// the round takes about half a tile.  Non-causal tiles only (with the causal
+// mask the last round holds the shortest tiles), long ones, only when the
+// tiles write O and LSE (a split-KV launch, even of one split, writes
+// partials for its merge), and only when every cluster of two of the grid
+// can be resident at once (else the extra clusters would wait for whole
+// persistent CTAs to finish).  Sets tail_base / tail_pairs (0 = no split).
+template <int D>
+void plan_tail(AttnParams* q, int grid) {
+  q->tail_base = 0;
+  q->tail_pairs = 0;
+  const int kv_blocks = (q->S_kv + kBlockN - 1) / kBlockN;
+  if (q->kv_splits != 1 || q->o_part != nullptr || q->causal || kv_blocks < kSplitTailMinBlocks ||
+      q->num_tiles <= grid || grid % 2 != 0)
+    return;
+  const int rounds = q->num_tiles / grid;
+  const int tail = q->num_tiles - rounds * grid;
+  if (tail <= 0 || tail > grid / 2) return;
+  if (resident_tail_clusters<D>(grid) < grid / 2) return;
+  q->tail_base = rounds * grid;
+  q->tail_pairs = tail;
+}
+
 template <int D, bool kTrace>
 cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
   int sms = 0;
@@ -1016,46 +1101,37 @@ cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
   q.tail_base = 0;
   q.tail_pairs = 0;
   if constexpr (!kTrace) {
-    // Split tail: when the last round of whole tiles would leave more than
-    // half of the CTAs idle, each of its tiles goes to a pair of CTAs instead
-    // (half of its KV blocks each), so the round takes about half a tile.
-    // Clusters of two CTAs, one per SM, all fit at once on this part.
-    // Non-causal tiles only (with the causal mask the last round holds the
-    // shortest tiles), long ones, and only when the tiles write O and LSE
-    // (a split-KV launch, even of one split, writes partials for its merge).
-    const int kv_blocks = (p.S_kv + kBlockN - 1) / kBlockN;
-    if (p.kv_splits == 1 && p.o_part == nullptr && !p.causal &&
-        kv_blocks >= kSplitTailMinBlocks && p.num_tiles > grid && grid % 2 == 0) {
-      const int rounds = p.num_tiles / grid;
-      const int tail = p.num_tiles - rounds * grid;
-      if (tail > 0 && tail <= grid / 2) {
-        q.tail_base = rounds * grid;
-        q.tail_pairs = tail;
-      }
-    }
+    plan_tail<D>(&q, grid);
     if (q.tail_pairs > 0) {
       err = prepare<D, false, true>(&sms);
       if (err != cudaSuccess) return err;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
-      cfg.stream = stream;
       cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cudaLaunchConfig_t cfg = tail_config<D>(grid, stream, attr);
       return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, false, true>, q);
     }
+    // the hand-off test needs a split tail
+    if (p.fault_drop_xfer) return cudaErrorInvalidValue;
   }
   attn_fwd_kernel<D, kTrace, false><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int fwd_tail_pairs(const AttnParams& p, int D) {
+  int sms = 0;
+  AttnParams q = p;
+  if (D == 128) {
+    if (prepare<128, false, false>(&sms) != cudaSuccess || sms <= 0) return -1;
+    plan_tail<128>(&q, p.num_tiles < sms ? p.num_tiles : sms);
+  } else if (D == 64) {
+    if (prepare<64, false, false>(&sms) != cudaSuccess || sms <= 0) return -1;
+    plan_tail<64>(&q, p.num_tiles < sms ? p.num_tiles : sms);
+  } else {
+    return -1;
+  }
+  return q.tail_pairs;
+}
 
 cudaError_t launch_attn_fwd(const AttnParams& p, int D, cudaStream_t stream) {
   if (p.trace || p.fault_drop_block >= 0) {

@@ -67,6 +67,11 @@ struct AttnParams {
   // first softmax warpgroup does not signal "P ready" for this KV block, so
   // the tensor-core issuer's bounded wait runs out.  -1 in normal use.
   int fault_drop_block;
+  // Test of the split tail's hand-off (split-tail instantiation only): when
+  // non-zero, the second CTA of each pair withholds its "partial result
+  // ready" arrival, so both CTAs' bounded cluster waits run out.  0 in normal
+  // use.
+  int fault_drop_xfer;
 };
 
 // Everything the backward kernels read.  Q and dO are viewed as [B*H_kv,
@@ -153,6 +158,10 @@ cudaError_t launch_attn_fwd(const AttnParams& p, int D, cudaStream_t stream);
 // Queues the merge of split-KV partial results into O (bf16) and LSE.
 cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* o, float* lse,
                                    long long rows, int D, int splits, cudaStream_t stream);
+
+// The number of tiles a launch of these parameters on the current device
+// splits across CTA pairs (0: none), or -1 if the device cannot be queried.
+int fwd_tail_pairs(const AttnParams& p, int D);
 
 // Reads (and optionally clears) the device status word of the current device.
 cudaError_t read_device_status(int* status, bool reset);

@@ -47,7 +47,7 @@ typedef void *attn_stream_t;
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID_ARG = 1, /* null pointer, a size <= 0, H_q % H_kv != 0, bad scale */
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, a size <= 0, H_q % H_kv != 0, scale not finite */
   ATTN_ERR_UNSUPPORTED = 2, /* D not 64 or 128, size beyond the kernel's limits, not sm_103 */
   ATTN_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
@@ -63,8 +63,9 @@ typedef enum {
  *   o    [B, H_q, S_q, D]  bf16, device, written
  *   lse  [B, H_q, S_q]     fp32, device, written (natural log)
  *   D in {64, 128}; H_q a multiple of H_kv; every size >= 1;
- *   causal 0 or 1; scale finite and >= 0 (the scores are multiplied by it
- *   before the mask and the softmax; 1/sqrt(D) is the usual choice).
+ *   causal 0 or 1; scale any finite value, negative and zero included (the
+ *   scores are multiplied by it before the mask and the softmax; 1/sqrt(D)
+ *   is the usual choice).
  *
  * All pointers must be 16-byte aligned and must not alias o/lse with inputs.
  * Returns once the kernel is queued; no synchronisation happens inside.
@@ -157,7 +158,10 @@ int attn_splitkv_default_splits(int B, int H_q, int H_kv, int S_q, int S_kv, int
  * exits.  A call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine).  The first call on a device looks up the array's device
  * address once (cudaGetSymbolAddress with that device current) and caches
- * it; make that first call before any stream capture.
+ * it; make that first call before any stream capture.  The cached address
+ * belongs to the device's current context: after cudaDeviceReset on that
+ * device it no longer points at the array, and this entry point must not be
+ * called again in that process (use attn_fwd_splitkv with a workspace).
  *
  * All calls on a device share the one array, which keeps the last call's
  * contents; every partial a call reads is written by that same call, so

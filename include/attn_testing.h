@@ -1,11 +1,11 @@
 /*
- * attn_testing.h -- test hook for the kernel's failure detection.
+ * attn_testing.h -- test hooks for the kernel's failure detection.
  *
  * Every wait inside the fused kernel gives up after a time budget; the CTA
  * then stops, lets its own copies and tensor-core work finish, frees its
  * tensor memory, and records ATTN_ERR_TIMEOUT in the device status word
  * (attn_device_status in attn.h).  The pages describe no failure handling;
- * this hook exists so that path can be tested without faulting the GPU.
+ * these hooks exist so that path can be tested without faulting the GPU.
  *
  * attn_fwd_timeout_test runs the same computation as attn_fwd (same
  * arguments and buffers) in the diagnostic instantiation of the kernel, with
@@ -16,7 +16,24 @@
  * timed-out CTA are unspecified.  `wait_budget_ns` must lie in
  * [1 ms, 2 s]; `drop_block` must be >= 0 (else ATTN_ERR_INVALID_ARG).
  * For tests only.
+ *
+ * attn_fwd_tail_timeout_test does the same for the split tail of attn_fwd (see
+ * attn.h: the last round's tiles split across a cluster of two CTAs).  The
+ * call runs the split-tail launch with one difference: the second CTA of
+ * each pair never signals that its partial result is in its shared memory,
+ * so the first CTA's bounded wait for it runs out after `wait_budget_ns`,
+ * and then the second CTA's wait for the first to have read it.  Both CTAs
+ * unwind, reach the cluster barrier at exit and return; the status word reads
+ * ATTN_ERR_TIMEOUT.  Returns ATTN_ERR_UNSUPPORTED (nothing launched) when
+ * attn_fwd would not split the tail for these sizes on this device;
+ * `wait_budget_ns` must lie in [1 ms, 2 s].  Outputs are unspecified.
+ * For tests only.
+ *
+ * attn_fwd_tail_pairs returns how many tiles attn_fwd splits across CTA
+ * pairs for these sizes on the current device (0 when the tail is not
+ * split), or -1 for invalid sizes or a device that cannot be queried.
  */
+
 #ifndef ATTN_GB300_TESTING_H
 #define ATTN_GB300_TESTING_H
 
@@ -30,6 +47,13 @@ attn_status_t attn_fwd_timeout_test(const void *q, const void *k, const void *v,
                                     float *lse, int B, int H_q, int H_kv, int S_q, int S_kv,
                                     int D, int causal, float scale, int drop_block,
                                     unsigned long long wait_budget_ns, attn_stream_t stream);
+
+attn_status_t attn_fwd_tail_timeout_test(const void *q, const void *k, const void *v, void *o,
+                                         float *lse, int B, int H_q, int H_kv, int S_q, int S_kv,
+                                         int D, int causal, float scale,
+                                         unsigned long long wait_budget_ns, attn_stream_t stream);
+
+int attn_fwd_tail_pairs(int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal);
 
 #ifdef __cplusplus
 }

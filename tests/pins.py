@@ -236,5 +236,31 @@ def pin_library_sdpa(orc) -> list[str]:
     return errs
 
 
+def pin_negative_scale(orc) -> list[str]:
+    """A negative scale: torch's float64 SDPA agrees (a library special case),
+    and negating the scale is the same as negating the keys (the scores are
+    scale * q . k, and negation is exact), bit for bit."""
+    import torch.nn.functional as F
+    errs = []
+    for (B, Hq, Hkv, Sq, Skv, D) in [(1, 2, 2, 33, 47, 16), (2, 4, 2, 40, 40, 32)]:
+        for causal in (False, True):
+            for scale in (-0.3, -2.5):
+                q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, seed=29)
+                o, lse = orc.attn_fwd(q, k, v, causal, scale)
+                # (an explicit boolean mask: torch's is_causal path gives NaN
+                # for a negative scale)
+                mask = torch.ones(Sq, Skv, dtype=torch.bool).tril() if causal else None
+                ref = F.scaled_dot_product_attention(
+                    q.double(), k.double(), v.double(), attn_mask=mask, scale=scale,
+                    enable_gqa=(Hq != Hkv)).numpy()
+                dev = np.abs(o - ref).max()
+                if not dev <= 1e-12:
+                    errs.append(f"SDPA differs by {dev} at scale {scale} causal={causal}")
+                o2, l2 = orc.attn_fwd(q, (-k).contiguous(), v, causal, -scale)
+                if not (np.array_equal(o, o2) and np.array_equal(lse, l2)):
+                    errs.append(f"scale {scale} and keys negated with -scale differ")
+    return errs
+
+
 ALL_PINS = [pin_row_sums, pin_ones, pin_single_key, pin_zero_query, pin_permutation,
-            pin_brute_force, pin_powers_of_two, pin_library_sdpa]
+            pin_brute_force, pin_powers_of_two, pin_library_sdpa, pin_negative_scale]

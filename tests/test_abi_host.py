@@ -68,12 +68,20 @@ def _call(lib, q=A, k=A, v=A, o=A, lse=A, **kw):
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(H_q=0), 1), (dict(H_kv=0), 1), (dict(S_q=0), 1), (dict(S_kv=-3), 1),
     (dict(D=0), 1), (dict(H_q=3, H_kv=2), 1), (dict(causal=2), 1),
-    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-0.5), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=float("-inf")), 1),
     (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2), (dict(B=70000), 2),
     (dict(q=A + 8), 3), (dict(k=A + 2), 3), (dict(v=A + 4), 3), (dict(o=A + 1), 3), (dict(lse=A + 4), 3),
 ])
 def test_validation_rejects_before_launch(lib, kw, code):
     assert _call(lib, **kw) == code
+
+
+@pytest.mark.parametrize("scale", [-0.5, -0.0, 0.0, -1e30])
+def test_validation_accepts_any_finite_scale(lib, scale):
+    # the definition admits any real scale: a negative one passes the scale
+    # check and the call stops at the next rule (a misaligned pointer here),
+    # still before any CUDA call
+    assert _call(lib, scale=scale, o=A + 8) == 3
 
 
 def test_host_entry_rejects_null_host_buffers(lib):

@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: a kernel wait is made to run
-out (one "P ready" signal is withheld, nothing else sets it) with a short wait
-budget; the kernel must return, the device status word must read
-ATTN_ERR_TIMEOUT, and the same CUDA context must keep working."""
+out (a signal is withheld that nothing else sets: one "P ready", or the split
+tail's hand-off between the CTAs of a cluster) with a short wait budget; the
+kernel must return, the device status word must read ATTN_ERR_TIMEOUT, and
+the same CUDA context must keep working."""
 import math
 
 import pytest
@@ -49,3 +50,29 @@ def test_withheld_signal_beyond_last_block_is_harmless():
     assert ap.device_status(reset=True) == 0
     o64, lse64 = oracle.attn_fwd(q, k, v, True, scale)
     assert_parity(o.cpu(), lse.cpu(), o64, lse64, "drop beyond end")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_tail_handoff_runs_out_and_context_survives(D):
+    """The second CTA of each split tail pair withholds its "partial ready"
+    arrival: the first CTA's cluster-scope wait runs out, then the second's
+    wait for the first to have read it; both reach the exit barrier."""
+    q, k, v = make_qkv(1, 40, 40, 1024, 4096, D, seed=23)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 4096, D, False) > 0
+    assert ap.device_status(reset=True) == 0
+    ap.fwd_tail_timeout_test(qd, kd, vd, False, scale, wait_budget_ns=20_000_000)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 5        # ATTN_ERR_TIMEOUT
+    o, lse = ap.attn_fwd(qd, kd, vd, False, scale)
+    torch.cuda.synchronize()
+    assert ap.device_status(reset=True) == 0
+    o64, lse64 = oracle.attn_fwd(q, k, v, False, scale)
+    assert_parity(o.cpu(), lse.cpu(), o64, lse64, f"after hand-off timeout D={D}")
+
+
+def test_split_tail_handoff_test_needs_a_split_tail():
+    q, k, v = make_qkv(1, 2, 2, 512, 512, 64, seed=24)
+    with pytest.raises(ap.AttnError):
+        ap.fwd_tail_timeout_test(q.cuda(), k.cuda(), v.cuda(), False, 0.125)

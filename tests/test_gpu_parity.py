@@ -89,6 +89,33 @@ def test_zero_scale_gives_mean_of_v():
         assert_parity(o, lse, o64, lse64, f"scale=0 causal={causal}")
 
 
+@pytest.mark.parametrize("case", [
+    # B, H_q, H_kv, S_q, S_kv, D, causal, scale
+    (1, 2, 2, 300, 300, 128, False, -0.125),
+    (1, 2, 2, 300, 300, 128, True, -0.125),
+    (2, 8, 2, 512, 512, 64, True, -1.0 / 8),     # grouped heads
+    (1, 4, 1, 77, 1000, 64, False, -0.4),        # a large negative scale, ragged
+    (1, 2, 2, 260, 260, 64, True, -0.0),
+])
+def test_negative_scale(case):
+    """The definition admits any real scale: with a negative one the row max
+    is the smallest raw score times the scale, and masked keys must still
+    drop out."""
+    B, Hq, Hkv, Sq, Skv, D, causal, scale = case
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, D, seed=80 + Sq)
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o64, lse64 = oracle.attn_fwd(q, k, v, causal, scale)
+    assert_parity(o, lse, o64, lse64, f"negative scale {case}")
+
+
+def test_negative_scale_split_tail():
+    """A negative scale through the split tail (the pair merge by LSE)."""
+    q, k, v = make_qkv(1, 40, 40, 1024, 4096, 64, seed=81)
+    o, lse = run_gpu(q, k, v, False, -0.125)
+    o64, lse64 = oracle.attn_fwd(q, k, v, False, -0.125)
+    assert_parity(o, lse, o64, lse64, "negative scale, split tail")
+
+
 def test_deterministic():
     q, k, v = make_qkv(2, 4, 2, 700, 700, 128, seed=9)
     q, k, v = q.cuda(), k.cuda(), v.cuda()
@@ -111,6 +138,34 @@ def test_split_tail_repeatable():
     assert ap.device_status(reset=True) == 0
     for o, lse in outs:
         assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_tail_ragged_rows(D):
+    """A split tail that holds ragged tiles: one head per row group, S_q = 400
+    (a group's second tile has rows 256..399, its second sub-tile only 16
+    rows), 32 KV blocks, and SMs / 2 + 4 heads, so the grid's last round is
+    the last four groups' eight tiles, each split across a CTA pair."""
+    sms = _sms()
+    H, Sq, Skv = sms // 2 + 4, 400, 4096
+    assert ap.fwd_tail_pairs(1, H, H, Sq, Skv, D, False) == 8
+    _check(1, H, H, Sq, Skv, D, False, 1.0, seed=70 + D)
+
+
+def test_split_tail_plan():
+    """The shapes the split-tail tests rely on do split their tail; causal,
+    short-KV and whole-round shapes do not."""
+    sms = _sms()
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 4096, 64, False) == 160 - sms
+    assert ap.fwd_tail_pairs(10, 8, 2, 512, 4096, 64, False) == 160 - sms
+    assert ap.fwd_tail_pairs(1, 32, 32, 16384, 16384, 128, False) == 2048 % sms
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 4096, 64, True) == 0       # causal
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 2048, 64, False) == 0      # 16 KV blocks
+    assert ap.fwd_tail_pairs(1, sms // 2, sms // 2, 512, 4096, 64, False) == 0  # whole rounds
 
 
 def test_side_stream_and_host_entry():
