@@ -104,12 +104,11 @@ using namespace attnpipe;
 namespace attnpipe {
 
 // scale * log2(e), the factor the kernels apply to the raw scores (their
-// softmax runs in base 2).  It is never zero: the forward's masked scores
-// are infinities whose sign is chosen against the sign of this factor, so
-// it must have one.  A zero (or underflowing) scale runs as the smallest
-// normal float of the same sign: then every scaled score of magnitude below
-// 2^100 is under 2^-26, and its probability rounds to exactly 1, as with a
-// zero scale.
+// softmax runs in base 2).  It is never zero: a masked score is an infinity,
+// which must keep its sign after scaling.  A zero (or underflowing) scale
+// runs as the smallest normal float of the same sign: then every scaled
+// score of magnitude below 2^100 is under 2^-26, and its probability rounds
+// to exactly 1, as with a zero scale.
 static float scale_log2_of(float scale) {
   const float v = (float)((double)scale * 1.4426950408889634);
   if (v == 0.f) return std::signbit(scale) ? -FLT_MIN : FLT_MIN;
@@ -136,7 +135,11 @@ static attn_status_t make_params(AttnParams* p, const void* q, const void* k, co
   p->causal = causal;
   p->rows_per_group = R;
   p->total_rows = (long long)B * H_q * S_q;
-  p->scale_log2 = scale_log2_of(scale);
+  // The forward's softmax takes its row max over the raw scores and needs a
+  // positive factor: a negative scale runs as -Q K^T (the QK GEMM negates
+  // its A operand) times |scale|, the same scores.
+  p->neg_scores = std::signbit(scale) ? 1 : 0;
+  p->scale_log2 = scale_log2_of(std::fabs(scale));
   p->timeout_ns = kDefaultTimeoutNs;
   p->kv_splits = 1;
   p->kv_blocks_per_split = 1 << 30;

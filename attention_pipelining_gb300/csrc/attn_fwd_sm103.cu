@@ -83,7 +83,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 // Register split across the four warpgroups (setmaxnreg): softmax x2,
 // correction, load/MMA.  The kernel launches with 128 registers per thread
 // (launch bounds 512 x 1), and the split must fit in that pool.
-constexpr int kRegsSoftmax = 160, kRegsCorrection = 88, kRegsLoadMma = 104;
+constexpr int kRegsSoftmax = 168, kRegsCorrection = 80, kRegsLoadMma = 96;
 static_assert((2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma) * 128 <= 65536 &&
                   kRegsCorrection <= 128 && kRegsLoadMma <= 128,
               "setmaxnreg split exceeds the launch register pool");
@@ -340,12 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::kTmS1 : C::kTmS0);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    // With a negative scale the largest scaled score is the smallest raw
-    // score times the scale, and a masked key is +inf so that its scaled
-    // score is -inf: the row max is then taken over the negated raw scores.
-    const bool neg = sl2 < 0.f;
-    const float sl2_abs = fabsf(sl2);
-    const uint32_t masked_bits = f2u(neg ? INFINITY : -INFINITY);
     uint32_t nblk = 0;  // blocks of sub-tile t so far: the phase of s_full[t]
     uint32_t ntl = 0;   // tiles with sub-tile t so far: row-stat buffer, fin phase
     bool ok = true;
@@ -408,30 +402,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // keys this row may not see drop out of the max
 #pragma unroll
             for (int c = 0; c < 128; ++c)
-              if (c >= lim) s[c] = masked_bits;
+              if (c >= lim) s[c] = f2u(-INFINITY);
           }
-          // row max of the raw scores, or of the negated raw scores for a
-          // negative scale (4 independent chains of 3-input max)
+          // row max of the raw scores (4 independent chains of 3-input max)
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (!neg) {
 #pragma unroll
-            for (int c = 0; c < 128; c += 8) {
+          for (int c = 0; c < 128; c += 8) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                mx[i] = max3(mx[i], -u2f(s[c + 2 * i]), -u2f(s[c + 2 * i + 1]));
-            }
+            for (int i = 0; i < 4; ++i) mx[i] = max3(mx[i], u2f(s[c + 2 * i]), u2f(s[c + 2 * i + 1]));
           }
           const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          // the max of the scaled scores is mblk * |scale log2(e)|; a row
-          // whose keys are all masked here leaves the running max unchanged
-          const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2_abs);
+          // scale_log2 > 0 (a negative scale negates S in the GEMM instead),
+          // so the max of the scaled scores is the scaled max; a row whose
+          // keys are all masked here leaves the running max unchanged
+          const float m_new = (mblk == -INFINITY) ? m_run : fmaxf(m_run, mblk * sl2);
           if (j == 0) {
             m_use = m_new;
           } else if (m_new - m_run > kRescaleThreshold) {
@@ -442,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             sScale[t * kBlockM + r] = alpha;
             mbar_arrive(&stats[t]);
           }
-          // A masked score is -inf (+inf for a negative scale), so its x
-          // below is -inf and its p exactly 0 -- unless the row has seen no key yet
+          // A masked score is -inf, and so is its x below (scale_log2 > 0),
+          // so its p is exactly 0 -- unless the row has seen no key yet
           // (m_use = -inf, only possible inside one KV split): then subtract
           // 0 instead, which keeps x = -inf rather than -inf + inf.
           float m_sub = m_use;
@@ -788,6 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t dv0 = mnmajor_tile_desc<D>(smem_u32(sKV));
       constexpr uint64_t kSlotDesc = C::kTileBytes >> 4;  // start-address step per ring slot
       const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
+      // a negative scale: S = -Q K^T (the GEMM negates A), and the softmax
+      // applies |scale|
+      const bool neg_s = p.neg_scores != 0;
       const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
       // The CTA's KV blocks form one stream over its tiles, b = 0, 1, ...
       // Ring entry 0 holds K of stream block 0; entry e >= 1 holds V of block
@@ -821,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!warp_wait(&q_full[t], nq[t] & 1, sAbort, budget)) { ok = false; break; }
           tc_fence_after_sync();
           if (leader) {
-            issue_qk_gemm<D>(tS[t], dq[t], dk_first);
+            issue_qk_gemm<D>(tS[t], dq[t], dk_first, neg_s);
             tc_commit(&s_full[t]);
             if (n == 1) tc_commit(&q_free[t]);  // the tile's last read of Q_t
           }
@@ -858,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (more) {
               stamp(tr && leader, t ? kEvMmaS1Begin : kEvMmaS0Begin, j + 1);
               if (leader) {
-                issue_qk_gemm<D>(tS[t], dq[t], dk);
+                issue_qk_gemm<D>(tS[t], dq[t], dk, neg_s);
                 tc_commit(&s_full[t]);
                 if (j + 2 == n) tc_commit(&q_free[t]);
               }

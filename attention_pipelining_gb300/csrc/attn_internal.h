@@ -56,7 +56,8 @@ struct AttnParams {
   // the first writes the merged O and LSE.  Off in split-KV launches.
   int tail_base;
   int tail_pairs;
-  float scale_log2;  // scale * log2(e): the softmax runs in base 2
+  float scale_log2;  // |scale| * log2(e) > 0: the softmax runs in base 2
+  int neg_scores;    // 1 for a negative scale: the QK GEMM computes -Q K^T
   unsigned long long timeout_ns;  // budget of any single wait inside the kernel
   // Timeline trace (the trace instantiation only): SM clock stamps of the
   // first tile of each CTA with index < trace_ctas, layout [cta][event][block].

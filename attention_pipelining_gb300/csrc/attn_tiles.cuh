@@ -54,15 +54,19 @@ __device__ __forceinline__ uint64_t mnmajor_tile_desc(uint32_t smem_addr) {
   return make_smem_desc_sw128(smem_addr, (D == 64) ? 1024 : kSlabBytes, 1024);
 }
 
-// S[tmem, 128 x 128 fp32] = Q K^T for one 128-row Q tile and one 128-row K
-// tile, given their K-major tile descriptors.  Both operands are K-major (the
-// head dimension is contiguous): per K step of 16 elements the start advances
+// S[tmem, 128 x 128 fp32] = Q K^T (or -Q K^T) for one 128-row Q tile and one
+// 128-row K tile, given their K-major tile descriptors.  Both operands are
+// K-major (the head dimension is contiguous): per K step of 16 elements the
+// start advances
 // 32 bytes inside a swizzle row, and moves to the next slab every 64
 // elements.  Stride between 8-row groups (SBO) is 1024 bytes; the leading
 // offset is unused for swizzled K-major operands.  Issued by one thread.
 template <int D>
-__device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc) {
-  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 128, false, false);
+__device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc,
+                                              bool negate = false) {
+  // with `negate`, the instruction descriptor's negate-A bit gives -Q K^T
+  const uint32_t idesc =
+      make_idesc_bf16_f32(128, 128, false, false) | (negate ? kIdescNegateA : 0u);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = (uint64_t)(((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4);

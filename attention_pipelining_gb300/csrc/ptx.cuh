@@ -459,6 +459,8 @@ __host__ __device__ constexpr uint64_t make_smem_desc_sw128(uint32_t saddr, uint
 //   bits  4-5   D format (1: f32)
 //   bits  7-9   A format (1: bf16)
 //   bits 10-12  B format (1: bf16)
+//   bit  13     negate A (1: the product uses -A)
+//   bit  14     negate B
 //   bit  15     A major-ness (0: K-major, 1: MN-major)
 //   bit  16     B major-ness (0: K-major, 1: MN-major)
 //   bits 17-22  N >> 3
@@ -468,6 +470,9 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16_f32(uint32_t M, uint32_t 
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
+
+// Negate-A bit of the instruction descriptor above.
+constexpr uint32_t kIdescNegateA = 1u << 13;
 
 // ---------------------------------------------------------------- math
 
