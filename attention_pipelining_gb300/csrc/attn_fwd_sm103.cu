@@ -80,6 +80,17 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 befo
 // +5 % at 128 blocks per tile, none at 16, a loss for short causal tiles)
 constexpr int kSplitTailMinBlocks = 32;
 constexpr uint32_t kFull = 0xffffffffu;
+// Pairs of probabilities out of every 8 whose exp2 runs on the FMA pipe
+// (exp2_poly_x2) instead of MUFU, in unmasked blocks.  0: every exp2 on
+// MUFU.  Measured on GB300 (grouped-query D = 64 workload, 828 TFLOP/s with
+// 0): 1 pair 782, 2 pairs 747, 4 pairs 635 -- the softmax is bound by
+// instruction issue, not by MUFU (whose exp2 rate on this part matches the
+// tensor core's at D = 64), and each pair on the FMA pipe costs about ten
+// issue slots instead of two.
+#ifndef ATTN_POLY_PAIRS
+#define ATTN_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = ATTN_POLY_PAIRS;
 // Register split across the four warpgroups (setmaxnreg): softmax x2,
 // correction, load/MMA.  The kernel launches with 128 registers per thread
 // (launch bounds 512 x 1), and the split must fit in that pool.
@@ -442,8 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               // x = s * scale * log2(e) - m, two lanes per instruction
               float x0, x1;
               f2_unpack(f2_fma(f2_pack(u2f(s[c]), u2f(s[c + 1])), sl2x2, neg_m2), x0, x1);
-              const float p0 = ex2_approx(x0);
-              const float p1 = ex2_approx(x1);
+              float p0, p1;
+              if (!kMasked && i >= 8 - kPolyPairs) {
+                exp2_poly_x2(x0, x1, p0, p1);
+              } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+              }
               l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
               add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);

@@ -528,6 +528,35 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x0 and 2^x1 on the FMA pipe (no MUFU), for x in [-126, 8]; below -126
+// the argument is clamped (the polynomial value, below 2 and at least 2^-1/2,
+// then keeps an exponent field >= 0 after 126 is subtracted: a result of at
+// most 2^-125, finite and non-negative).  Cody-Waite
+// split x = n + r with n = rint(x) (adding and subtracting 1.5 * 2^23 rounds
+// to the nearest integer) and r in [-1/2, 1/2]; 2^r by a degree-3
+// polynomial fitted here by Remez exchange for minimum relative error on
+// [-1/2, 1/2] (levelled relative error 7.5e-5, the same for the fp32
+// evaluation below on [-125, 8]);
+// 2^n by adding n to the exponent field (n sits in the low bits of the
+// rounding sum t, so t << 23 is n << 23).
+__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& y0, float& y1) {
+  constexpr float kC0 = 0.99992805719375610f, kC1 = 0.69326096773147583f;
+  constexpr float kC2 = 0.24261112511157990f, kC3 = 0.05517166852951050f;
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+  const uint64_t t = f2_add(x, f2_pack(kRound, kRound));
+  const uint64_t n = f2_add(t, f2_pack(-kRound, -kRound));
+  const uint64_t r = f2_fma(n, f2_pack(-1.f, -1.f), x);
+  uint64_t q = f2_fma(f2_pack(kC3, kC3), r, f2_pack(kC2, kC2));
+  q = f2_fma(q, r, f2_pack(kC1, kC1));
+  q = f2_fma(q, r, f2_pack(kC0, kC0));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
 // Packs two floats into bf16x2 (round to nearest even): `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
