@@ -123,7 +123,8 @@ static attn_status_t make_params(AttnParams* p, const void* q, const void* k, co
   const int R = (H_q / H_kv) * S_q;
   if (!encode_bf16_map_3d(&p->tm_q, q, D, R, (uint64_t)B * H_kv, 128) ||
       !encode_bf16_map_3d(&p->tm_k, k, D, S_kv, (uint64_t)B * H_kv, 128) ||
-      !encode_bf16_map_3d(&p->tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128))
+      !encode_bf16_map_3d(&p->tm_v, v, D, S_kv, (uint64_t)B * H_kv, 128) ||
+      !encode_bf16_map_3d(&p->tm_o, o, D, R, (uint64_t)B * H_kv, 32))
     return ATTN_ERR_CUDA;
   p->o = o;
   p->lse = lse;

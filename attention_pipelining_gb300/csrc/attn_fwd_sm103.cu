@@ -118,9 +118,16 @@ struct Cfg {
   static constexpr int kOffRowSumP = kOffRowSum + 4 * 128 * 4;  // float [2][2][128]: sum of bf16(p)
   static constexpr int kOffRowMax = kOffRowSumP + 4 * 128 * 4;  // float [2][2][128]
   static constexpr int kOffMisc = kOffRowMax + 4 * 128 * 4;     // tmem base, abort flag
-  // timeline stamps of the trace instantiation, uint64 [event][block]
-  static constexpr int kOffTrace = kOffMisc + 16;
-  static constexpr int kSmemBytes = kOffTrace + kNumTraceEvents * kMaxTraceBlocks * 8 + 1024;
+  // One region, 1024-byte aligned, used by one of two instantiations: the
+  // trace instantiation's timeline stamps, uint64 [event][block]; or the
+  // epilogue's O staging, one [32 rows x 64 columns] bf16 slab per
+  // correction warp in the TMA 128-byte swizzle (4 x 4 KB)
+  static constexpr int kOffTrace = (kOffMisc + 16 + 1023) / 1024 * 1024;
+  static constexpr int kOffStage = kOffTrace;
+  static constexpr int kStageBytes = 4 * 32 * 128;
+  static constexpr int kTraceBytes = kNumTraceEvents * kMaxTraceBlocks * 8;
+  static constexpr int kSmemBytes =
+      kOffTrace + (kTraceBytes > kStageBytes ? kTraceBytes : kStageBytes) + 1024;
   // tensor memory columns
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
@@ -329,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tma_prefetch_map(&p.tm_q);
     tma_prefetch_map(&p.tm_k);
     tma_prefetch_map(&p.tm_v);
+    if (!kTrace) tma_prefetch_map(&p.tm_o);
   }
   if (warp == 12) {
     tmem_alloc(sTmemBase, C::kTmemCols);
@@ -658,64 +666,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int rho = cur.m0 + t * kBlockM + r;
           // The tensor-memory loads are warp-wide; only the stores depend on
           // whether the row exists.
-          if (cur.pair == 0) {
-            // First KV half of a split tail tile: merge with the partner's
-            // partial (in its shared memory; see the sender above) by the
-            // two halves' log-sum-exps, then write O and LSE.
+          //
+          // First KV half of a split tail tile (pair 0): the output merges
+          // this half with the partner's partial (in the partner's shared
+          // memory; see the sender above) by the two halves' log-sum-exps:
+          // O = w0 O_own + w1 O_partner.  Otherwise w0 = 1 / l, w1 = 0.
+          const bool merge = (cur.pair == 0);
+          float w0 = inv_l, w1 = 0.f, lse_out = lse_row;
+          uint32_t prow = 0;
+          if (merge) {
             if (t == 0 && !warp_wait_cluster(xfer_full, 0, sAbort, budget)) {
               ok = false;
               break;
             }
             const uint32_t peer = cluster_ctarank() ^ 1u;
-            const uint32_t prow =
-                mapa_shared(smem_u32(sKV), peer) + (uint32_t)((t * kBlockM + r) * D * 4);
+            prow = mapa_shared(smem_u32(sKV), peer) + (uint32_t)((t * kBlockM + r) * D * 4);
             const float l1 =
                 ld_shared_cluster_f32(mapa_shared(smem_u32(sQ), peer) + (uint32_t)((t * kBlockM + r) * 4));
             const float l0 = empty ? -INFINITY : m + log2f(l);
             const float mx = fmaxf(l0, l1);
-            float w0 = 0.f, w1 = 0.f, lse_m = -INFINITY;
+            w0 = 0.f;
+            lse_out = -INFINITY;
             if (mx > -INFINITY) {
               const float e0 = ex2_approx(l0 - mx), e1 = ex2_approx(l1 - mx);
               const float inv = 1.f / (e0 + e1);
               w0 = e0 * inv * inv_l;  // this half's O is unnormalised in tensor memory
               w1 = e1 * inv;
-              lse_m = (mx + log2f(e0 + e1)) * 0.69314718055994530942f;
+              lse_out = (mx + log2f(e0 + e1)) * 0.69314718055994530942f;
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                  ((size_t)cur.zkv * R + rho) * D);
-            // 16 columns at a time (the correction warpgroup's register budget)
-#pragma unroll 1
-            for (int ch = 0; ch < D / 16; ++ch) {
-              uint32_t o[16];
-              tmem_ld_x16(tO + ch * 16, o);
-              tmem_ld_wait();
-              reg_after_wait(o);
-#pragma unroll
-              for (int qd = 0; qd < 4; ++qd) {
-                const int cc = ch * 4 + qd;  // 16-byte piece of the row
-                const float4 pv = ld_shared_cluster_v4(prow + 16u * (uint32_t)(cc ^ (r & 7)));
-                // w1 = 0 (an empty partner half) must not meet its unset values
-                const float a[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float own = u2f(o[qd * 4 + e]) * w0;
-                  o[qd * 4 + e] = f2u(w1 > 0.f ? fmaf(w1, a[e], own) : own);
-                }
-              }
-              if (rho < R) {
-#pragma unroll
-                for (int qd = 0; qd < 2; ++qd) {
-                  uint4 val;
-                  val.x = pack_bf16x2(u2f(o[qd * 8 + 0]), u2f(o[qd * 8 + 1]));
-                  val.y = pack_bf16x2(u2f(o[qd * 8 + 2]), u2f(o[qd * 8 + 3]));
-                  val.z = pack_bf16x2(u2f(o[qd * 8 + 4]), u2f(o[qd * 8 + 5]));
-                  val.w = pack_bf16x2(u2f(o[qd * 8 + 6]), u2f(o[qd * 8 + 7]));
-                  dst[ch * 2 + qd] = val;
-                }
-              }
-            }
-            if (rho < R) p.lse[(size_t)cur.zkv * R + rho] = lse_m;
-          } else if (p.o_part != nullptr) {
+          }
+          if (p.o_part != nullptr) {
             // split-KV partial: fp32 O normalised within the split, and its LSE
             const size_t row = (size_t)cur.split * p.total_rows + (size_t)cur.zkv * R + rho;
             float4* dst = reinterpret_cast<float4*>(p.o_part + row * D);
@@ -734,9 +714,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               }
             }
             if (rho < R) p.lse_part[row] = lse_row;
+          } else if constexpr (!kTrace) {
+            // bf16 O through shared memory and TMA: per 64-column slab, each
+            // warp writes its 32 rows into its own staging slab (128-byte
+            // swizzle: 16-byte piece c of row r at piece c ^ (r % 8)), then
+            // one lane stores the slab with one TMA copy (rows past R are
+            // clipped by the tensor map).  The slab is reused once the
+            // previous copy has read it.
+            uint8_t* stage = smem + C::kOffStage + q4 * 4096;
+            const uint32_t srow = smem_u32(stage) + (uint32_t)lane * 128u;
+#pragma unroll 1
+            for (int h = 0; h < D / 64; ++h) {
+              if (lane == 0) tma_store_wait_read<0>();
+              __syncwarp();
+#pragma unroll 1
+              for (int q16 = 0; q16 < 4; ++q16) {
+                uint32_t o[16];
+                tmem_ld_x16(tO + h * 64 + q16 * 16, o);
+                tmem_ld_wait();
+                reg_after_wait(o);
+                if (merge) {
+#pragma unroll
+                  for (int qd = 0; qd < 4; ++qd) {
+                    const int cc = h * 16 + q16 * 4 + qd;  // 16-byte fp32 piece of the partner's row
+                    const float4 pv = ld_shared_cluster_v4(prow + 16u * (uint32_t)(cc ^ (lane & 7)));
+                    // w1 = 0 (an empty partner half) must not meet its unset values
+                    const float a[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const float own = u2f(o[qd * 4 + e]) * w0;
+                      o[qd * 4 + e] = f2u(w1 > 0.f ? fmaf(w1, a[e], own) : own);
+                    }
+                  }
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i] = f2u(u2f(o[i]) * w0);
+                }
+#pragma unroll
+                for (int qd = 0; qd < 2; ++qd) {
+                  const int c = q16 * 2 + qd;  // 16-byte piece of the slab row
+                  st_shared_v4(srow + 16u * (uint32_t)(c ^ (lane & 7)),
+                               pack_bf16x2(u2f(o[qd * 8 + 0]), u2f(o[qd * 8 + 1])),
+                               pack_bf16x2(u2f(o[qd * 8 + 2]), u2f(o[qd * 8 + 3])),
+                               pack_bf16x2(u2f(o[qd * 8 + 4]), u2f(o[qd * 8 + 5])),
+                               pack_bf16x2(u2f(o[qd * 8 + 6]), u2f(o[qd * 8 + 7])));
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&p.tm_o, stage, h * 64, cur.m0 + t * kBlockM + q4 * 32, cur.zkv);
+                tma_store_commit();
+              }
+            }
+            if (rho < R) p.lse[(size_t)cur.zkv * R + rho] = lse_out;
           } else {
-            // bf16 O straight from registers: each thread writes its own row
-            // in 16-byte pieces
+            // (trace instantiation, whose timeline stamps use the staging
+            // region, and which never splits a tail) bf16 O straight from
+            // registers: each thread writes its own row in 16-byte pieces
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                                   ((size_t)cur.zkv * R + rho) * D);
 #pragma unroll
@@ -976,6 +1011,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
 
   // ------------------------------------------------------------ teardown
+  // the epilogue's TMA stores are complete before the CTA exits
+  if (!kTrace && wg == 2 && lane == 0) tma_store_wait_all();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();

@@ -18,6 +18,7 @@ struct AttnParams {
   CUtensorMap tm_q;  // Q as [B*H_kv, R, D], box {64, 128, 1}, 128-byte swizzle (load)
   CUtensorMap tm_k;  // K as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
   CUtensorMap tm_v;  // V as [B*H_kv, S_kv, D], box {64, 128, 1} (load)
+  CUtensorMap tm_o;  // O as [B*H_kv, R, D], box {64, 32, 1}, 128-byte swizzle (store)
   void* o;           // [B, H_q, S_q, D] bf16 (row rho of group z at (z * R + rho) * D)
   float* lse;        // [B, H_q, S_q]
   int B, H_q, H_kv, S_q, S_kv, causal;
