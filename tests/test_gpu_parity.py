@@ -288,6 +288,33 @@ def test_full_size_sampled_rows(name):
     assert_parity(og, lg, o64, lse64, name)
 
 
+FULL_HEAD = [n for n in ("long_b1_h32_s16384_d128", "long_causal_b1_h32_s16384_d128",
+                         "causal_b2_h16_s8192_d128", "batched_b4_h16_s2048_d128",
+                         "gqa_b8_hq32_hkv8_s4096_d64_k3", "single_head_b1_h1_s256_d64")]
+
+
+@pytest.mark.parametrize("name", FULL_HEAD)
+def test_full_size_one_whole_head(name):
+    """Full-size workloads: every row of one query head, element by element.
+    The head is the last one of the last batch entry: its tiles come last in
+    the tile list, so on the non-causal long sequence it is wholly inside the
+    split tail (every one of its tiles split across a CTA pair), and on the
+    grouped-query shape it is the last head of the last KV group."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    if name == "long_b1_h32_s16384_d128":
+        tiles = (w.H_q * w.S_q // 256)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        tail = ap.fwd_tail_pairs(w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.D, w.causal)
+        assert tail == tiles % sms and tail >= w.S_q // 256   # the last head is all tail
+    b, h = w.B - 1, w.H_q - 1
+    first = (b * w.H_q + h) * w.S_q
+    rows = np.arange(first, first + w.S_q)
+    o64, lse64 = oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
+    assert_parity(o[b, h], lse[b, h], o64.reshape(w.S_q, w.D), lse64.reshape(w.S_q), name)
+
+
 def test_trace_instantiation_matches_and_stamps():
     """The trace instantiation computes the same result and stamps every role
     (S = 512: every traced tile has both 128-row sub-tiles)."""
