@@ -126,10 +126,23 @@ struct Cfg {
   static constexpr int kOffStage = kOffTrace;
   static constexpr int kStageBytes = 4 * 32 * 128;
   static constexpr int kTraceBytes = kNumTraceEvents * kMaxTraceBlocks * 8;
-  static constexpr int kSmemBytes =
-      kOffTrace + (kTraceBytes > kStageBytes ? kTraceBytes : kStageBytes) + 1024;
+  static constexpr int kSmemEnd0 =
+      (kOffTrace + (kTraceBytes > kStageBytes ? kTraceBytes : kStageBytes) + 1023) / 1024 * 1024;
+  static constexpr int kOnesBytes = (D == 64) ? kSlabBytes : 0;  // one [128 x 64] bf16 atom of ones
+  static constexpr int kSmemBytes = kSmemEnd0 + kOnesBytes + 1024;
+  // Row sums on the tensor core (D = 64, where tensor memory has room): the
+  // PV GEMM runs with N = D + 16 against [V | ones], so columns D .. D + 15
+  // of O_t accumulate the sum of the bf16 probabilities the GEMM consumed,
+  // with exactly O's weights and rescales.  The ones are a constant slab of
+  // one 64-column atom in shared memory, reached from every V slot through
+  // the descriptor's leading-dimension offset.
+  static constexpr bool kSumCol = (D == 64);
+  static constexpr int kOCols = D + (kSumCol ? 16 : 0);
+  static constexpr int kOffOnes = kSmemEnd0;  // 1024-aligned, after the staging / trace region
+  static_assert(kOffOnes % 1024 == 0 && kOffOnes - kOffKV < (1 << 18),
+                "the ones atom's offset from every V slot fits the descriptor's LBO field");
   // tensor memory columns
-  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
+  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + kOCols;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   // a split tail tile's partial result, [sub-tile][row][D] fp32, fits in
@@ -332,6 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     *sAbort = 0;
     fence_mbar_init();
   }
+  if constexpr (C::kSumCol) {
+    // the constant ones atom of [V | ones] (bf16 1.0 = 0x3f80), written
+    // before the tensor core reads it (async proxy: fenced below)
+    uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
+    for (int i = threadIdx.x; i < C::kOnesBytes / 16; i += kThreads)
+      ones[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+    fence_proxy_async_smem();
+  }
   if (warp == 13 && lane == 0) {
     tma_prefetch_map(&p.tm_q);
     tma_prefetch_map(&p.tm_k);
@@ -380,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // Two row sums: l_run of the fp32 probabilities (for the LSE), and
       // lp_run of the bf16-rounded probabilities that the PV GEMM actually
       // consumes, so O is normalised by the same weights it was accumulated
-      // with.
+      // with (with the sum column the tensor core accumulates the latter in
+      // O_t itself, and lp_run stays unused).
       float m_run = -INFINITY;
       float l_run = 0.f;
       float lp_run = 0.f;
@@ -470,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               }
               l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
-              add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);
+              if constexpr (!C::kSumCol)
+                add_bf16x2_to_f32(lp[(2 * i) & 3], lp[(2 * i + 1) & 3], pk[i]);
             }
             tmem_st_x8(tS + ch * 8, pk);
           }
@@ -565,6 +588,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
               tmem_st_x32(tO + ch * 32, o);
             }
+            if constexpr (C::kSumCol) {
+              uint32_t o[16];
+              tmem_ld_x16(tO + D, o);
+              tmem_ld_wait();
+              reg_after_wait(o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+              tmem_st_x16(tO + D, o);
+            }
             tmem_st_wait();
           }
           tc_fence_before_sync();
@@ -607,6 +639,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             lmax[t] = sRowMax[sb];
           }
           tc_fence_after_sync();
+          if constexpr (C::kSumCol) {
+            // the sum of the bf16 probabilities, from O_t's sum columns
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t < n_sub && ok) {
+                uint32_t v = tmem_ld_x1(tmem + lane_base + (t ? C::kTmO1 : C::kTmO0) + D);
+                tmem_ld_wait();
+                asm volatile("" : "+r"(v));
+                lpsum[t] = u2f(v);
+              }
+            }
+          }
         }
         if (!ok) break;
         // the ring and the Q buffer were last written by TMA and read by the
@@ -656,7 +700,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int sb = (buf * 2 + t) * kBlockM + r;
           const float l = sRowSum[sb];
           const float m = sRowMax[sb];
-          const float lp = sRowSumP[sb];
+          float lp = sRowSumP[sb];
+          if constexpr (C::kSumCol) {
+            // the sum of the bf16 probabilities, from O_t's sum columns
+            uint32_t v = tmem_ld_x1(tmem + lane_base + (t ? C::kTmO1 : C::kTmO0) + D);
+            tmem_ld_wait();
+            asm volatile("" : "+r"(v));
+            lp = u2f(v);
+          }
           // a row with no visible key (possible only within one KV split)
           // has l = 0: its partial result is O = 0, LSE = -inf
           const bool empty = !(lp > 0.f);
@@ -879,7 +930,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             break;
           }
           ++e_next;
-          const uint64_t dv = dv0 + (uint64_t)((2 * st + C::kSlots - 1) % C::kSlots) * kSlotDesc;
+          const uint32_t vslot = (2 * st + C::kSlots - 1) % C::kSlots;
+          uint64_t dv = dv0 + (uint64_t)vslot * kSlotDesc;
+          if constexpr (C::kSumCol) {
+            // [V | ones]: the ones atom sits at a fixed place above the ring,
+            // so each V slot has its own leading offset to it
+            const uint32_t va = smem_u32(sKV) + vslot * C::kTileBytes;
+            dv = make_smem_desc_sw128(va, smem_u32(smem + C::kOffOnes) - va, 1024);
+          }
           const uint64_t dk = dk0 + (uint64_t)(2 * st) * kSlotDesc;
           // per sub-tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}^T
 #pragma unroll
@@ -889,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tc_fence_after_sync();
             stamp(tr && leader, t ? kEvMmaPV1Begin : kEvMmaPV0Begin, j);
             if (leader) {
-              issue_pv_gemm<D>(tO[t], tS[t], dv, j > 0);
+              issue_pv_gemm<D, C::kOCols>(tO[t], tS[t], dv, j > 0);
               if (!more) tc_commit(&pv_done[t]);  // the epilogue waits for the last PV only
             }
             stamp(tr && leader, t ? kEvMmaPV1 : kEvMmaPV0, j);

@@ -81,10 +81,16 @@ __device__ __forceinline__ void issue_qk_gemm(uint32_t s_tmem, uint64_t q_desc, 
 // bytes; the 8-row groups along K are 1024 bytes apart (SBO); the 64-column
 // slabs along N are one slab apart (LBO).  `accumulate` = false overwrites
 // O.  Issued by one thread.
-template <int D>
+//
+// With N > D (a multiple of 16 up to D + 64), B is [V | W]: the columns
+// past D come from the 64-column atom at the descriptor's leading offset
+// from V (the attention kernel's constant ones, which make those columns of
+// O the row sums of P).
+template <int D, int N = D>
 __device__ __forceinline__ void issue_pv_gemm(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
+  static_assert(N % 16 == 0 && N >= D && N <= D + 64, "PV GEMM width");
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, N, false, true);
 #pragma unroll
   for (int kk = 0; kk < kTileRows / 16; ++kk) {
     mma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)((kk * 2048) >> 4), idesc,
