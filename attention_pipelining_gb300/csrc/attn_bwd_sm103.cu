@@ -81,6 +81,48 @@ __device__ __forceinline__ void issue_qk_half(uint32_t c_tmem, uint64_t a_desc, 
   }
 }
 
+// The same product with A in tensor memory: a [128 x D] bf16 tile copied
+// there once (row i in lane i, elements 2c and 2c + 1 in column c, as the
+// tensor core reads an A operand).  Only B is then read from shared memory,
+// so these N = 64 products run at the tensor core's rate instead of at the
+// rate shared memory can feed both operands.
+template <int D>
+__device__ __forceinline__ void issue_qk_half_ts(uint32_t c_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 int h) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64, false, false);
+  const uint64_t b_half = b_desc + (uint64_t)((h * 64 * 128) >> 4);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4);
+    mma_ts(c_tmem, a_tmem + kk * 8, b_half + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Copies a [128 x D] bf16 tile from shared memory (the TMA 128-byte swizzle:
+// 16-byte piece c of row r at piece c ^ (r % 8) of its 64-column slab) into
+// tensor memory as an A operand (D / 2 columns from `t_col`); thread = row
+// = lane of the warp's quadrant (lane_base).  Whole warp.
+template <int D>
+__device__ __forceinline__ void copy_tile_to_tmem(const uint8_t* tile, uint32_t t_col, int row) {
+  const uint32_t base = smem_u32(tile) + (uint32_t)row * 128u;
+#pragma unroll
+  for (int sl = 0; sl < D / 64; ++sl) {
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t a, b, cc, d;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                   : "r"(base + (uint32_t)(sl * kSlabBytes) + 16u * (uint32_t)(c ^ (row & 7))));
+      w[4 * c + 0] = a;
+      w[4 * c + 1] = b;
+      w[4 * c + 2] = cc;
+      w[4 * c + 3] = d;
+    }
+    tmem_st_x32(t_col + sl * 32, w);
+  }
+}
+
 // Acc[tmem, 128 x D fp32] (+)= A_h B_h: A_h [128 x 64] bf16 in tensor memory,
 // two per column, written by the elementwise warpgroups (warpgroup w's 32
 // elements at columns 32w .. 32w + 15 from `a_tmem`); B_h rows 64h..64h+63
@@ -119,12 +161,17 @@ struct BwdCfg {
   static constexpr int kOffDO = kTileBytes;
   static constexpr int kOffKVRing = 2 * kTileBytes;
   static constexpr int kOffBarQ = kOffKVRing + kKVStages * 2 * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], sp_full[2], ds_ready[2], acc_done, drain
-  static constexpr int kNumBarsQ = 2 * kKVStages + 7;
+  // q_full, kv_full[S], kv_empty[S], sp_full[2], ds_ready[2], acc_done, drain,
+  // qt_ready (Q and dO copied into tensor memory)
+  static constexpr int kNumBarsQ = 2 * kKVStages + 8;
   static constexpr int kOffMiscQ = kOffBarQ + kNumBarsQ * 8;
   static constexpr int kSmemQ = kOffMiscQ + 16 + 1024;
-  // tensor memory: S (or S^T) [0,128), dP [128,256), accumulators after
+  // tensor memory: S (or S^T) [0,128), dP [128,256), accumulators after;
+  // the dQ kernel keeps Q and dO as A operands (D / 2 columns each) after its
+  // one accumulator
   static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
+  static constexpr uint32_t kTmQt = 256 + D, kTmDOt = 256 + D + D / 2;
+  static_assert(kTmDOt + D / 2 <= 512, "tensor memory budget of the dQ kernel");
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemKV <= 227 * 1024 && kSmemQ <= 227 * 1024, "shared memory budget");
 };
@@ -577,6 +624,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
   uint64_t* ds_ready = sp_full + 2;             // [half]: dS of the half stored
   uint64_t* acc_done = sp_full + 4;
   uint64_t* drain = sp_full + 5;
+  uint64_t* qt_ready = sp_full + 6;             // Q and dO copied into tensor memory
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscQ);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscQ + 4);
   const int warp = threadIdx.x >> 5;
@@ -623,6 +671,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(qt_ready, 2 * 128);
     *sAbort = 0;
     fence_mbar_init();
   }
@@ -653,7 +702,15 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     const int key_limit = p.causal ? min(p.S_kv, pos + 1) : p.S_kv;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    bool ok = true;
+    // Q (warpgroup 0) and dO (warpgroup 1) into tensor memory, the A
+    // operands of every S and dP product of this CTA
+    bool ok = warp_wait_b(q_full, 0, sAbort, budget);
+    if (ok) {
+      copy_tile_to_tmem<D>(w == 0 ? sQ : sDO, tmem + lane_base + (w == 0 ? C::kTmQt : C::kTmDOt), r);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(qt_ready);
+    }
     for (int j = 0; j < n_kb && ok; ++j) {
       const int kb0 = j * kRows;
       const bool masked = !row_ok || (kb0 + kRows > key_limit);
@@ -734,13 +791,17 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dq_kernel(const __grid_
     const uint64_t dQd = kmajor_tile_desc(smem_u32(sQ));
     const uint64_t dOd = kmajor_tile_desc(smem_u32(sDO));
     const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP, tdQ = tmem + C::kTmAcc0;
-    bool ok = warp_wait_b(q_full, 0, sAbort, budget);
-    // S and dP of half h of key block j (its K / V stage is loaded)
+    const uint32_t tQt = tmem + C::kTmQt, tDOt = tmem + C::kTmDOt;
+    (void)dQd;
+    (void)dOd;
+    bool ok = warp_wait_b(qt_ready, 0, sAbort, budget);
+    // S and dP of half h of key block j (its K / V stage is loaded), with Q
+    // and dO read from tensor memory
     auto issue_sp = [&](int j, int h) {
       const int s = j % C::kKVStages;
       if (leader) {
-        issue_qk_half<D>(tS + 64 * h, dQd, kmajor_tile_desc(smem_u32(stage_k(s))), h);
-        issue_qk_half<D>(tDP + 64 * h, dOd, kmajor_tile_desc(smem_u32(stage_v(s))), h);
+        issue_qk_half_ts<D>(tS + 64 * h, tQt, kmajor_tile_desc(smem_u32(stage_k(s))), h);
+        issue_qk_half_ts<D>(tDP + 64 * h, tDOt, kmajor_tile_desc(smem_u32(stage_v(s))), h);
         tc_commit(&sp_full[h]);
       }
     };
