@@ -151,8 +151,12 @@ struct BwdCfg {
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQRing = 2 * kTileBytes;
   static constexpr int kOffBarKV = kOffQRing + kQStages * kQStageBytes;
-  // kv_full, q_full[S], q_empty[S], sp_full[2], ps_ready[2], acc_done, drain
-  static constexpr int kNumBarsKV = 2 * kQStages + 7;
+  // kv_full, q_full[S], q_empty[S], sp_full[2], ps_ready[2], acc_done, drain,
+  // kt_ready (K and V copied into tensor memory; D = 64)
+  static constexpr int kNumBarsKV = 2 * kQStages + 8;
+  // dK/dV kernel at D = 64: K and V as tensor-memory A operands too (D / 2
+  // columns each after the two accumulators; at D = 128 there is no room)
+  static constexpr bool kKVinTmem = (D == 64);
   static constexpr int kOffMiscKV = kOffBarKV + kNumBarsKV * 8;
   static constexpr int kSmemKV = kOffMiscKV + 16 + 1024;
   // dQ kernel: Q, dO, then a ring of (K, V) stages
@@ -172,6 +176,9 @@ struct BwdCfg {
   static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
   static constexpr uint32_t kTmQt = 256 + D, kTmDOt = 256 + D + D / 2;
   static_assert(kTmDOt + D / 2 <= 512, "tensor memory budget of the dQ kernel");
+  static constexpr uint32_t kTmKt = 256 + 2 * D, kTmVt = 256 + 2 * D + D / 2;
+  static_assert(!kKVinTmem || (kTmKt < kTmVt && kTmVt + D / 2 <= 512),
+                "tensor memory budget of the dK/dV kernel");
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemKV <= 227 * 1024 && kSmemQ <= 227 * 1024, "shared memory budget");
 };
@@ -294,6 +301,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   uint64_t* ps_ready = sp_full + 2;            // [half]: P^T, dS^T of the half stored
   uint64_t* acc_done = sp_full + 4;
   uint64_t* drain = sp_full + 5;
+  uint64_t* kt_ready = sp_full + 6;            // K and V copied into tensor memory (D = 64)
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscKV);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscKV + 4);
   const int warp = threadIdx.x >> 5;
@@ -330,6 +338,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(kt_ready, 2 * 128);
     *sAbort = 0;
     fence_mbar_init();
   }
@@ -363,6 +372,19 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     bool ok = true;
+    if constexpr (C::kKVinTmem) {
+      // K (warpgroup 0) and V (warpgroup 1) into tensor memory, the A
+      // operands of every S^T and dP^T product of this CTA
+      if (n_work > 0) {
+        ok = warp_wait_b(kv_full, 0, sAbort, budget);
+        if (ok) {
+          copy_tile_to_tmem<D>(w == 0 ? sK : sV, tmem + lane_base + (w == 0 ? C::kTmKt : C::kTmVt), r);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(kt_ready);
+        }
+      }
+    }
     int n = 0;
     for (int qb = 0; qb < n_qb && ok; ++qb) {
       const int r0 = qb * kRows;
@@ -510,13 +532,20 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     const uint64_t dV = kmajor_tile_desc(smem_u32(sV));
     const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP;
     const uint32_t tdV = tmem + C::kTmAcc0, tdK = tmem + C::kTmAcc1;
-    bool ok = n_work > 0 && warp_wait_b(kv_full, 0, sAbort, budget);
-    // S^T and dP^T of half h of work item n (its Q / dO stage is loaded)
+    bool ok = n_work > 0 &&
+              warp_wait_b(C::kKVinTmem ? kt_ready : kv_full, 0, sAbort, budget);
+    // S^T and dP^T of half h of work item n (its Q / dO stage is loaded);
+    // at D = 64 K and V are read from tensor memory
     auto issue_sp = [&](int n, int h) {
       const int s = n % C::kQStages;
       if (leader) {
-        issue_qk_half<D>(tS + 64 * h, dK, kmajor_tile_desc(smem_u32(stage_q(s))), h);
-        issue_qk_half<D>(tDP + 64 * h, dV, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+        if constexpr (C::kKVinTmem) {
+          issue_qk_half_ts<D>(tS + 64 * h, tmem + C::kTmKt, kmajor_tile_desc(smem_u32(stage_q(s))), h);
+          issue_qk_half_ts<D>(tDP + 64 * h, tmem + C::kTmVt, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+        } else {
+          issue_qk_half<D>(tS + 64 * h, dK, kmajor_tile_desc(smem_u32(stage_q(s))), h);
+          issue_qk_half<D>(tDP + 64 * h, dV, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+        }
         tc_commit(&sp_full[h]);
       }
     };
