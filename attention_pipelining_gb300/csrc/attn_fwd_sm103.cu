@@ -44,12 +44,14 @@
 // Split tail (the kTail instantiation, launched as clusters of two CTAs):
 // when the grid's last round would leave more than half of the CTAs idle,
 // each of its tiles is split across a CTA pair, half of the KV blocks each.
-// Both halves run as ordinary tiles; at the end the second CTA writes its
-// normalised fp32 partial O and base-2 log-sum-exp into its own idle K/V
-// ring and Q buffer and arrives on the first CTA's xfer_full (remote
-// mbarrier arrivals, release at cluster scope); the first reads them through
-// distributed shared memory, merges them with its own half by the two
-// log-sum-exps, writes O and LSE, and arrives on the second's xfer_free.
+// Both halves run as ordinary tiles.  At the end the first CTA, once its
+// own K/V ring and Q buffer are idle (its last PV GEMMs done), arrives on the
+// second's xfer_free; the second then writes its normalised fp32 partial O
+// and base-2 log-sum-exp straight into the first's ring and Q buffer with
+// remote (distributed shared memory) stores, which are posted, and arrives
+// on the first's xfer_full (release at cluster scope); the first merges them,
+// from its own shared memory, with its half by the two log-sum-exps and
+// writes O and LSE.
 // Cluster barriers at start (barriers initialised) and exit (no CTA leaves
 // while its partner may still touch its shared memory) bracket the kernel.
 //
@@ -286,8 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* drain = q_full + 10;
   uint64_t* fin = q_full + 11;     // [buffer][sub-tile]
   uint64_t* q_free = q_full + 15;
-  // split tail: the partner's partial result is in its shared memory
-  // (128 remote arrivals), and it has been read (128 remote arrivals)
+  // split tail: the second CTA's partial result is in the first CTA's
+  // shared memory (128 remote arrivals on the first's xfer_full), and the
+  // first CTA's ring and Q buffer are free to receive it (128 remote
+  // arrivals on the second's xfer_free)
   uint64_t* xfer_full = q_full + 17;
   uint64_t* xfer_free = q_full + 18;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
@@ -610,17 +614,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool have_next = next_work(k_next, nxt);
       if (cur.pair == 1) {
         // Second KV half of a split tail tile, the CTA's last tile.  Once its
-        // last PV is done (PV_1 is issued after PV_0, and tensor-core work
-        // runs in issue order) the K/V ring and the Q buffer are idle: the
-        // normalised fp32 partial O_t goes to the ring as [t][row][D], the
-        // 16-byte pieces of a row XOR-swizzled by row % 8, and its base-2
-        // log-sum-exp to the Q buffer as [t][row].  Then every thread arrives
-        // on the partner's xfer_full and waits on this CTA's xfer_free: the
-        // partner has read it all.  A half with no KV block (not produced by
-        // the launch's split rule, which needs long tiles, but handled) leaves
-        // O unset and its log-sum-exp -inf (weight 0 in the merge).
-        float* part = reinterpret_cast<float*>(sKV);
-        float* part_l = reinterpret_cast<float*>(sQ);
+        // last PV is done and the partner's ring and Q buffer are idle
+        // (xfer_free), the normalised fp32 partial O_t goes into the
+        // partner's ring as [t][row][D], the 16-byte pieces of a row
+        // XOR-swizzled by row % 8, and its base-2 log-sum-exp into the
+        // partner's Q buffer as [t][row], by remote stores; then every thread
+        // arrives on the partner's xfer_full.  A half with no KV block (not
+        // produced by the launch's split rule, which needs long tiles, but
+        // handled) leaves O unset and its log-sum-exp -inf (weight 0 in the
+        // merge).
+        const uint32_t peer = cluster_ctarank() ^ 1u;
+        const uint32_t part = mapa_shared(smem_u32(sKV), peer);
+        const uint32_t part_l = mapa_shared(smem_u32(sQ), peer);
         float lsum[2] = {0.f, 0.f}, lpsum[2] = {0.f, 0.f}, lmax[2] = {0.f, 0.f};
         if (cur.n_blocks > 0) {
 #pragma unroll
@@ -653,17 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
         if (!ok) break;
-        // the ring and the Q buffer were last written by TMA and read by the
-        // tensor core (both complete): order the plain stores after them
-        fence_proxy_async_smem();
+        if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) break;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (t >= n_sub) break;
           const bool empty = !(lpsum[t] > 0.f);
           const float inv_l = empty ? 0.f : 1.f / lpsum[t];
-          part_l[t * kBlockM + r] = empty ? -INFINITY : lmax[t] + log2f(lsum[t]);
+          st_shared_cluster_f32(part_l + (uint32_t)((t * kBlockM + r) * 4),
+                                empty ? -INFINITY : lmax[t] + log2f(lsum[t]));
           if (cur.n_blocks > 0) {
-            float* row = part + (size_t)(t * kBlockM + r) * D;
+            const uint32_t row = part + (uint32_t)((t * kBlockM + r) * D * 4);
             const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
 #pragma unroll 1
             for (int ch = 0; ch < D / 16; ++ch) {
@@ -674,18 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
               for (int qd = 0; qd < 4; ++qd) {
                 const int cc = ch * 4 + qd;  // 16-byte piece of the row
-                *reinterpret_cast<float4*>(row + 4 * (cc ^ (r & 7))) =
-                    make_float4(u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
-                                u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
+                st_shared_cluster_v4(row + 16u * (uint32_t)(cc ^ (r & 7)),
+                                     u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
+                                     u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
               }
             }
           }
         }
         tc_fence_before_sync();
         // (the test of the hand-off's timeout path withholds this arrival)
-        if (!p.fault_drop_xfer)
-          mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), cluster_ctarank() ^ 1u));
-        if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) ok = false;
+        if (!p.fault_drop_xfer) mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), peer));
         break;  // the tail round is the last: no tile follows
       }
 #pragma unroll
@@ -726,14 +728,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           float w0 = inv_l, w1 = 0.f, lse_out = lse_row;
           uint32_t prow = 0;
           if (merge) {
-            if (t == 0 && !warp_wait_cluster(xfer_full, 0, sAbort, budget)) {
-              ok = false;
-              break;
+            if (t == 0) {
+              // this CTA's ring and Q buffer receive the partner's partial
+              // once every PV GEMM of the tile is done (the last readers of
+              // both): then tell the partner, and wait for its data
+              // (sub-tile 0's wait above has counted this tile already;
+              // sub-tile 1's has not)
+              const bool ready =
+                  n_sub < 2 || warp_wait(&pv_done[1], ntl[1] & 1, sAbort, budget);
+              if (!ready) { ok = false; break; }
+              tc_fence_after_sync();
+              fence_proxy_async_smem();
+              mbar_arrive_remote(mapa_shared(smem_u32(xfer_free), cluster_ctarank() ^ 1u));
+              if (!warp_wait_cluster(xfer_full, 0, sAbort, budget)) {
+                ok = false;
+                break;
+              }
             }
-            const uint32_t peer = cluster_ctarank() ^ 1u;
-            prow = mapa_shared(smem_u32(sKV), peer) + (uint32_t)((t * kBlockM + r) * D * 4);
-            const float l1 =
-                ld_shared_cluster_f32(mapa_shared(smem_u32(sQ), peer) + (uint32_t)((t * kBlockM + r) * 4));
+            prow = smem_u32(sKV) + (uint32_t)((t * kBlockM + r) * D * 4);
+            const float l1 = reinterpret_cast<const float*>(sQ)[t * kBlockM + r];
             const float l0 = empty ? -INFINITY : m + log2f(l);
             const float mx = fmaxf(l0, l1);
             w0 = 0.f;
@@ -788,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                   for (int qd = 0; qd < 4; ++qd) {
                     const int cc = h * 16 + q16 * 4 + qd;  // 16-byte fp32 piece of the partner's row
-                    const float4 pv = ld_shared_cluster_v4(prow + 16u * (uint32_t)(cc ^ (lane & 7)));
+                    const float4 pv = ld_shared_v4f(prow + 16u * (uint32_t)(cc ^ (lane & 7)));
                     // w1 = 0 (an empty partner half) must not meet its unset values
                     const float a[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
@@ -851,8 +864,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // of the next tile may start on sub-tile t
         if (have_next && (t == 0 || nxt.has_sub1)) mbar_arrive(&p_full[t]);
       }
-      // the partner's partial has been read
-      if (cur.pair == 0 && ok) mbar_arrive_remote(mapa_shared(smem_u32(xfer_free), cluster_ctarank() ^ 1u));
       if (!ok) break;
       stamp(tr, kEvEnd, 0);
       k = k_next;

@@ -195,21 +195,27 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
-// 4 bytes from another CTA's shared memory (a shared::cluster address).
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+// 16 bytes from this CTA's shared memory (a shared::cta address).
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
   return v;
 }
 
-// 16 bytes from another CTA's shared memory (a shared::cluster address).
-__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
+// 16 bytes to another CTA's shared memory (a shared::cluster address); the
+// store is posted (no round trip), and a later remote arrival with release
+// at cluster scope orders it before what the partner does after its wait.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float a, float b, float c,
+                                                     float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
                : "memory");
-  return v;
+}
+
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
 }
 
 // ---------------------------------------------------------------- fences
