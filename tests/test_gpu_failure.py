@@ -54,9 +54,9 @@ def test_withheld_signal_beyond_last_block_is_harmless():
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_split_tail_handoff_runs_out_and_context_survives(D):
-    """The second CTA of each split tail pair withholds its "partial ready"
-    arrival: the first CTA's cluster-scope wait runs out, then the second's
-    wait for the first to have read it; both reach the exit barrier."""
+    """The second CTA of each split tail pair writes its partial but
+    withholds its "partial ready" arrival: the first CTA's cluster-scope wait
+    runs out; both reach the exit barrier."""
     q, k, v = make_qkv(1, 40, 40, 1024, 4096, D, seed=23)
     scale = 1.0 / math.sqrt(D)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
