@@ -24,10 +24,12 @@
 //               N = 64, K = 16) of the A slices (tensor memory) with the x
 //               slices (shared memory, MN-major) into one of four 128 x 64
 //               fp32 accumulators (heads rotate over them);
-//   warp 22     vectors and key factors: per head, loads dA_cs and dt (1-D
-//               bulk copies, ahead as far as its ring allows) and computes the per-key
-//               factors of the decay and the mask of portions where dA_cs
-//               rises (see below);
+//   warps 22-23 vectors and key factors, heads alternating between the two
+//               warps: per head, loads dA_cs and dt of the keys the tile's
+//               rows see (1-D bulk copies, into a ring of 4 heads of 256
+//               keys or 8 of 128, as far ahead as the ring allows) and
+//               computes the per-key factors of the decay and the mask of
+//               portions where dA_cs rises (see below);
 //   warp 21     TMA producer: the tile's cb once (3-D map, 32-key boxes;
 //               one barrier per 64-key slice, issued along with the first
 //               head's x slices), then per head its x slices (4-D map over
@@ -54,7 +56,8 @@ constexpr int kCsOutWarp0 = 4 * kCsScaleGroups;  // first warp of the output war
 constexpr int kCsMmaWarp = kCsOutWarp0 + 4;
 constexpr int kCsProdWarp = kCsMmaWarp + 1;
 constexpr int kCsVecWarp = kCsProdWarp + 1;
-constexpr int kCsThreads = (kCsVecWarp + 1) * 32;
+constexpr int kCsVecWarps = 2;     // vector warps, heads alternating between them
+constexpr int kCsThreads = (kCsVecWarp + kCsVecWarps) * 32;
 constexpr int kCsRows = 128;       // rows of a CTA's tile
 constexpr int kCsSlice = 64;       // keys per slice of the reduction axis
 constexpr int kCsPortion = 16;     // keys per portion (one decay pivot)
@@ -65,7 +68,8 @@ constexpr int kCsRing = 8;         // A slices in tensor memory
 constexpr int kCsPairs = kCsRing / 2;  // slices go in pairs (gs, gs + 1), gs even
 constexpr int kCsRingX = 8;        // x slices in shared memory
 constexpr int kCsPairsX = kCsRingX / 2;
-constexpr int kCsRingV = 4;        // heads' vectors in shared memory
+constexpr int kCsRingV = 4;        // heads' vectors in shared memory (256 keys each)
+constexpr int kCsRingVMax = kCsRingV * (kCsMaxQ / kCsRows);  // heads of 128 keys in the same space
 constexpr int kCsAcc = 4;          // accumulators in tensor memory
 constexpr uint32_t kCsAll = 0xffffffffu;
 
@@ -76,17 +80,20 @@ constexpr int kCsSliceBytesX = kCsSlice * kCsP * 2;                  // 8 KB
 constexpr int kCsOffX = kCsOffCb + (kCsMaxQ / kCsBox) * kCsBoxBytes; // [ring]
 constexpr int kCsStageBytes = kCsRows * kCsP * 2;                    // 16 KB
 constexpr int kCsOffStage = kCsOffX + kCsRingX * kCsSliceBytesX;     // one tile
-constexpr int kCsVecBytes = 2 * kCsMaxQ * 4;                         // dA_cs, dt of one head
-constexpr int kCsOffVec = kCsOffStage + kCsStageBytes;               // [ring]
-constexpr int kCsOffKf = kCsOffVec + kCsRingV * kCsVecBytes;         // [vector ring][Q] key factors
-constexpr int kCsOffMask = kCsOffKf + kCsRingV * kCsMaxQ * 4;        // [vector ring] rise masks
-constexpr int kCsOffBar = kCsOffMask + kCsRingV * 4;
+// The vector ring holds, per head, dA_cs and dt of the keys the tile's rows
+// see (nkeys = 128 or 256; rows see keys up to the tile's last row) and
+// their key factors: 4 heads of 256 keys or 8 of 128 in the same space.
+constexpr int kCsVecRegion = kCsRingV * 2 * kCsMaxQ * 4;             // dA_cs, dt
+constexpr int kCsOffVec = kCsOffStage + kCsStageBytes;               // [ring][2][nkeys]
+constexpr int kCsOffKf = kCsOffVec + kCsVecRegion;                   // [ring][nkeys] key factors
+constexpr int kCsOffMask = kCsOffKf + kCsRingV * kCsMaxQ * 4;        // [ring] rise masks
+constexpr int kCsOffBar = kCsOffMask + kCsRingVMax * 4;
 // cb_full[Q / 64], pair_full[R / 2], pair_free[R / 2], xp_full[RX / 2],
 // xp_free[RX / 2], v_full[RV], v_free[RV], kf_full[RV], acc_full[ACC],
 // acc_free[ACC], drain
 constexpr int kCsCbSlices = kCsMaxQ / kCsSlice;  // cb arrives slice by slice
 constexpr int kCsNumBars =
-    kCsCbSlices + 2 * kCsPairs + 2 * kCsPairsX + 3 * kCsRingV + 2 * kCsAcc + 1;
+    kCsCbSlices + 2 * kCsPairs + 2 * kCsPairsX + 3 * kCsRingVMax + 2 * kCsAcc + 1;
 constexpr int kCsOffMisc = kCsOffBar + kCsNumBars * 8;
 constexpr int kCsSmemBytes = kCsOffMisc + 16 + 1024;
 static_assert(kCsSmemBytes <= 227 * 1024, "shared memory budget");
@@ -132,9 +139,9 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   uint64_t* xp_full = pair_free + kCsPairs;
   uint64_t* xp_free = xp_full + kCsPairsX;
   uint64_t* v_full = xp_free + kCsPairsX;
-  uint64_t* v_free = v_full + kCsRingV;
-  uint64_t* kf_full = v_free + kCsRingV;    // the head's key factors and rise mask written
-  uint64_t* acc_full = kf_full + kCsRingV;
+  uint64_t* v_free = v_full + kCsRingVMax;
+  uint64_t* kf_full = v_free + kCsRingVMax;  // the head's key factors and rise mask written
+  uint64_t* acc_full = kf_full + kCsRingVMax;
   uint64_t* acc_free = acc_full + kCsAcc;
   uint64_t* drain = acc_free + kCsAcc;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + kCsOffMisc);
@@ -160,6 +167,9 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
   const int n_slices = (m0 + kCsRows) / kCsSlice;  // keys 0 .. m0 + 127 are visible to some row
   const int log_ns = (n_slices == 4) ? 2 : 1;      // n_slices is 2 or 4 (Q = 128 or 256)
   const int total = p.HB * n_slices;           // slices of the CTA
+  const int nkeys = n_slices * kCsSlice;       // keys some row of the tile sees
+  const int log_rv = (nkeys == kCsMaxQ) ? 2 : 3;  // heads in the vector ring: 4 or 8
+  const int ringv = 1 << log_rv;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kCsCbSlices; ++i) mbar_init(&cb_full[i], 1);
@@ -171,7 +181,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       mbar_init(&xp_full[i], 2);
       mbar_init(&xp_free[i], 1);
     }
-    for (int i = 0; i < kCsRingV; ++i) {
+    for (int i = 0; i < kCsRingVMax; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_free[i], 128 * n_slices);  // every slice's warpgroup
       mbar_init(&kf_full[i], 32);
@@ -208,20 +218,20 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     for (int gs = w; gs < total && ok; gs += kCsScaleGroups) {
       const int j = gs >> log_ns;              // head of the block
       const int s = gs & (n_slices - 1);       // slice of the head
-      const int vs = j % kCsRingV;
+      const int vs = j & (ringv - 1);
       const int slot = gs % kCsRing;
       const int pr = gs >> 1;                  // pair
       if (!((cb_seen >> s) & 1u)) {
         ok = cs_warp_wait(&cb_full[s], 0, sAbort, budget);
         cb_seen |= 1u << s;
       }
-      ok = ok && cs_warp_wait(&kf_full[vs], (j / kCsRingV) & 1, sAbort, budget);
+      ok = ok && cs_warp_wait(&kf_full[vs], (j >> log_rv) & 1, sAbort, budget);
       ok = ok && (pr < kCsPairs || cs_warp_wait(&pair_free[pr % kCsPairs],
                                                 ((pr / kCsPairs) - 1) & 1, sAbort, budget));
       tc_fence_after_sync();                   // the slot's last products are done before it is rewritten
-      const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
-      const float* sDT = sDA + kCsMaxQ;
-      const float* sKf = sKfAll + vs * kCsMaxQ + s * kCsSlice;
+      const float* sDA = reinterpret_cast<const float*>(sVec) + vs * 2 * nkeys;
+      const float* sDT = sDA + nkeys;
+      const float* sKf = sKfAll + vs * nkeys + s * kCsSlice;
       const uint32_t rises = sMask[vs] >> (s * (kCsSlice / kCsPortion));
       const int r = ((warp + j) & 3) * 32 + lane;  // row of the tile
       const int m = m0 + r;                      // row of the chunk
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
       cs_drain_wait(drain, 0, budget);
     }
     __syncwarp();
-  } else if (warp == kCsVecWarp) {
+  } else if (warp >= kCsVecWarp) {
     // ---------------------------------------------------------- key factors
     // Per head, kf[k] = exp(dA_cs[k | 15] - dA_cs[k]) dt[k] (k | 15 is the
     // last key of k's 16-key portion) and a mask with bit i set where
@@ -401,67 +411,85 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
     // dt > 0 and A < 0) both factors lie in [0, 1]: a portion wholly at or
     // before a row then costs one exponential per row and one per key
     // instead of one per (row, key).
-    // It also loads each head's dA_cs and dt (1-D bulk copies) into a ring of
-    // kCsRingV slots, as far ahead of the head it works on as the slots
-    // allow.
+    // It also loads each head's dA_cs and dt (1-D bulk copies, the keys
+    // 0 .. nkeys - 1 the tile's rows see) into a ring of 4 or 8 slots, as far
+    // ahead of the head it works on as the slots allow.  Warp v takes the
+    // heads j = v, v + 2, ... (so the even slots or the odd ones).
     const float l2e = 1.4426950408889634f;
     const bool leader = elect_one();
+    const int v = warp - kCsVecWarp;
     bool ok = true;
-    int issued = 0;
+    int issued = v;                            // next head of this warp to load
     auto issue = [&](int jn) {
-      const int vs = jn % kCsRingV;
+      const int vs = jn & (ringv - 1);
       if (leader) {
         const size_t off = (((size_t)b * p.H + h0 + jn) * p.nchunks + c) * p.Q;
-        float* dst = reinterpret_cast<float*>(sVec + vs * kCsVecBytes);
-        mbar_arrive_expect_tx(&v_full[vs], 2 * p.Q * 4);
-        bulk_load(dst, p.dA_cs + off, p.Q * 4, &v_full[vs]);
-        bulk_load(dst + kCsMaxQ, p.dt + off, p.Q * 4, &v_full[vs]);
+        float* dst = reinterpret_cast<float*>(sVec) + vs * 2 * nkeys;
+        mbar_arrive_expect_tx(&v_full[vs], 2 * nkeys * 4);
+        bulk_load(dst, p.dA_cs + off, nkeys * 4, &v_full[vs]);
+        bulk_load(dst + nkeys, p.dt + off, nkeys * 4, &v_full[vs]);
       }
       __syncwarp();
     };
-    for (int j = 0; j < p.HB && ok; ++j) {
-      const int vs = j % kCsRingV;
-      // issue every later head whose slot is free (without waiting), and
-      // head j itself in any case (waiting for its slot if need be)
+    for (int j = v; j < p.HB && ok; j += kCsVecWarps) {
+      const int vs = j & (ringv - 1);
+      // issue every later head of this warp whose slot is free (without
+      // waiting), and head j itself in any case (waiting for its slot if
+      // need be)
       while (ok && issued < p.HB) {
         const int jn = issued;
-        if (jn >= kCsRingV) {
-          bool free_now = mbar_test_wait(&v_free[jn % kCsRingV], ((jn / kCsRingV) - 1) & 1);
+        if (jn >= ringv) {
+          bool free_now = mbar_test_wait(&v_free[jn & (ringv - 1)], ((jn >> log_rv) - 1) & 1);
           free_now = __all_sync(kCsAll, free_now);
           if (!free_now) {
             if (jn > j) break;
-            ok = cs_warp_wait(&v_free[jn % kCsRingV], ((jn / kCsRingV) - 1) & 1, sAbort, budget);
+            ok = cs_warp_wait(&v_free[jn & (ringv - 1)], ((jn >> log_rv) - 1) & 1, sAbort,
+                              budget);
             if (!ok) break;
           }
         }
         issue(jn);
-        ++issued;
+        issued += kCsVecWarps;
       }
-      if (!ok || !cs_warp_wait(&v_full[vs], (j / kCsRingV) & 1, sAbort, budget)) {
+      if (!ok || !cs_warp_wait(&v_full[vs], (j >> log_rv) & 1, sAbort, budget)) {
         ok = false;
         break;
       }
-      const float* sDA = reinterpret_cast<const float*>(sVec + vs * kCsVecBytes);
-      const float* sDT = sDA + kCsMaxQ;
-      float* sKf = sKfAll + vs * kCsMaxQ;
+      const float* sDA = reinterpret_cast<const float*>(sVec) + vs * 2 * nkeys;
+      const float* sDT = sDA + nkeys;
+      float* sKf = sKfAll + vs * nkeys;
       uint32_t mask = 0;
-      for (int i = 0; i < p.Q / 32; ++i) {
-        const int k = 32 * i + lane;
-        const float dak = sDA[k];
-        const float dap = sDA[k | (kCsPortion - 1)];
-        sKf[k] = ex2_approx((dap - dak) * l2e) * sDT[k];
-        const uint32_t bal = __ballot_sync(kCsAll, !(dap <= dak));
-        mask |= ((bal & 0xffffu) ? 1u : 0u) << (2 * i);
-        mask |= ((bal >> 16) ? 1u : 0u) << (2 * i + 1);
+      // every load first, then the arithmetic and the stores, so the
+      // 32-key groups overlap (a store to sKf could otherwise alias a
+      // later load)
+      float dak[kCsMaxQ / 32], dap[kCsMaxQ / 32], dtk[kCsMaxQ / 32];
+#pragma unroll
+      for (int i = 0; i < kCsMaxQ / 32; ++i) {
+        if (32 * i < nkeys) {
+          const int k = 32 * i + lane;
+          dak[i] = sDA[k];
+          dap[i] = sDA[k | (kCsPortion - 1)];
+          dtk[i] = sDT[k];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCsMaxQ / 32; ++i) {
+        if (32 * i < nkeys) {
+          sKf[32 * i + lane] = ex2_approx((dap[i] - dak[i]) * l2e) * dtk[i];
+          const uint32_t bal = __ballot_sync(kCsAll, !(dap[i] <= dak[i]));
+          mask |= ((bal & 0xffffu) ? 1u : 0u) << (2 * i);
+          mask |= ((bal >> 16) ? 1u : 0u) << (2 * i + 1);
+        }
       }
       if (lane == 0) sMask[vs] = mask;
       __syncwarp();
       mbar_arrive(&kf_full[vs]);
     }
-    // every copy issued lands before the CTA exits
+    // every copy this warp issued lands before the CTA exits (the last
+    // loads into its slots: heads issued - ringv .. issued - 2 of its parity)
     if (leader) {
-      for (int j = issued > kCsRingV ? issued - kCsRingV : 0; j < issued; ++j)
-        cs_drain_wait(&v_full[j % kCsRingV], (j / kCsRingV) & 1, budget);
+      for (int j = issued - kCsVecWarps; j >= v && j >= issued - ringv; j -= kCsVecWarps)
+        cs_drain_wait(&v_full[j & (ringv - 1)], (j >> log_rv) & 1, budget);
     }
     __syncwarp();
   } else {
@@ -482,8 +510,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
           for (int s = 0; s < n_slices; ++s)
             tma_prefetch_4d(&p.tm_x, 0, h0 + jj, c * p.Q + s * kCsSlice, b);
           const size_t off = (((size_t)b * p.H + h0 + jj) * p.nchunks + c) * p.Q;
-          bulk_prefetch_l2(p.dA_cs + off, p.Q * 4);
-          bulk_prefetch_l2(p.dt + off, p.Q * 4);
+          bulk_prefetch_l2(p.dA_cs + off, nkeys * 4);
+          bulk_prefetch_l2(p.dt + off, nkeys * 4);
         }
       }
       for (int s = 0; s < n_slices; ++s, ++gs) {

@@ -140,6 +140,9 @@ CHUNK_SCAN_WORKLOADS = {
         ChunkScanWorkload("chunkscan_b1_s1024", 1, 1024),
         ChunkScanWorkload("chunkscan_b1_s8192", 1, 8192),
         ChunkScanWorkload("chunkscan_b64_s8192", 64, 8192),
+        # the CTA shape of 64 x 8192 (32 heads per CTA) at an eighth of the
+        # memory: for profiling
+        ChunkScanWorkload("chunkscan_b8_s8192", 8, 8192),
     ]
 }
 
