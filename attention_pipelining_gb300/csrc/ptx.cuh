@@ -272,6 +272,18 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+// tma_store_4d with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* map, const void* src,
+                                                  int32_t x, int32_t y, int32_t z, int32_t w,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4, %5}], [%1], %6;"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "l"(policy)
+      : "memory");
+}
+
 // 3-D tiled store shared -> global (the innermost coordinate 16-byte aligned;
 // no coordinate negative), tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
