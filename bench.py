@@ -46,13 +46,16 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
 KERNEL_SOURCES = ["attention_pipelining_gb300/csrc/attn_fwd_sm103.cu",
                   "attention_pipelining_gb300/csrc/attn_tiles.cuh",
                   "attention_pipelining_gb300/csrc/ptx.cuh"]
+CS_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chunk_scan_traffic.json")
+CS_KERNEL_SOURCES = ["attention_pipelining_gb300/csrc/chunk_scan_sm103.cu",
+                     "attention_pipelining_gb300/csrc/ptx.cuh"]
 
 
 # ----------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -144,17 +147,37 @@ def timed_steps(requested, per_step_s):
     return int(min(MAX_DEFAULT_STEPS, max(MIN_DEFAULT_STEPS, want)))
 
 
-def load_traffic():
+def load_traffic(path=TRAFFIC_FILE, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    if d.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return d
+
+
+def chunk_scan_traffic(w):
+    """(DRAM bytes per launch, note) of the chunk scan on workload w from the
+    committed capture, scaled by the batch size when w differs from the
+    captured workload only in a larger B (the same CTAs, 32 heads each, in
+    more waves: inputs, output and traffic grow with B); (None, None) if the
+    capture is stale or of other shapes."""
+    d = load_traffic(CS_TRAFFIC_FILE, CS_KERNEL_SOURCES)
+    if d is None:
+        return None, None
+    shape = d.get("shape", {})
+    if any(shape.get(k) != getattr(w, k) for k in ("L", "H", "P", "G", "Q")):
+        return None, None
+    if w.B < shape.get("B", 0):
+        return None, None            # smaller grids choose smaller head blocks
+    if shape.get("B") == w.B:
+        return d["dram_bytes_per_launch"], f"ncu capture of {d['workload']}"
+    return (d["dram_bytes_per_launch"] * w.B / shape["B"],
+            f"ncu capture of {d['workload']}, scaled by B {w.B} / {shape['B']}")
 
 
 class ClockSampler:
@@ -721,6 +744,7 @@ def run_chunk_scan(args, name):
         return
     hbm_peak = load_hbm_peak()
     per_launch = t_local / args.steps
+    traffic, traffic_note = chunk_scan_traffic(w)
     line = {
         "metric": "Mamba2 chunk scan TFLOP/s (bf16 products, fp32 acc; 2 P per visible key)",
         "value": world * w.flops * args.steps / t / 1e12,
@@ -747,7 +771,8 @@ def run_chunk_scan(args, name):
             "unit": "GB/s",
             "frac": w.io_bytes / per_launch / 1e9 / hbm_peak[0],
             "peak_kind": f"{hbm_peak[1]} HBM copy",
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_source": traffic_note,
             "algorithmic_bytes_per_launch": w.io_bytes,
             "kernel": "chunk_scan_kernel",
         },
