@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) chunk_scan_kernel(const __grid_
         const float da_m = da_raw * l2e;
         const uint64_t dam2 = f2_pack(da_m, da_m);
         const uint32_t a_col = tmem + lane_base + kCsTmemA + slot * (kCsSlice / 2);
-#pragma unroll 2
+        // the four portions unrolled: their loads and products interleave
+#pragma unroll
         for (int pi = 0; pi < kCsSlice / kCsPortion; ++pi) {
           const int k0 = s * kCsSlice + pi * kCsPortion;   // first key of the portion
           const float* cb_row = reinterpret_cast<const float*>(
