@@ -9,13 +9,13 @@
 //   out[m, :] = sum_{k <= m} cb[m, k] exp(dA_cs[m] - dA_cs[k]) dt[k] x[k, :]
 //
 // One CTA = (batch, chunk, 128-row tile of the chunk, block of HB heads of
-// one group), 736 threads.  The CTA's slices (64 keys of one head) are
+// one group), 768 threads.  The CTA's slices (64 keys of one head) are
 // numbered gs = 0, 1, ... head by head:
 //   warps 0-15  four scaling warpgroups; warpgroup w takes slices gs = w,
 //               w + 4, ...: thread = row of the tile, it scales its row's 64
 //               keys of cb (kept in shared memory for all the CTA's heads)
 //               by the decay and dt, rounds to bf16 and stores them into the
-//               slice's A slot in tensor memory (a ring of six slots; two
+//               slice's A slot in tensor memory (a ring of eight slots; two
 //               consecutive slices share one full/free barrier pair);
 //   warps 16-19 output warpgroup: per head, reads the accumulator from tensor
 //               memory, rounds to bf16 into a staging tile in shared memory
