@@ -349,9 +349,9 @@ def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,
 
 def fwd_tail_timeout_test(q, k, v, causal: bool, scale: float,
                           wait_budget_ns: int = 20_000_000, stream=None):
-    """Test hook: runs the forward's split-tail launch with the second CTA of
-    each pair withholding its hand-off, so both CTAs' bounded cluster waits
-    run out (see attn_testing.h).  Returns (o, lse); the device status word
+    """Test hook: runs the forward's split-tail launch with no CTA of a pair
+    sending its staged partial, so the bounded cluster waits for it run out
+    (see attn_testing.h).  Returns (o, lse); the device status word
     then reads ATTN_ERR_TIMEOUT."""
     import torch
     _check_inputs(q, k, v)

@@ -44,14 +44,16 @@
 // Split tail (the kTail instantiation, launched as clusters of two CTAs):
 // when the grid's last round would leave more than half of the CTAs idle,
 // each of its tiles is split across a CTA pair, half of the KV blocks each.
-// Both halves run as ordinary tiles.  At the end the first CTA, once its
-// own K/V ring and Q buffer are idle (its last PV GEMMs done), arrives on the
-// second's xfer_free; the second then writes its normalised fp32 partial O
-// and base-2 log-sum-exp straight into the first's ring and Q buffer with
-// remote (distributed shared memory) stores, which are posted, and arrives
-// on the first's xfer_full (release at cluster scope); the first merges them,
-// from its own shared memory, with its half by the two log-sum-exps and
-// writes O and LSE.
+// Both halves run as ordinary tiles.  At the end each CTA writes one
+// sub-tile (the first sub-tile 0, the second sub-tile 1; with one sub-tile,
+// the first) and sends the other one's partial (normalised fp32 O and
+// base-2 log-sum-exp) to its partner: it stages the partial in its own idle
+// K/V ring and Q buffer, arms its xfer_full with the bytes it will receive
+// and arrives on the partner's xfer_free; once its own xfer_free completes
+// it sends the staged partial with two bulk copies (shared memory to the
+// partner's shared memory, completing as transaction bytes on the partner's
+// xfer_full); then it merges its sub-tile with the received partial by the
+// two log-sum-exps and writes O and LSE.
 // Cluster barriers at start (barriers initialised) and exit (no CTA leaves
 // while its partner may still touch its shared memory) bracket the kernel.
 //
@@ -74,13 +76,16 @@ __device__ int g_attn_status = 0;
 namespace {
 
 constexpr int kThreads = 512;
+constexpr uint32_t kBarCorrection = 1;  // named barrier of the correction warpgroup (split tail)
 constexpr int kBlockM = 128;  // rows per query sub-tile
 constexpr int kBlockN = 128;  // keys per KV block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
 // Split tail only for tiles of at least this many KV blocks: half a tile must
-// save more than the merge and the cluster start cost (measured on GB300:
-// +5 % at 128 blocks per tile, none at 16, a loss for short causal tiles)
-constexpr int kSplitTailMinBlocks = 32;
+// save more than the exchange, the merge and the cluster start cost.  Measured
+// on GB300 with the one-bulk-copy exchange: +2.8 % at 16 blocks per tile (4 x
+// 16 heads x 2048, 128-dim), the same at 8; causal tiles are never split (the
+// last round holds the shortest of them).
+constexpr int kSplitTailMinBlocks = 16;
 constexpr uint32_t kFull = 0xffffffffu;
 // Pairs of probabilities out of every 8 whose exp2 runs on the FMA pipe
 // (exp2_poly_x2) instead of MUFU, in unmasked blocks.  0: every exp2 on
@@ -132,6 +137,11 @@ struct Cfg {
       (kOffTrace + (kTraceBytes > kStageBytes ? kTraceBytes : kStageBytes) + 1023) / 1024 * 1024;
   static constexpr int kOnesBytes = (D == 64) ? kSlabBytes : 0;  // one [128 x 64] bf16 atom of ones
   static constexpr int kSmemBytes = kSmemEnd0 + kOnesBytes + 1024;
+  // split tail: a received partial (128 rows x D fp32) lands here in the
+  // K/V ring, after the sender's own staged one
+  static constexpr uint32_t kSplitIn = (uint32_t)kBlockM * D * 4;
+  static_assert(2 * kSplitIn <= (uint32_t)(kSlots * kTileBytes), "split-tail partials in the ring");
+  static_assert(2 * kBlockM * 4 <= 2 * kTileBytes, "split-tail log-sum-exps in the Q buffer");
   // Row sums on the tensor core (D = 64, where tensor memory has room): the
   // PV GEMM runs with N = D + 16 against [V | ones], so columns D .. D + 15
   // of O_t accumulate the sum of the bf16 probabilities the GEMM consumed,
@@ -288,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint64_t* drain = q_full + 10;
   uint64_t* fin = q_full + 11;     // [buffer][sub-tile]
   uint64_t* q_free = q_full + 15;
-  // split tail: the second CTA's partial result is in the first CTA's
-  // shared memory (128 remote arrivals on the first's xfer_full), and the
-  // first CTA's ring and Q buffer are free to receive it (128 remote
-  // arrivals on the second's xfer_free)
+  // split tail: the partner's partial result is in this CTA's shared
+  // memory (one arrival with the expected bytes by this CTA, the bytes of
+  // the partner's bulk copies), and the partner's receiving region is idle
+  // (128 remote arrivals by the partner's correction warpgroup)
   uint64_t* xfer_full = q_full + 17;
   uint64_t* xfer_free = q_full + 18;
   float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
-    mbar_init(xfer_full, kBlockM);
+    mbar_init(xfer_full, 1);
     mbar_init(xfer_free, kBlockM);
     *sAbort = 0;
     fence_mbar_init();
@@ -612,21 +622,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int k_next = k + 1;
       Tile nxt;
       const bool have_next = next_work(k_next, nxt);
-      if (cur.pair == 1) {
-        // Second KV half of a split tail tile, the CTA's last tile.  Once its
-        // last PV is done and the partner's ring and Q buffer are idle
-        // (xfer_free), the normalised fp32 partial O_t goes into the
-        // partner's ring as [t][row][D], the 16-byte pieces of a row
-        // XOR-swizzled by row % 8, and its base-2 log-sum-exp into the
-        // partner's Q buffer as [t][row], by remote stores; then every thread
-        // arrives on the partner's xfer_full.  A half with no KV block (not
-        // produced by the launch's split rule, which needs long tiles, but
-        // handled) leaves O unset and its log-sum-exp -inf (weight 0 in the
-        // merge).
+      // Split tail tile (the CTA's last): the two KV halves exchange
+      // partial results.  With two sub-tiles each CTA writes one (the first
+      // CTA sub-tile 0, the second sub-tile 1) and sends the other one's
+      // partial to its partner; with one sub-tile the second CTA sends it and
+      // the first writes it.  A partial is O_t normalised by its half's own
+      // sum (fp32, [row][D], the 16-byte pieces of a row XOR-swizzled by
+      // row % 8) and the half's base-2 log-sum-exp; it is staged at the
+      // start of the sender's own idle K/V ring (and Q buffer) and lands at
+      // C::kSplitIn into the receiver's (and at row 128 of its Q buffer), by
+      // one bulk copy each, completing as transaction bytes on the
+      // receiver's xfer_full.  A half with no KV block (not produced by the
+      // launch's split rule, which needs long tiles, but handled) sends zeros
+      // and a log-sum-exp of -inf (weight 0 in the merge).
+      bool split_done = false;  // the exchange below took this tile's waits
+      int t_write = -1;         // the sub-tile this CTA writes
+      float sl[2] = {0.f, 0.f}, slp[2] = {0.f, 0.f}, sm[2] = {0.f, 0.f};
+      if (cur.pair >= 0) {
         const uint32_t peer = cluster_ctarank() ^ 1u;
-        const uint32_t part = mapa_shared(smem_u32(sKV), peer);
-        const uint32_t part_l = mapa_shared(smem_u32(sQ), peer);
-        float lsum[2] = {0.f, 0.f}, lpsum[2] = {0.f, 0.f}, lmax[2] = {0.f, 0.f};
+        const bool sym = cur.has_sub1;
+        const int t_send = sym ? 1 - cur.pair : (cur.pair == 1 ? 0 : -1);
+        t_write = sym ? cur.pair : (cur.pair == 0 ? 0 : -1);
+        // every GEMM of the tile done: the ring and the Q buffer are idle,
+        // and the row statistics final
         if (cur.n_blocks > 0) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -639,9 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             ++ntl[t];
             const int sb = (buf * 2 + t) * kBlockM + r;
-            lsum[t] = sRowSum[sb];
-            lpsum[t] = sRowSumP[sb];
-            lmax[t] = sRowMax[sb];
+            sl[t] = sRowSum[sb];
+            slp[t] = sRowSumP[sb];
+            sm[t] = sRowMax[sb];
           }
           tc_fence_after_sync();
           if constexpr (C::kSumCol) {
@@ -652,64 +670,93 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 uint32_t v = tmem_ld_x1(tmem + lane_base + (t ? C::kTmO1 : C::kTmO0) + D);
                 tmem_ld_wait();
                 asm volatile("" : "+r"(v));
-                lpsum[t] = u2f(v);
+                slp[t] = u2f(v);
               }
             }
           }
         }
-        if (!ok) break;
-        if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) break;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t >= n_sub) break;
-          const bool empty = !(lpsum[t] > 0.f);
-          const float inv_l = empty ? 0.f : 1.f / lpsum[t];
-          st_shared_cluster_f32(part_l + (uint32_t)((t * kBlockM + r) * 4),
-                                empty ? -INFINITY : lmax[t] + log2f(lsum[t]));
-          if (cur.n_blocks > 0) {
-            const uint32_t row = part + (uint32_t)((t * kBlockM + r) * D * 4);
-            const uint32_t tO = tmem + lane_base + (t ? C::kTmO1 : C::kTmO0);
+        if (ok && t_send >= 0) {
+          const bool empty = !(slp[t_send] > 0.f);
+          const float inv_l = empty ? 0.f : 1.f / slp[t_send];
+          reinterpret_cast<float*>(sQ)[r] = empty ? -INFINITY : sm[t_send] + log2f(sl[t_send]);
+          const uint32_t row = smem_u32(sKV) + (uint32_t)(r * D * 4);
+          const uint32_t tO = tmem + lane_base + (t_send ? C::kTmO1 : C::kTmO0);
 #pragma unroll 1
-            for (int ch = 0; ch < D / 16; ++ch) {
-              uint32_t o[16];
+          for (int ch = 0; ch < D / 16; ++ch) {
+            uint32_t o[16];
+            if (cur.n_blocks > 0) {
               tmem_ld_x16(tO + ch * 16, o);
               tmem_ld_wait();
               reg_after_wait(o);
+            } else {
 #pragma unroll
-              for (int qd = 0; qd < 4; ++qd) {
-                const int cc = ch * 4 + qd;  // 16-byte piece of the row
-                st_shared_cluster_v4(row + 16u * (uint32_t)(cc ^ (r & 7)),
-                                     u2f(o[qd * 4 + 0]) * inv_l, u2f(o[qd * 4 + 1]) * inv_l,
-                                     u2f(o[qd * 4 + 2]) * inv_l, u2f(o[qd * 4 + 3]) * inv_l);
-              }
+              for (int i = 0; i < 16; ++i) o[i] = 0u;
+            }
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+              const int cc = ch * 4 + qd;  // 16-byte piece of the row
+              st_shared_v4(row + 16u * (uint32_t)(cc ^ (r & 7)), f2u(u2f(o[qd * 4 + 0]) * inv_l),
+                           f2u(u2f(o[qd * 4 + 1]) * inv_l), f2u(u2f(o[qd * 4 + 2]) * inv_l),
+                           f2u(u2f(o[qd * 4 + 3]) * inv_l));
             }
           }
+          fence_proxy_async_smem();            // the staged rows before the bulk copy reads them
         }
-        tc_fence_before_sync();
-        // (the test of the hand-off's timeout path withholds this arrival)
-        if (!p.fault_drop_xfer) mbar_arrive_remote(mapa_shared(smem_u32(xfer_full), peer));
-        break;  // the tail round is the last: no tile follows
+        if (ok && t_write >= 0) {
+          // this CTA's receiving region is idle: arm xfer_full with the bytes
+          // to come and tell the partner
+          if (threadIdx.x == 2 * 128)
+            mbar_arrive_expect_tx(xfer_full, (uint32_t)(kBlockM * (D + 1) * 4));
+          mbar_arrive_remote(mapa_shared(smem_u32(xfer_free), peer));
+        }
+        // every thread of the warpgroup has staged its row (and a wait that
+        // ran out in any of them stops all)
+        if (barrier_or(kBarCorrection, 128, !ok)) { ok = false; break; }
+        if (t_send >= 0) {
+          // the partner's receiving region is idle: the two copies (the test
+          // of the hand-off's timeout path withholds them)
+          if (!warp_wait_cluster(xfer_free, 0, sAbort, budget)) { ok = false; break; }
+          if (threadIdx.x == 2 * 128 && !p.fault_drop_xfer) {
+            const uint32_t bar = mapa_shared(smem_u32(xfer_full), peer);
+            bulk_copy_to_cluster(mapa_shared(smem_u32(sKV) + C::kSplitIn, peer), smem_u32(sKV),
+                                 (uint32_t)(kBlockM * D * 4), bar);
+            bulk_copy_to_cluster(mapa_shared(smem_u32(sQ) + kBlockM * 4, peer), smem_u32(sQ),
+                                 (uint32_t)(kBlockM * 4), bar);
+          }
+        }
+        if (t_write < 0) break;  // the tail round is the last: no tile follows
+        if (!warp_wait_cluster(xfer_full, 0, sAbort, budget)) { ok = false; break; }
+        split_done = true;
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (t < n_sub) {
-          const int buf = (int)(ntl[t] & 1);
-          if (!warp_wait(&fin[buf * 2 + t], (ntl[t] >> 1) & 1, sAbort, budget)) { ok = false; break; }
-          if (!warp_wait(&pv_done[t], ntl[t] & 1, sAbort, budget)) { ok = false; break; }
-          ++ntl[t];
-          tc_fence_after_sync();
-          stamp(tr, kEvEpilogue, t);
-          const int sb = (buf * 2 + t) * kBlockM + r;
-          const float l = sRowSum[sb];
-          const float m = sRowMax[sb];
-          float lp = sRowSumP[sb];
-          if constexpr (C::kSumCol) {
-            // the sum of the bf16 probabilities, from O_t's sum columns
-            uint32_t v = tmem_ld_x1(tmem + lane_base + (t ? C::kTmO1 : C::kTmO0) + D);
-            tmem_ld_wait();
-            asm volatile("" : "+r"(v));
-            lp = u2f(v);
+          // (a split tail tile: the partner writes the other sub-tile)
+          if (split_done && t != t_write) continue;
+          float l, m, lp;
+          if (split_done) {
+            l = sl[t];
+            m = sm[t];
+            lp = slp[t];
+          } else {
+            const int buf = (int)(ntl[t] & 1);
+            if (!warp_wait(&fin[buf * 2 + t], (ntl[t] >> 1) & 1, sAbort, budget)) { ok = false; break; }
+            if (!warp_wait(&pv_done[t], ntl[t] & 1, sAbort, budget)) { ok = false; break; }
+            ++ntl[t];
+            tc_fence_after_sync();
+            const int sb = (buf * 2 + t) * kBlockM + r;
+            l = sRowSum[sb];
+            m = sRowMax[sb];
+            lp = sRowSumP[sb];
+            if constexpr (C::kSumCol) {
+              // the sum of the bf16 probabilities, from O_t's sum columns
+              uint32_t v = tmem_ld_x1(tmem + lane_base + (t ? C::kTmO1 : C::kTmO0) + D);
+              tmem_ld_wait();
+              asm volatile("" : "+r"(v));
+              lp = u2f(v);
+            }
           }
+          stamp(tr, kEvEpilogue, t);
           // a row with no visible key (possible only within one KV split)
           // has l = 0: its partial result is O = 0, LSE = -inf
           const bool empty = !(lp > 0.f);
@@ -720,33 +767,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           // The tensor-memory loads are warp-wide; only the stores depend on
           // whether the row exists.
           //
-          // First KV half of a split tail tile (pair 0): the output merges
-          // this half with the partner's partial (in the partner's shared
-          // memory; see the sender above) by the two halves' log-sum-exps:
-          // O = w0 O_own + w1 O_partner.  Otherwise w0 = 1 / l, w1 = 0.
-          const bool merge = (cur.pair == 0);
+          // A split tail tile's written sub-tile merges this half with the
+          // partner's partial (received at C::kSplitIn) by the two halves'
+          // log-sum-exps: O = w0 O_own + w1 O_partner.  Otherwise w0 = 1 / l,
+          // w1 = 0.
+          const bool merge = split_done;
           float w0 = inv_l, w1 = 0.f, lse_out = lse_row;
           uint32_t prow = 0;
           if (merge) {
-            if (t == 0) {
-              // this CTA's ring and Q buffer receive the partner's partial
-              // once every PV GEMM of the tile is done (the last readers of
-              // both): then tell the partner, and wait for its data
-              // (sub-tile 0's wait above has counted this tile already;
-              // sub-tile 1's has not)
-              const bool ready =
-                  n_sub < 2 || warp_wait(&pv_done[1], ntl[1] & 1, sAbort, budget);
-              if (!ready) { ok = false; break; }
-              tc_fence_after_sync();
-              fence_proxy_async_smem();
-              mbar_arrive_remote(mapa_shared(smem_u32(xfer_free), cluster_ctarank() ^ 1u));
-              if (!warp_wait_cluster(xfer_full, 0, sAbort, budget)) {
-                ok = false;
-                break;
-              }
-            }
-            prow = smem_u32(sKV) + (uint32_t)((t * kBlockM + r) * D * 4);
-            const float l1 = reinterpret_cast<const float*>(sQ)[t * kBlockM + r];
+            prow = smem_u32(sKV) + C::kSplitIn + (uint32_t)(r * D * 4);
+            const float l1 = reinterpret_cast<const float*>(sQ)[kBlockM + r];
             const float l0 = empty ? -INFINITY : m + log2f(l);
             const float mx = fmaxf(l0, l1);
             w0 = 0.f;
@@ -806,7 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     const float a[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                      const float own = u2f(o[qd * 4 + e]) * w0;
+                      // (w0 = 0: an empty own half, whose O was never written)
+                      const float own = w0 != 0.f ? u2f(o[qd * 4 + e]) * w0 : 0.f;
                       o[qd * 4 + e] = f2u(w1 > 0.f ? fmaf(w1, a[e], own) : own);
                     }
                   }

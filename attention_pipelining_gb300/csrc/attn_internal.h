@@ -52,9 +52,11 @@ struct AttnParams {
   // Split tail (set at launch; 0 = off): when the last round of the grid
   // holds tail_pairs <= G / 2 tiles (list entries tail_base = R * G ..),
   // the grid runs as clusters of two CTAs and cluster i takes tail tile
-  // tail_base + i, each CTA one half of its KV blocks.  The second CTA hands
-  // its partial result to the first through distributed shared memory, and
-  // the first writes the merged O and LSE.  Off in split-KV launches.
+  // tail_base + i, each CTA one half of its KV blocks.  Each CTA of the pair
+  // writes the merged O and LSE of one 128-row sub-tile and sends its partial
+  // result for the other one to its partner, one bulk copy into the partner's
+  // shared memory (a tile with one sub-tile: the second CTA sends, the first
+  // writes).  Off in split-KV launches.
   int tail_base;
   int tail_pairs;
   float scale_log2;  // |scale| * log2(e) > 0: the softmax runs in base 2
@@ -69,10 +71,9 @@ struct AttnParams {
   // first softmax warpgroup does not signal "P ready" for this KV block, so
   // the tensor-core issuer's bounded wait runs out.  -1 in normal use.
   int fault_drop_block;
-  // Test of the split tail's hand-off (split-tail instantiation only): when
-  // non-zero, the second CTA of each pair withholds its "partial result
-  // ready" arrival, so both CTAs' bounded cluster waits run out.  0 in normal
-  // use.
+  // Test of the split tail's exchange (split-tail instantiation only): when
+  // non-zero, no CTA of a pair issues the bulk copy of its staged partial,
+  // so every receiving CTA's bounded wait for it runs out.  0 in normal use.
   int fault_drop_xfer;
 };
 

@@ -19,11 +19,11 @@
  *
  * attn_fwd_tail_timeout_test does the same for the split tail of attn_fwd (see
  * attn.h: the last round's tiles split across a cluster of two CTAs).  The
- * call runs the split-tail launch with one difference: the second CTA of
- * each pair writes its partial result into the first CTA's shared memory but
- * never signals that it is there, so the first CTA's bounded wait for it runs
- * out after `wait_budget_ns`.  Both CTAs unwind, reach the cluster barrier at
- * exit and return; the status word reads ATTN_ERR_TIMEOUT.  Returns ATTN_ERR_UNSUPPORTED (nothing launched) when
+ * call runs the split-tail launch with one difference: no CTA of a pair
+ * sends its partner the partial result it has staged, so each CTA's bounded
+ * wait for the partner's partial runs out after `wait_budget_ns`.  Both
+ * CTAs unwind, reach the cluster barrier at exit and return; the status word
+ * reads ATTN_ERR_TIMEOUT.  Returns ATTN_ERR_UNSUPPORTED (nothing launched) when
  * attn_fwd would not split the tail for these sizes on this device;
  * `wait_budget_ns` must lie in [1 ms, 2 s].  Outputs are unspecified.
  * For tests only.

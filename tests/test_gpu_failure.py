@@ -54,9 +54,9 @@ def test_withheld_signal_beyond_last_block_is_harmless():
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_split_tail_handoff_runs_out_and_context_survives(D):
-    """The second CTA of each split tail pair writes its partial but
-    withholds its "partial ready" arrival: the first CTA's cluster-scope wait
-    runs out; both reach the exit barrier."""
+    """No CTA of a split tail pair sends its staged partial: each CTA's
+    cluster-scope wait for the partner's runs out; both reach the exit
+    barrier."""
     q, k, v = make_qkv(1, 40, 40, 1024, 4096, D, seed=23)
     scale = 1.0 / math.sqrt(D)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()

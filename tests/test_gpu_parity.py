@@ -126,10 +126,11 @@ def test_deterministic():
 
 
 def test_split_tail_repeatable():
-    """A grid whose last round is split across CTA pairs (the second CTA's
-    partial crosses to the first through distributed shared memory), run 20
-    times: every launch gives the same bits and no wait runs out, so the
-    hand-off has no race that shows up from one launch to the next."""
+    """A grid whose last round is split across CTA pairs (each CTA's
+    partial for the sub-tile its partner writes crosses by a bulk copy into
+    the partner's shared memory), run 20 times: every launch gives the same
+    bits and no wait runs out, so the exchange has no race that shows up
+    from one launch to the next."""
     q, k, v = make_qkv(1, 40, 40, 1024, 4096, 64, seed=61)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o0, l0 = ap.attn_fwd(qd, kd, vd, False, 0.125)
@@ -156,6 +157,19 @@ def test_split_tail_ragged_rows(D):
     _check(1, H, H, Sq, Skv, D, False, 1.0, seed=70 + D)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_split_tail_one_subtile_and_ragged_keys(D):
+    """A split tail at the shortest split tiles (S_kv = 2000: 16 KV blocks,
+    the last one ragged, so each half holds 8 and the second half the ragged
+    block) whose tiles alternate between two sub-tiles (one CTA of the pair
+    writes each) and one (S_q = 384: a group's second tile is 128 rows, so
+    the second CTA only sends and the first only writes)."""
+    sms = _sms()
+    H, Sq, Skv = sms // 2 + 4, 384, 2000
+    assert ap.fwd_tail_pairs(1, H, H, Sq, Skv, D, False) == 8
+    _check(1, H, H, Sq, Skv, D, False, 1.0 / math.sqrt(D), seed=90 + D)
+
+
 def test_split_tail_plan():
     """The shapes the split-tail tests rely on do split their tail; causal,
     short-KV and whole-round shapes do not."""
@@ -164,7 +178,9 @@ def test_split_tail_plan():
     assert ap.fwd_tail_pairs(10, 8, 2, 512, 4096, 64, False) == 160 - sms
     assert ap.fwd_tail_pairs(1, 32, 32, 16384, 16384, 128, False) == 2048 % sms
     assert ap.fwd_tail_pairs(1, 40, 40, 1024, 4096, 64, True) == 0       # causal
-    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 2048, 64, False) == 0      # 16 KV blocks
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 2048, 64, False) == 160 - sms  # 16 KV blocks
+    assert ap.fwd_tail_pairs(4, 16, 16, 2048, 2048, 128, False) == 512 % sms
+    assert ap.fwd_tail_pairs(1, 40, 40, 1024, 1920, 64, False) == 0      # 15 KV blocks
     assert ap.fwd_tail_pairs(1, sms // 2, sms // 2, 512, 4096, 64, False) == 0  # whole rounds
 
 
@@ -297,14 +313,15 @@ FULL_HEAD = [n for n in ("long_b1_h32_s16384_d128", "long_causal_b1_h32_s16384_d
 def test_full_size_one_whole_head(name):
     """Full-size workloads: every row of one query head, element by element.
     The head is the last one of the last batch entry: its tiles come last in
-    the tile list, so on the non-causal long sequence it is wholly inside the
-    split tail (every one of its tiles split across a CTA pair), and on the
+    the tile list, so it is wholly inside the
+    split tail (every one of its tiles split across a CTA pair) on the
+    non-causal long sequence and batched shapes, and on the
     grouped-query shape it is the last head of the last KV group."""
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
     o, lse = run_gpu(q, k, v, w.causal, w.scale)
-    if name == "long_b1_h32_s16384_d128":
-        tiles = (w.H_q * w.S_q // 256)
+    if name in ("long_b1_h32_s16384_d128", "batched_b4_h16_s2048_d128"):
+        tiles = w.B * w.H_q * w.S_q // 256
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         tail = ap.fwd_tail_pairs(w.B, w.H_q, w.H_kv, w.S_q, w.S_kv, w.D, w.causal)
         assert tail == tiles % sms and tail >= w.S_q // 256   # the last head is all tail
