@@ -38,7 +38,8 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_fwd_timeout_test", "attn_fwd_tail_timeout_test", "attn_fwd_tail_pairs",
            "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
-           "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_workspace_bytes",
+           "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_deterministic",
+           "attn_bwd_workspace_bytes",
            "attn_bwd_host", "chunk_scan_fwd", "chunk_scan_fwd_host"]
 
 
@@ -103,9 +104,11 @@ def _load():
     lib.attn_splitkv_noalloc_capacity.restype = ctypes.c_size_t
     lib.attn_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
     lib.attn_bwd.restype = ci
+    lib.attn_bwd_deterministic.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
+    lib.attn_bwd_deterministic.restype = ci
     lib.attn_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
     lib.attn_bwd_host.restype = ci
-    lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.chunk_scan_fwd.argtypes = [vp] * 5 + [ci] * 6 + [vp]
     lib.chunk_scan_fwd.restype = ci
@@ -241,16 +244,17 @@ def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int = 0, w
     return o, lse
 
 
-def bwd_workspace_bytes(B, H_q, H_kv, S_q) -> int:
-    return int(_load().attn_bwd_workspace_bytes(B, H_q, H_kv, S_q))
+def bwd_workspace_bytes(B, H_q, H_kv, S_q, D) -> int:
+    return int(_load().attn_bwd_workspace_bytes(B, H_q, H_kv, S_q, D))
 
 
 def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, out=None,
-             stream=None):
+             stream=None, deterministic: bool = False):
     """Backward of attn_fwd: returns (dq, dk, dv) for the upstream gradient
     ``dout``, given the forward's ``o`` and ``lse``.  ``workspace``: optional
     uint8 CUDA tensor of at least bwd_workspace_bytes(...) bytes (allocated if
-    None); ``out``: optional (dq, dk, dv) to write into."""
+    None); ``out``: optional (dq, dk, dv) to write into.  ``deterministic``
+    calls attn_bwd_deterministic (bit-reproducible dQ, see attn.h)."""
     import torch
     _check_inputs(q, k, v)
     for name, t, ref in (("o", o, q), ("dout", dout, q)):
@@ -261,7 +265,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, 
     Hkv, Skv = k.shape[1], k.shape[2]
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H_q, S_q] tensor")
-    nbytes = bwd_workspace_bytes(B, Hq, Hkv, Sq)
+    nbytes = bwd_workspace_bytes(B, Hq, Hkv, Sq, D)
     if nbytes == 0:
         raise AttnError(1, "attn_bwd_workspace_bytes")
     if workspace is None:
@@ -269,11 +273,13 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, workspace=None, 
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = out
-    _check(_load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                            B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
-                            _stream_handle(stream)), "attn_bwd")
+    lib = _load()
+    fn = lib.attn_bwd_deterministic if deterministic else lib.attn_bwd
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+              lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+              dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+              B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+              _stream_handle(stream)), "attn_bwd_deterministic" if deterministic else "attn_bwd")
     return dq, dk, dv
 
 

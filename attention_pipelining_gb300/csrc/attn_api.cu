@@ -267,8 +267,10 @@ static int64_t bwd_padded_rows(int H_q, int H_kv, int S_q) {
   return (R + 127) / 128 * 128;
 }
 
-size_t bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q) {
-  return 2 * (size_t)B * H_kv * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
+// [groups, Rp] -LSE log2(e), [groups, Rp] -D_i, then [groups, Rp, D] the
+// fused backward's fp32 dQ accumulator.
+size_t bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int D) {
+  return (size_t)(D + 2) * B * H_kv * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
 }
 
 // Every check of attn_bwd's arguments, the device's included.
@@ -283,7 +285,7 @@ static attn_status_t bwd_validate(const void* q, const void* k, const void* v, c
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return ATTN_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
-  if (workspace_bytes < bwd_workspace_bytes(B, H_q, H_kv, S_q)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < bwd_workspace_bytes(B, H_q, H_kv, S_q, D)) return ATTN_ERR_INVALID_ARG;
   // grids: key blocks x groups and query blocks x groups CTAs, in one dimension
   const int64_t R64 = (int64_t)(H_q / H_kv) * S_q;
   if (((S_kv + 127) / 128) * (int64_t)B * H_kv >= (1ll << 31) ||
@@ -296,7 +298,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
                               int S_q, int S_kv, int D, int causal, float scale,
-                              attn_stream_t stream) {
+                              bool deterministic, attn_stream_t stream) {
   attn_status_t st = bwd_validate(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
                                   B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
@@ -314,6 +316,8 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   const int64_t Rp = bwd_padded_rows(H_q, H_kv, S_q);
   p.nlse2 = static_cast<float*>(workspace);
   p.ndelta = p.nlse2 + (size_t)B * H_kv * Rp;
+  // the fused dQ (D = 128): accumulated in the workspace's third part
+  p.dq_acc = (!deterministic && D == 128) ? p.ndelta + (size_t)B * H_kv * Rp : nullptr;
   p.B = B;
   p.H_q = H_q;
   p.H_kv = H_kv;
@@ -542,7 +546,7 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
       return ATTN_ERR_CUDA;
     attn_status_t st = bwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, dout_dev, dq_dev, dk_dev,
                                 dv_dev, workspace, workspace_bytes, B, H_q, H_kv, S_q, S_kv, D,
-                                causal, scale, s);
+                                causal, scale, false, s);
     if (st != ATTN_OK) return st;
     if (!down(dq_host, dq_dev, q_bytes, s) || !down(dk_host, dk_dev, kv_bytes, s) ||
         !down(dv_host, dv_dev, kv_bytes, s))
@@ -563,7 +567,7 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
   const size_t lse_group = (size_t)r * S_q;           // floats of one group's LSE
   // a chunk's workspace is its own slice: the per-group layout of a call on
   // ng groups takes 2 * ng padded row vectors (a multiple of 1024 bytes)
-  const size_t ws_group = 2 * (size_t)bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
+  const size_t ws_group = (size_t)(D + 2) * bwd_padded_rows(H_q, H_kv, S_q) * sizeof(float);
   auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
   auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
   for (int c = 0; c < chunks; ++c) {
@@ -586,7 +590,7 @@ static attn_status_t bwd_host_impl(const void* q_host, const void* k_host, const
     attn_status_t st = bwd_impl(db(q_dev, qo), db(k_dev, ko), db(v_dev, ko), db(o_dev, qo),
                                 lse_dev + lo, db(dout_dev, qo), db(dq_dev, qo), db(dk_dev, ko),
                                 db(dv_dev, ko), db(workspace, z0 * ws_group), ng * ws_group, 1,
-                                ng * r, ng, S_q, S_kv, D, causal, scale, cs);
+                                ng * r, ng, S_q, S_kv, D, causal, scale, false, cs);
     if (st != ATTN_OK) return leave(st);
     if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->down, hp->computed[c], 0) != cudaSuccess ||
@@ -764,12 +768,22 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
                        int S_q, int S_kv, int D, int causal, float scale, attn_stream_t stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv,
-                  S_q, S_kv, D, causal, scale, stream);
+                  S_q, S_kv, D, causal, scale, false, stream);
 }
 
-size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q) {
+attn_status_t attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t workspace_bytes, int B,
+                                     int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                                     float scale, attn_stream_t stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv,
+                  S_q, S_kv, D, causal, scale, true, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int D) {
   if (B <= 0 || H_q <= 0 || H_kv <= 0 || S_q <= 0 || H_q % H_kv != 0) return 0;
-  return bwd_workspace_bytes(B, H_q, H_kv, S_q);
+  if (D != 64 && D != 128) return 0;
+  return bwd_workspace_bytes(B, H_q, H_kv, S_q, D);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,

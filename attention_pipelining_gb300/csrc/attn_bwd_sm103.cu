@@ -46,6 +46,7 @@ __device__ int g_bwd_status = 0;
 namespace {
 
 constexpr int kThreadsB = 384;
+constexpr int kThreadsFused = 512;  // the dK/dV kernel with dQ: + the dQ read-out warpgroup
 constexpr int kRows = 128;       // rows of a tile: keys (dK/dV kernel) or queries (dQ kernel)
 constexpr uint32_t kAll = 0xffffffffu;
 
@@ -140,6 +141,40 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
   }
 }
 
+// dQ^T[tmem, 128 x 64 fp32] = K^T dS^T_h (D = 128): M = the head
+// dimension (lanes), N = the half's 64 queries, K = the block's 128 keys.
+// A is the K tile used MN-major (its rows are keys, the head dimension
+// contiguous; the two 64-column slabs along M one slab apart), B the half's
+// dS^T buffer used MN-major (rows are keys, 64 queries contiguous).  Per K
+// step of 16 keys both starts advance 16 rows = 2048 bytes.  Overwrites the
+// accumulator.
+__device__ __forceinline__ void issue_dqt_half(uint32_t d_tmem, uint64_t k_desc_mn,
+                                               uint64_t ds_desc_mn) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64, true, true);
+#pragma unroll
+  for (int kk = 0; kk < kRows / 16; ++kk) {
+    const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+    mma_ss(d_tmem, k_desc_mn + off, ds_desc_mn + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// dK[tmem, 128 x D fp32] (+)= dS^T_h Q_h with dS^T_h read from its shared
+// buffer as a K-major A operand (rows = keys, the half's 64 queries
+// contiguous: per K step of 16 queries the start advances 32 bytes inside
+// the swizzle row) and Q_h rows 64h..64h+63 of the stage's Q tile used
+// MN-major, as in issue_pv_half.
+template <int D>
+__device__ __forceinline__ void issue_dk_half_ss(uint32_t d_tmem, uint64_t ds_desc_k,
+                                                 uint64_t b_desc, int h, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    mma_ss(d_tmem, ds_desc_k + (uint64_t)((kk * 32) >> 4),
+           b_desc + (uint64_t)(((4 * h + kk) * 2048) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = TileShape<D>::kBytes;
@@ -150,10 +185,16 @@ struct BwdCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQRing = 2 * kTileBytes;
-  static constexpr int kOffBarKV = kOffQRing + kQStages * kQStageBytes;
+  // dK/dV kernel with dQ (kFuse): dS^T of one half block, [128 keys x 64
+  // queries] bf16 in the 128-byte swizzle (one slab), the A operand of
+  // dK += dS^T Q (K-major) and the B operand of dQ^T = K^T dS^T (MN-major)
+  static constexpr int kDsBytes = kRows * 64 * 2;
+  static constexpr int kOffDsT = kOffQRing + kQStages * kQStageBytes;
+  static constexpr int kOffBarKV = kOffDsT + kDsBytes;
   // kv_full, q_full[S], q_empty[S], sp_full[2], ps_ready[2], acc_done, drain,
-  // kt_ready (K and V copied into tensor memory; D = 64)
-  static constexpr int kNumBarsKV = 2 * kQStages + 8;
+  // kt_ready (K and V copied into tensor memory; D = 64), then with kFuse
+  // dq_full[2], dq_free[2], ds_free
+  static constexpr int kNumBarsKV = 2 * kQStages + 8 + 5;
   // dK/dV kernel at D = 64: K and V as tensor-memory A operands too (D / 2
   // columns each after the two accumulators; at D = 128 there is no room)
   static constexpr bool kKVinTmem = (D == 64);
@@ -172,7 +213,9 @@ struct BwdCfg {
   static constexpr int kSmemQ = kOffMiscQ + 16 + 1024;
   // tensor memory: S (or S^T) [0,128), dP [128,256), accumulators after;
   // the dQ kernel keeps Q and dO as A operands (D / 2 columns each) after its
-  // one accumulator
+  // one accumulator.  The dK/dV kernel places the two halves as slots of
+  // 128 columns instead: half h's S^T at 128 h, its dP^T at 128 h + 64 (and,
+  // with kFuse, the half's dQ^T over the dP^T columns once they are read).
   static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
   static constexpr uint32_t kTmQt = 256 + D, kTmDOt = 256 + D + D / 2;
   static_assert(kTmDOt + D / 2 <= 512, "tensor memory budget of the dQ kernel");
@@ -222,7 +265,8 @@ __device__ __forceinline__ void banded_rank(int idx, int n_ranks, int groups, in
 // ---------------------------------------------------------------- prep
 
 // D_i = dO_i . O_i and LSE_i * log2(e), per row of the padded per-group
-// layout [groups, Rp] (rows R..Rp-1 of a group get 0).  A warp takes
+// layout [groups, Rp] (rows R..Rp-1 of a group get 0); with the fused dQ
+// also zeros for the row's D fp32 accumulators.  A warp takes
 // kPrepRowsPerWarp consecutive rows; a lane reads 16 bytes of O and of dO
 // per row, and every load of the warp's rows is issued before any product,
 // so each thread keeps several loads in flight (the kernel streams O and dO
@@ -272,6 +316,11 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
 #pragma unroll
     for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kAll, acc, off);
     const long long row = row0 + i * kRowsPerLoad + sub;
+    if (p.dq_acc != nullptr && row < total) {
+      float4* acc = reinterpret_cast<float4*>(p.dq_acc + row * D + piece * 8);
+      acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (piece == 0 && row < total) {
       const long long z = row / p.Rp;
       const int rho = (int)(row - z * p.Rp);
@@ -286,10 +335,40 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p,
   }
 }
 
+// dq = bf16(scale * dq_acc) over the rows of every group (padding rows
+// skipped); one thread per 8 elements.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const BwdParams p) {
+  constexpr int kPieces = D / 8;
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long total = (long long)p.groups * p.R * kPieces;
+  if (i >= total) return;
+  const long long row = i / kPieces;   // z * R + rho
+  const int piece = (int)(i - row * kPieces);
+  const long long z = row / p.R;
+  const long long rho = row - z * p.R;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + (z * p.Rp + rho) * D + piece * 8);
+  const float4 a = src[0], b = src[1];
+  const float sc = p.scale;
+  uint4 out;
+  out.x = pack_bf16x2(a.x * sc, a.y * sc);
+  out.y = pack_bf16x2(a.z * sc, a.w * sc);
+  out.z = pack_bf16x2(b.x * sc, b.y * sc);
+  out.w = pack_bf16x2(b.z * sc, b.w * sc);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + row * D + piece * 8) = out;
+}
+
 // ---------------------------------------------------------------- dK, dV
 
-template <int D>
-__global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+// kFuse (D = 128): dQ too.  Per half block the tensor core also computes
+// dQ^T = K^T dS^T (dS^T from a shared buffer the elementwise warps write)
+// into the half's dP^T columns, and warps 12-15 read it out and add it into
+// the fp32 accumulator p.dq_acc in L2 (red.global.add), while dK takes its
+// A operand from the same shared buffer.  512 threads then.
+template <int D, bool kFuse>
+__global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  static_assert(!kFuse || D == 128, "the fused dQ is built for D = 128");
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw_b[];
   uint8_t* smem = align_smem_1024(smem_raw_b);
@@ -302,6 +381,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   uint64_t* acc_done = sp_full + 4;
   uint64_t* drain = sp_full + 5;
   uint64_t* kt_ready = sp_full + 6;            // K and V copied into tensor memory (D = 64)
+  uint64_t* dq_full = sp_full + 7;             // [half]: dQ^T of the half computed (kFuse)
+  uint64_t* dq_free = sp_full + 9;             // [half]: dQ^T of the half read out (kFuse)
+  uint64_t* ds_free = sp_full + 11;            // the GEMMs reading the dS^T buffer are done
+  uint8_t* sDsT = smem + C::kOffDsT;
   uint32_t* sTmemBase = reinterpret_cast<uint32_t*>(smem + C::kOffMiscKV);
   volatile int* sAbort = reinterpret_cast<volatile int*>(smem + C::kOffMiscKV + 4);
   const int warp = threadIdx.x >> 5;
@@ -322,6 +405,12 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
   }
   const int kv0 = kvb * kRows;              // first key of the block
   const int n_qb = (p.R + kRows - 1) / kRows;
+  // the order every role walks the query blocks in: with kFuse and no mask
+  // rotated by the key block, so the CTAs running at once add into
+  // different dQ rows (with the causal mask each key block starts at its own
+  // diagonal anyway)
+  const int rot = (kFuse && !p.causal) ? kvb % n_qb : 0;
+  auto qb_at = [&](int i) { return i + rot < n_qb ? i + rot : i + rot - n_qb; };
   // query blocks with work, counted once here (every role walks the same list)
   int n_work = 0;
   for (int qb = 0; qb < n_qb; ++qb) n_work += qblock_sees(p, qb * kRows, kv0) ? 1 : 0;
@@ -339,6 +428,11 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     mbar_init(kt_ready, 2 * 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&dq_full[h], 1);
+      mbar_init(&dq_free[h], 128);
+    }
+    mbar_init(ds_free, 1);
     *sAbort = 0;
     fence_mbar_init();
   }
@@ -386,8 +480,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
       }
     }
     int n = 0;
-    for (int qb = 0; qb < n_qb && ok; ++qb) {
-      const int r0 = qb * kRows;
+    for (int i = 0; i < n_qb && ok; ++i) {
+      const int r0 = qb_at(i) * kRows;
       if (!qblock_sees(p, r0, kv0)) continue;
       const int s = n % C::kQStages;
       // masking: rows past R, keys past S_kv, and (causal) keys after a row's
@@ -410,9 +504,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         }
         tc_fence_after_sync();
         const int col0 = 64 * h + 32 * w;            // first query of this thread's slice
+        const uint32_t cS = 128 * h + 32 * w;        // its S^T columns (dP^T: + 64)
         uint32_t sv[32], dp[32];
-        tmem_ld_x32(tmem + lane_base + C::kTmS + col0, sv);
-        tmem_ld_x32(tmem + lane_base + C::kTmDP + col0, dp);
+        tmem_ld_x32(tmem + lane_base + cS, sv);
+        tmem_ld_x32(tmem + lane_base + cS + 64, dp);
         const float4* lse4 = reinterpret_cast<const float4*>(stage_lse(s) + col0);
         const float4* dl4 = reinterpret_cast<const float4*>(stage_delta(s) + col0);
         tmem_ld_wait();
@@ -475,10 +570,28 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
           body(std::true_type{});
         else
           body(std::false_type{});
-        // P^T and dS^T of the slice: 16 columns from col0 in the S^T and
-        // dP^T regions (this warpgroup's own, already-read columns)
-        tmem_st_x16(tmem + lane_base + C::kTmS + col0, pk);
-        tmem_st_x16(tmem + lane_base + C::kTmDP + col0, dk);
+        // P^T of the slice: 16 columns from its S^T columns (this
+        // warpgroup's own, already read)
+        tmem_st_x16(tmem + lane_base + cS, pk);
+        if constexpr (kFuse) {
+          // dS^T of the slice into the shared buffer (row = key, this
+          // warpgroup's 32 queries = 16-byte pieces 4w .. 4w + 3 of the
+          // swizzled row), once the previous half's GEMMs have read it
+          const int nh = 2 * n + h;
+          if (nh > 0 && !warp_wait_b(ds_free, (nh - 1) & 1, sAbort, budget)) {
+            ok = false;
+            break;
+          }
+          const uint32_t row = smem_u32(sDsT) + (uint32_t)r * 128u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(row + 16u * (uint32_t)((4 * w + j) ^ (r & 7)), dk[4 * j], dk[4 * j + 1],
+                         dk[4 * j + 2], dk[4 * j + 3]);
+          fence_proxy_async_smem();  // the tensor core reads it through the async proxy
+        } else {
+          // dS^T over the slice's dP^T columns, likewise
+          tmem_st_x16(tmem + lane_base + cS + 64, dk);
+        }
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&ps_ready[h]);
@@ -530,7 +643,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
     const bool leader = elect_one();
     const uint64_t dK = kmajor_tile_desc(smem_u32(sK));
     const uint64_t dV = kmajor_tile_desc(smem_u32(sV));
-    const uint32_t tS = tmem + C::kTmS, tDP = tmem + C::kTmDP;
+    // half h's slot: S^T (then P^T) at 128 h, dP^T (then dQ^T) at 128 h + 64
+    const uint32_t tS = tmem, tDP = tmem + 64;
     const uint32_t tdV = tmem + C::kTmAcc0, tdK = tmem + C::kTmAcc1;
     bool ok = n_work > 0 &&
               warp_wait_b(C::kKVinTmem ? kt_ready : kv_full, 0, sAbort, budget);
@@ -540,11 +654,11 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
       const int s = n % C::kQStages;
       if (leader) {
         if constexpr (C::kKVinTmem) {
-          issue_qk_half_ts<D>(tS + 64 * h, tmem + C::kTmKt, kmajor_tile_desc(smem_u32(stage_q(s))), h);
-          issue_qk_half_ts<D>(tDP + 64 * h, tmem + C::kTmVt, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+          issue_qk_half_ts<D>(tS + 128 * h, tmem + C::kTmKt, kmajor_tile_desc(smem_u32(stage_q(s))), h);
+          issue_qk_half_ts<D>(tDP + 128 * h, tmem + C::kTmVt, kmajor_tile_desc(smem_u32(stage_do(s))), h);
         } else {
-          issue_qk_half<D>(tS + 64 * h, dK, kmajor_tile_desc(smem_u32(stage_q(s))), h);
-          issue_qk_half<D>(tDP + 64 * h, dV, kmajor_tile_desc(smem_u32(stage_do(s))), h);
+          issue_qk_half<D>(tS + 128 * h, dK, kmajor_tile_desc(smem_u32(stage_q(s))), h);
+          issue_qk_half<D>(tDP + 128 * h, dV, kmajor_tile_desc(smem_u32(stage_do(s))), h);
         }
         tc_commit(&sp_full[h]);
       }
@@ -563,11 +677,23 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         if (!warp_wait_b(&ps_ready[h], n & 1, sAbort, budget)) { ok = false; break; }
         tc_fence_after_sync();
         if (leader) {
+          if constexpr (kFuse) {
+            // dQ^T = K^T dS^T first, so its read-out overlaps the next two
+            issue_dqt_half(tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(sK)),
+                           mnmajor_tile_desc<64>(smem_u32(sDsT)));
+            tc_commit(&dq_full[h]);
+          }
           // dV += P^T dO and dK += dS^T Q over this half's 64 queries
-          issue_pv_half<D>(tdV, tS + 64 * h, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), h,
+          issue_pv_half<D>(tdV, tS + 128 * h, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), h,
                            n > 0 || h > 0);
-          issue_pv_half<D>(tdK, tDP + 64 * h, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h,
-                           n > 0 || h > 0);
+          if constexpr (kFuse) {
+            issue_dk_half_ss<D>(tdK, kmajor_tile_desc(smem_u32(sDsT)),
+                                mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h, n > 0 || h > 0);
+            tc_commit(ds_free);                // the dS^T buffer may be rewritten
+          } else {
+            issue_pv_half<D>(tdK, tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h,
+                             n > 0 || h > 0);
+          }
           if (h == 1) tc_commit(&q_empty[s]);  // both halves read: the stage is free
         }
         // the next item's half h overwrites what these GEMMs read: issued
@@ -579,6 +705,11 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
               ok = false;
               break;
             }
+            tc_fence_after_sync();
+          }
+          if constexpr (kFuse) {
+            // ... and over this half's dQ^T once it has been read out
+            if (!warp_wait_b(&dq_free[h], n & 1, sAbort, budget)) { ok = false; break; }
             tc_fence_after_sync();
           }
           issue_sp(n + 1, h);
@@ -603,8 +734,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
       tma_load_tile<D>(sK, &p.tm_k, kv_full, kv0, zkv, pol_kv);
       tma_load_tile<D>(sV, &p.tm_v, kv_full, kv0, zkv, pol_kv);
     }
-    for (int qb = 0; qb < n_qb && ok; ++qb) {
-      const int r0 = qb * kRows;
+    for (int i = 0; i < n_qb && ok; ++i) {
+      const int r0 = qb_at(i) * kRows;
       if (!qblock_sees(p, r0, kv0)) continue;
       const int s = issued % C::kQStages;
       const int round = issued / C::kQStages;
@@ -629,6 +760,43 @@ __global__ void __launch_bounds__(kThreadsB, 1) attn_bwd_dkdv_kernel(const __gri
         drain_wait_b(&q_full[t % C::kQStages], (t / C::kQStages) & 1, budget);
     }
     __syncwarp();
+  } else if (kFuse && warp >= 12) {
+    // -------------------------------------------------------- dQ read-out
+    // thread = TMEM lane = head dimension d; per half block it takes the 64
+    // queries' dQ^T values of its d and adds them into rows r0 + 64 h + j of
+    // the group's fp32 accumulator (a warp's 32 lanes cover 128 contiguous
+    // bytes of a row)
+    const int d = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    int n = 0;
+    for (int i = 0; i < n_qb && ok; ++i) {
+      const int r0 = qb_at(i) * kRows;
+      if (!qblock_sees(p, r0, kv0)) continue;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait_b(&dq_full[h], n & 1, sAbort, budget)) { ok = false; break; }
+        tc_fence_after_sync();
+        uint32_t v0[32], v1[32];
+        tmem_ld_x32(tmem + lane_base + 128 * h + 64, v0);
+        tmem_ld_x32(tmem + lane_base + 128 * h + 96, v1);
+        tmem_ld_wait();
+        reg_after_wait(v0);
+        reg_after_wait(v1);
+        tc_fence_before_sync();
+        mbar_arrive(&dq_free[h]);            // the columns may be overwritten
+        const int q0 = r0 + 64 * h;
+        const int rows = p.R - q0;           // rows past R are padding: skipped
+        float* dst = p.dq_acc + ((size_t)zkv * p.Rp + q0) * D + d;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < rows) red_add_f32(dst + (size_t)j * D, u2f_b(v0[j]));
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 + j < rows) red_add_f32(dst + (size_t)(32 + j) * D, u2f_b(v1[j]));
+      }
+      ++n;
+    }
   }
 
   tc_fence_before_sync();
@@ -916,6 +1084,16 @@ namespace {
 std::mutex g_bwd_mu;
 bool g_bwd_attr[2][64] = {};  // [D == 128][device]
 
+template <int D, bool kFuse>
+cudaError_t set_dkdv_attr() {
+  if constexpr (kFuse && D != 128) {
+    return cudaSuccess;
+  } else {
+    return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kFuse>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemKV);
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, const float* lse,
                          cudaStream_t stream) {
@@ -927,8 +1105,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, co
   {
     std::lock_guard<std::mutex> lk(g_bwd_mu);
     if (!g_bwd_attr[D == 128][dev]) {
-      err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemKV);
+      err = set_dkdv_attr<D, false>();
+      if (err != cudaSuccess) return err;
+      err = set_dkdv_attr<D, true>();
       if (err != cudaSuccess) return err;
       err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemQ);
@@ -944,7 +1123,18 @@ cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, co
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned grid_kv = (unsigned)((p.S_kv + kRows - 1) / kRows) * (unsigned)p.groups;
-  attn_bwd_dkdv_kernel<D><<<grid_kv, kThreadsB, C::kSmemKV, stream>>>(p);
+  if constexpr (D == 128) {
+    if (p.dq_acc != nullptr) {
+      attn_bwd_dkdv_kernel<D, true><<<grid_kv, kThreadsFused, C::kSmemKV, stream>>>(p);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+      const long long pieces = (long long)p.groups * p.R * (D / 8);
+      attn_bwd_dq_convert_kernel<D><<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(p);
+      return cudaGetLastError();
+    }
+  }
+  if (p.dq_acc != nullptr) return cudaErrorInvalidValue;  // the fused dQ is built for D = 128
+  attn_bwd_dkdv_kernel<D, false><<<grid_kv, kThreadsB, C::kSmemKV, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned grid_q = (unsigned)((p.R + kRows - 1) / kRows) * (unsigned)p.groups;

@@ -89,13 +89,19 @@ struct BwdParams {
   float* nlse2;       // [groups, Rp]: -LSE * log2(e) (workspace; negated so the
                       // kernels' products and sums map onto packed fma / add)
   float* ndelta;      // [groups, Rp]: -D_i = -(dO_i . O_i) (workspace)
+  // [groups, Rp, D] fp32 dQ accumulator (workspace): set for the fused path
+  // (the dK/dV kernel adds dS K into it, a last kernel scales and rounds it
+  // into dq); nullptr for the three-kernel path (dQ by its own kernel)
+  float* dq_acc;
   int B, H_q, H_kv, S_q, S_kv, causal;
   int R, Rp, groups;
   float scale, scale_log2;
   unsigned long long timeout_ns;
 };
 
-// Queues the three backward kernels (D_i, dK/dV, dQ) on `stream`.
+// Queues the backward on `stream`: with p.dq_acc set (D = 128) prep (which
+// also clears dq_acc), dK/dV with dQ, and the dQ conversion; otherwise prep,
+// dK/dV and dQ.
 cudaError_t launch_attn_bwd(const BwdParams& p, int D, const void* o, const void* dout,
                             const float* lse, cudaStream_t stream);
 

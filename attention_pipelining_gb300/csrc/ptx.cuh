@@ -300,6 +300,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Adds x to the fp32 at `addr` in global memory, performed in L2 (no
+// return value; relaxed, device scope).
+__device__ __forceinline__ void red_add_f32(float* addr, float x) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -547,7 +547,7 @@ def run_bwd(args, w):
     q, k, v, dout = (t.to(dev) for t in (q_cpu, k_cpu, v_cpu, do_cpu))
     o, lse = ap.attn_fwd(q, k, v, w.causal, w.scale)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(ap.bwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q), dtype=torch.uint8,
+    ws = torch.empty(ap.bwd_workspace_bytes(w.B, w.H_q, w.H_kv, w.S_q, w.D), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.current_stream(dev)
 

@@ -202,11 +202,18 @@ size_t attn_splitkv_noalloc_capacity(void);
  *   dq          [B, H_q, S_q, D] bf16, device, written
  *   dk, dv      [B, H_kv, S_kv, D] bf16, device, written
  *   workspace   caller-owned device scratch, 256-byte aligned, of at least
- *               attn_bwd_workspace_bytes(B, H_q, H_kv, S_q) bytes (per-row
- *               D_i and LSE; no need to clear it)
+ *               attn_bwd_workspace_bytes(B, H_q, H_kv, S_q, D) bytes (per-row
+ *               D_i and LSE, and an fp32 dQ accumulator; no need to clear it)
  *
  * Arithmetic: bf16 operands, fp32 accumulation; P and dS are rounded to
- * bf16 before the GEMMs that consume them.  Three kernels are queued on
+ * bf16 before the GEMMs that consume them.  At D = 128 dQ is computed in the
+ * same kernel as dK and dV: each (key block, query block) pair adds its fp32
+ * partial dS K into the accumulator in the workspace with atomic adds in L2,
+ * and a last kernel scales and rounds it to bf16.  The order of those adds
+ * varies from run to run, so dQ may differ in its last bit between runs
+ * (dK and dV do not); attn_bwd_deterministic gives reproducible bits.  At
+ * D = 64 (and in attn_bwd_deterministic) dQ has a kernel of its own that
+ * recomputes S and dP per query block.  Three kernels are queued on
  * `stream`; the workspace must not be shared with concurrent calls.  Errors
  * as attn_fwd, plus ATTN_ERR_INVALID_ARG for a null dout / dq / dk / dv /
  * workspace or a too small workspace, and ATTN_ERR_MISALIGNED for a workspace
@@ -217,8 +224,22 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
                        void *workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
                        int S_q, int S_kv, int D, int causal, float scale, attn_stream_t stream);
 
-/* Workspace bytes attn_bwd needs (0 if the arguments are invalid). */
-size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
+/*
+ * attn_bwd with bit-reproducible results: dQ by its own kernel, which
+ * recomputes S and dP per query block (two more GEMMs per block pair than
+ * attn_bwd at D = 128), with no atomic adds.  Arguments, workspace and
+ * errors as attn_bwd.
+ */
+attn_status_t attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dout, void *dq, void *dk,
+                                     void *dv, void *workspace, size_t workspace_bytes, int B,
+                                     int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                                     float scale, attn_stream_t stream);
+
+/* Workspace bytes attn_bwd and attn_bwd_deterministic need (0 if the
+ * arguments are invalid): 4 (D + 2) bytes per query row, rows padded to a
+ * multiple of 128 per (batch, kv-head) group. */
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q, int D);
 
 /*
  * attn_bwd with host inputs and outputs, pipelined as attn_fwd_host is:
@@ -232,7 +253,8 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int S_q);
  * its own slice of `workspace`, and its gradients come back on another, so
  * each chunk's copies overlap the other chunks' kernels.  Every gradient
  * element is computed by the same tiles in the same order as in one
- * attn_bwd call, so the results are bit-identical to it.  Host buffers
+ * attn_bwd call, so dK and dV are bit-identical to it and dQ is up to the
+ * order of its atomic adds (see attn_bwd).  Host buffers
  * should be page-locked for the copies to be asynchronous.  Returns once
  * everything is queued; the host gradients are valid once `stream` has
  * been synchronised.  Argument rules and errors as attn_bwd for the device

@@ -96,7 +96,7 @@ def test_bwd_host_entry_rejects_before_queuing(lib):
     """attn_bwd_host: a null host buffer, then the device-side rules of
     attn_bwd (fake, never-dereferenced device addresses), all on the host."""
     dims = [1, 4, 2, 128, 128, 128, 0, ctypes.c_float(0.1), None]
-    ws_bytes = lib.attn_bwd_workspace_bytes(1, 4, 2, 128)
+    ws_bytes = lib.attn_bwd_workspace_bytes(1, 4, 2, 128, 128)
     assert ws_bytes > 0
 
     def call(host=None, dev=None, ws=A, nbytes=ws_bytes, d=dims):
