@@ -158,23 +158,6 @@ __device__ __forceinline__ void issue_dqt_half(uint32_t d_tmem, uint64_t k_desc_
   }
 }
 
-// dK[tmem, 128 x D fp32] (+)= dS^T_h Q_h with dS^T_h read from its shared
-// buffer as a K-major A operand (rows = keys, the half's 64 queries
-// contiguous: per K step of 16 queries the start advances 32 bytes inside
-// the swizzle row) and Q_h rows 64h..64h+63 of the stage's Q tile used
-// MN-major, as in issue_pv_half.
-template <int D>
-__device__ __forceinline__ void issue_dk_half_ss(uint32_t d_tmem, uint64_t ds_desc_k,
-                                                 uint64_t b_desc, int h, bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16_f32(128, D, false, true);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    mma_ss(d_tmem, ds_desc_k + (uint64_t)((kk * 32) >> 4),
-           b_desc + (uint64_t)(((4 * h + kk) * 2048) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
-}
-
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = TileShape<D>::kBytes;
@@ -186,8 +169,8 @@ struct BwdCfg {
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQRing = 2 * kTileBytes;
   // dK/dV kernel with dQ (kFuse): dS^T of one half block, [128 keys x 64
-  // queries] bf16 in the 128-byte swizzle (one slab), the A operand of
-  // dK += dS^T Q (K-major) and the B operand of dQ^T = K^T dS^T (MN-major)
+  // queries] bf16 in the 128-byte swizzle (one slab), the B operand of
+  // dQ^T = K^T dS^T (MN-major)
   static constexpr int kDsBytes = kRows * 64 * 2;
   static constexpr int kOffDsT = kOffQRing + kQStages * kQStageBytes;
   static constexpr int kOffBarKV = kOffDsT + kDsBytes;
@@ -363,8 +346,8 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const BwdParam
 // kFuse (D = 128): dQ too.  Per half block the tensor core also computes
 // dQ^T = K^T dS^T (dS^T from a shared buffer the elementwise warps write)
 // into the half's dP^T columns, and warps 12-15 read it out and add it into
-// the fp32 accumulator p.dq_acc in L2 (red.global.add), while dK takes its
-// A operand from the same shared buffer.  512 threads then.
+// the fp32 accumulator p.dq_acc in L2 (red.global.add); dS^T for dK then
+// sits in tensor memory next to P^T.  512 threads.
 template <int D, bool kFuse>
 __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -588,6 +571,9 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
             st_shared_v4(row + 16u * (uint32_t)((4 * w + j) ^ (r & 7)), dk[4 * j], dk[4 * j + 1],
                          dk[4 * j + 2], dk[4 * j + 3]);
           fence_proxy_async_smem();  // the tensor core reads it through the async proxy
+          // and into the slice's own S^T columns 16-31 (dK's A operand): the
+          // half's dP^T columns take dQ^T
+          tmem_st_x16(tmem + lane_base + cS + 16, dk);
         } else {
           // dS^T over the slice's dP^T columns, likewise
           tmem_st_x16(tmem + lane_base + cS + 64, dk);
@@ -678,22 +664,20 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
         tc_fence_after_sync();
         if (leader) {
           if constexpr (kFuse) {
-            // dQ^T = K^T dS^T first, so its read-out overlaps the next two
+            // dQ^T = K^T dS^T first, so its read-out overlaps the next two;
+            // it is the only reader of the dS^T buffer
             issue_dqt_half(tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(sK)),
                            mnmajor_tile_desc<64>(smem_u32(sDsT)));
             tc_commit(&dq_full[h]);
+            tc_commit(ds_free);
           }
-          // dV += P^T dO and dK += dS^T Q over this half's 64 queries
+          // dV += P^T dO and dK += dS^T Q over this half's 64 queries; with
+          // kFuse dS^T sits in the S^T columns next to P^T (columns 16-31 of
+          // each warpgroup's 32), otherwise over the dP^T columns
           issue_pv_half<D>(tdV, tS + 128 * h, mnmajor_tile_desc<D>(smem_u32(stage_do(s))), h,
                            n > 0 || h > 0);
-          if constexpr (kFuse) {
-            issue_dk_half_ss<D>(tdK, kmajor_tile_desc(smem_u32(sDsT)),
-                                mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h, n > 0 || h > 0);
-            tc_commit(ds_free);                // the dS^T buffer may be rewritten
-          } else {
-            issue_pv_half<D>(tdK, tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h,
-                             n > 0 || h > 0);
-          }
+          issue_pv_half<D>(tdK, kFuse ? tS + 128 * h + 16 : tDP + 128 * h,
+                           mnmajor_tile_desc<D>(smem_u32(stage_q(s))), h, n > 0 || h > 0);
           if (h == 1) tc_commit(&q_empty[s]);  // both halves read: the stage is free
         }
         // the next item's half h overwrites what these GEMMs read: issued
