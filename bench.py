@@ -528,10 +528,12 @@ def run_ours(args, w):
 
 
 def run_bwd(args, w):
-    """The backward (attn_bwd: three kernels) on the same workload: one step =
-    dQ, dK, dV for one upstream gradient, inputs (q, k, v, O, LSE, dO)
-    resident in HBM.  FLOPs: the five GEMMs of a FlashAttention backward,
-    2.5 x the forward's count (halved when causal)."""
+    """The backward on the same workload: one step = dQ, dK, dV for one
+    upstream gradient, inputs (q, k, v, O, LSE, dO) resident in HBM.
+    attn_bwd (at D = 128: prep, dK/dV with dQ, dQ conversion), or with
+    --bwd-deterministic attn_bwd_deterministic (prep, dK/dV, dQ).  FLOPs: the
+    five GEMMs of a FlashAttention backward, 2.5 x the forward's count
+    (halved when causal)."""
     import torch
     import attention_pipelining_gb300 as ap
     from attention_pipelining_gb300.synthetic import make_workload
@@ -551,9 +553,12 @@ def run_bwd(args, w):
                      device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    det = bool(args.bwd_deterministic)
+    fused = (w.D == 128) and not det
+
     def step():
         ap.attn_bwd(q, k, v, o, lse, dout, w.causal, w.scale, workspace=ws, out=(dq, dk, dv),
-                    stream=stream)
+                    stream=stream, deterministic=det)
 
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dout, o, lse))
 
@@ -624,6 +629,7 @@ def run_bwd(args, w):
             "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
             "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
             "l2": l2_note(in_bytes, flush),
+            "path": "deterministic (dQ kernel)" if det or w.D != 128 else "fused dQ",
         },
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {
@@ -636,7 +642,9 @@ def run_bwd(args, w):
             "frac_of_sustained": achieved / peak_sustained,
             "traffic": None,
             "algorithmic_flops_per_launch": flops,
-            "kernel": "attn_bwd_prep + attn_bwd_dkdv + attn_bwd_dq, timed together",
+            "kernel": ("attn_bwd_prep + attn_bwd_dkdv (with dQ) + attn_bwd_dq_convert"
+                       if fused else "attn_bwd_prep + attn_bwd_dkdv + attn_bwd_dq") +
+                      ", timed together",
         },
         "e2e": {
             "value": world * flops * e2e_steps / t_e2e / 1e12,
@@ -854,6 +862,8 @@ def main(argv=None):
     ap_.add_argument("--trace", type=int, default=0,
                      help="print a timeline summary of the first N CTAs instead of a bench line")
     ap_.add_argument("--trace-out", default="", help="also save the raw trace (.npy)")
+    ap_.add_argument("--bwd-deterministic", action="store_true",
+                     help="--pass bwd: time attn_bwd_deterministic (dQ by its own kernel)")
     ap_.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd", "chunkscan"],
                      help="bwd: time the backward (attn_bwd) instead of the forward; "
                           "chunkscan: time the Mamba2 chunk scan (see --cs-workload)")
