@@ -316,8 +316,8 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   const int64_t Rp = bwd_padded_rows(H_q, H_kv, S_q);
   p.nlse2 = static_cast<float*>(workspace);
   p.ndelta = p.nlse2 + (size_t)B * H_kv * Rp;
-  // the fused dQ (D = 128): accumulated in the workspace's third part
-  p.dq_acc = (!deterministic && D == 128) ? p.ndelta + (size_t)B * H_kv * Rp : nullptr;
+  // the fused dQ: accumulated in the workspace's third part
+  p.dq_acc = deterministic ? nullptr : p.ndelta + (size_t)B * H_kv * Rp;
   p.B = B;
   p.H_q = H_q;
   p.H_kv = H_kv;

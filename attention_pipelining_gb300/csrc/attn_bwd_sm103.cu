@@ -141,16 +141,20 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
   }
 }
 
-// dQ^T[tmem, 128 x 64 fp32] = K^T dS^T_h (D = 128): M = the head
-// dimension (lanes), N = the half's 64 queries, K = the block's 128 keys.
-// A is the K tile used MN-major (its rows are keys, the head dimension
-// contiguous; the two 64-column slabs along M one slab apart), B the half's
-// dS^T buffer used MN-major (rows are keys, 64 queries contiguous).  Per K
-// step of 16 keys both starts advance 16 rows = 2048 bytes.  Overwrites the
-// accumulator.
+// dQ^T[tmem, D x 64 fp32] = K^T dS^T_h: M = the head dimension, N = the
+// half's 64 queries, K = the block's 128 keys.  A is the K tile used
+// MN-major (its rows are keys, the head dimension contiguous; at D = 128
+// the two 64-column slabs along M one slab apart), B the half's dS^T buffer
+// used MN-major (rows are keys, 64 queries contiguous).  Per K step of 16
+// keys both starts advance 16 rows = 2048 bytes.  Overwrites the
+// accumulator.  Row d lands in tensor-memory lane d for D = 128; for M = 64
+// rows 16 q .. 16 q + 15 land in lanes 32 q .. 32 q + 15 (measured on
+// GB300 with a one-MMA probe: the other 16 lanes of each quadrant are not
+// part of the result).
+template <int D>
 __device__ __forceinline__ void issue_dqt_half(uint32_t d_tmem, uint64_t k_desc_mn,
                                                uint64_t ds_desc_mn) {
-  constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64, true, true);
+  constexpr uint32_t idesc = make_idesc_bf16_f32(D, 64, true, true);
 #pragma unroll
   for (int kk = 0; kk < kRows / 16; ++kk) {
     const uint64_t off = (uint64_t)((kk * 2048) >> 4);
@@ -173,7 +177,12 @@ struct BwdCfg {
   // dQ^T = K^T dS^T (MN-major)
   static constexpr int kDsBytes = kRows * 64 * 2;
   static constexpr int kOffDsT = kOffQRing + kQStages * kQStageBytes;
-  static constexpr int kOffBarKV = kOffDsT + kDsBytes;
+  // ... and at D = 64 two staging buffers for a half block's dQ partial,
+  // [64 queries][64] fp32 each (the accumulator's own row layout), which one
+  // bulk reduction adds into it
+  static constexpr int kDqStageBytes = (D == 64) ? 64 * D * 4 : 0;
+  static constexpr int kOffDqStage = kOffDsT + kDsBytes;
+  static constexpr int kOffBarKV = kOffDqStage + 2 * kDqStageBytes;
   // kv_full, q_full[S], q_empty[S], sp_full[2], ps_ready[2], acc_done, drain,
   // kt_ready (K and V copied into tensor memory; D = 64), then with kFuse
   // dq_full[2], dq_free[2], ds_free
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const BwdParam
 
 // ---------------------------------------------------------------- dK, dV
 
-// kFuse (D = 128): dQ too.  Per half block the tensor core also computes
+// kFuse: dQ too.  Per half block the tensor core also computes
 // dQ^T = K^T dS^T (dS^T from a shared buffer the elementwise warps write)
 // into the half's dP^T columns, and warps 12-15 read it out and add it into
 // the fp32 accumulator p.dq_acc in L2 (red.global.add); dS^T for dK then
@@ -351,7 +360,6 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const BwdParam
 template <int D, bool kFuse>
 __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-  static_assert(!kFuse || D == 128, "the fused dQ is built for D = 128");
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw_b[];
   uint8_t* smem = align_smem_1024(smem_raw_b);
@@ -666,8 +674,8 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
           if constexpr (kFuse) {
             // dQ^T = K^T dS^T first, so its read-out overlaps the next two;
             // it is the only reader of the dS^T buffer
-            issue_dqt_half(tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(sK)),
-                           mnmajor_tile_desc<64>(smem_u32(sDsT)));
+            issue_dqt_half<D>(tDP + 128 * h, mnmajor_tile_desc<D>(smem_u32(sK)),
+                              mnmajor_tile_desc<64>(smem_u32(sDsT)));
             tc_commit(&dq_full[h]);
             tc_commit(ds_free);
           }
@@ -746,11 +754,19 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
     __syncwarp();
   } else if (kFuse && warp >= 12) {
     // -------------------------------------------------------- dQ read-out
-    // thread = TMEM lane = head dimension d; per half block it takes the 64
-    // queries' dQ^T values of its d and adds them into rows r0 + 64 h + j of
-    // the group's fp32 accumulator (a warp's 32 lanes cover 128 contiguous
+    // thread = TMEM lane = head dimension d (D = 64: lanes 0-15 of each
+    // quadrant, d = 16 q + lane); per half block it takes the 64 queries'
+    // dQ^T values of its d and adds them into rows r0 + 64 h + j of the
+    // group's fp32 accumulator (a warp's lanes cover 128 or 64 contiguous
     // bytes of a row)
-    const int d = (warp & 3) * 32 + lane;
+    const bool has_d = (D == 128) || lane < 16;
+    const int d = (D == 128) ? (warp & 3) * 32 + lane : (warp & 3) * 16 + (lane & 15);
+    // D = 64: a warp's red would carry 64 bytes only, and the L2 takes
+    // requests at a bounded rate whatever their size; instead the half's
+    // values go to a staging buffer and one thread adds all 16 KB with a
+    // bulk reduction (one bulk group per half block; two buffers)
+    float* sStage = reinterpret_cast<float*>(smem + C::kOffDqStage);
+    int nh = 0;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     int n = 0;
@@ -759,7 +775,19 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
       if (!qblock_sees(p, r0, kv0)) continue;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        if (!warp_wait_b(&dq_full[h], n & 1, sAbort, budget)) { ok = false; break; }
+        if constexpr (D == 64) {
+          // the bulk reduction that read this half's staging buffer two
+          // halves ago is done (one bulk group per half)
+          if (threadIdx.x == 12 * 32) tma_store_wait_read<1>();
+        }
+        const bool got = warp_wait_b(&dq_full[h], n & 1, sAbort, budget);
+        if constexpr (D == 64) {
+          // the four warps agree (they meet at named barriers below, which
+          // no warp may skip); this also orders the buffer's reuse
+          if (barrier_or(1, 128, !got)) { ok = false; break; }
+        } else {
+          if (!got) { ok = false; break; }
+        }
         tc_fence_after_sync();
         uint32_t v0[32], v1[32];
         tmem_ld_x32(tmem + lane_base + 128 * h + 64, v0);
@@ -770,17 +798,39 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
         tc_fence_before_sync();
         mbar_arrive(&dq_free[h]);            // the columns may be overwritten
         const int q0 = r0 + 64 * h;
-        const int rows = p.R - q0;           // rows past R are padding: skipped
-        float* dst = p.dq_acc + ((size_t)zkv * p.Rp + q0) * D + d;
+        if constexpr (D == 128) {
+          const int rows = p.R - q0;           // rows past R are padding: skipped
+          float* dst = p.dq_acc + ((size_t)zkv * p.Rp + q0) * D + d;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < rows) red_add_f32(dst + (size_t)j * D, u2f_b(v0[j]));
+          for (int j = 0; j < 32; ++j)
+            if (j < rows) red_add_f32(dst + (size_t)j * D, u2f_b(v0[j]));
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (32 + j < rows) red_add_f32(dst + (size_t)(32 + j) * D, u2f_b(v1[j]));
+          for (int j = 0; j < 32; ++j)
+            if (32 + j < rows) red_add_f32(dst + (size_t)(32 + j) * D, u2f_b(v1[j]));
+        } else {
+          float* stg = sStage + (nh & 1) * 64 * D;
+          if (has_d) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[j * D + d] = u2f_b(v0[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[(32 + j) * D + d] = u2f_b(v1[j]);
+          }
+          fence_proxy_async_smem();            // the bulk copy reads through the async proxy
+          named_barrier_sync(1, 128);
+          if (threadIdx.x == 12 * 32) {
+            const int rows = min(64, p.R - q0);  // rows past R are padding: skipped
+            if (rows > 0)
+              bulk_reduce_add_f32(p.dq_acc + ((size_t)zkv * p.Rp + q0) * D, smem_u32(stg),
+                                  (uint32_t)rows * D * 4);
+            tma_store_commit();                // one group per half, possibly empty
+          }
+          ++nh;
+        }
       }
       ++n;
     }
+    // every bulk reduction has read its buffer and reached global memory
+    if (D == 64 && threadIdx.x == 12 * 32) tma_store_wait_all();
   }
 
   tc_fence_before_sync();
@@ -1070,12 +1120,8 @@ bool g_bwd_attr[2][64] = {};  // [D == 128][device]
 
 template <int D, bool kFuse>
 cudaError_t set_dkdv_attr() {
-  if constexpr (kFuse && D != 128) {
-    return cudaSuccess;
-  } else {
-    return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kFuse>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemKV);
-  }
+  return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kFuse>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemKV);
 }
 
 template <int D>
@@ -1107,17 +1153,14 @@ cudaError_t launch_bwd_d(const BwdParams& p, const void* o, const void* dout, co
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned grid_kv = (unsigned)((p.S_kv + kRows - 1) / kRows) * (unsigned)p.groups;
-  if constexpr (D == 128) {
-    if (p.dq_acc != nullptr) {
-      attn_bwd_dkdv_kernel<D, true><<<grid_kv, kThreadsFused, C::kSmemKV, stream>>>(p);
-      err = cudaGetLastError();
-      if (err != cudaSuccess) return err;
-      const long long pieces = (long long)p.groups * p.R * (D / 8);
-      attn_bwd_dq_convert_kernel<D><<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(p);
-      return cudaGetLastError();
-    }
+  if (p.dq_acc != nullptr) {
+    attn_bwd_dkdv_kernel<D, true><<<grid_kv, kThreadsFused, C::kSmemKV, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const long long pieces = (long long)p.groups * p.R * (D / 8);
+    attn_bwd_dq_convert_kernel<D><<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(p);
+    return cudaGetLastError();
   }
-  if (p.dq_acc != nullptr) return cudaErrorInvalidValue;  // the fused dQ is built for D = 128
   attn_bwd_dkdv_kernel<D, false><<<grid_kv, kThreadsB, C::kSmemKV, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -530,7 +530,7 @@ def run_ours(args, w):
 def run_bwd(args, w):
     """The backward on the same workload: one step = dQ, dK, dV for one
     upstream gradient, inputs (q, k, v, O, LSE, dO) resident in HBM.
-    attn_bwd (at D = 128: prep, dK/dV with dQ, dQ conversion), or with
+    attn_bwd (prep, dK/dV with dQ, dQ conversion), or with
     --bwd-deterministic attn_bwd_deterministic (prep, dK/dV, dQ).  FLOPs: the
     five GEMMs of a FlashAttention backward, 2.5 x the forward's count
     (halved when causal)."""
@@ -554,7 +554,7 @@ def run_bwd(args, w):
     stream = torch.cuda.current_stream(dev)
 
     det = bool(args.bwd_deterministic)
-    fused = (w.D == 128) and not det
+    fused = not det
 
     def step():
         ap.attn_bwd(q, k, v, o, lse, dout, w.causal, w.scale, workspace=ws, out=(dq, dk, dv),
@@ -629,7 +629,7 @@ def run_bwd(args, w):
             "S_kv": w.S_kv, "D": w.D, "causal": w.causal, "k_scale": w.k_scale,
             "scale": w.scale, "seed": w.seed, "parallelism": f"replicas x{world}",
             "l2": l2_note(in_bytes, flush),
-            "path": "deterministic (dQ kernel)" if det or w.D != 128 else "fused dQ",
+            "path": "deterministic (dQ kernel)" if det else "fused dQ",
         },
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {

@@ -206,14 +206,14 @@ size_t attn_splitkv_noalloc_capacity(void);
  *               D_i and LSE, and an fp32 dQ accumulator; no need to clear it)
  *
  * Arithmetic: bf16 operands, fp32 accumulation; P and dS are rounded to
- * bf16 before the GEMMs that consume them.  At D = 128 dQ is computed in the
- * same kernel as dK and dV: each (key block, query block) pair adds its fp32
+ * bf16 before the GEMMs that consume them.  dQ is computed in the same
+ * kernel as dK and dV: each (key block, query block) pair adds its fp32
  * partial dS K into the accumulator in the workspace with atomic adds in L2,
  * and a last kernel scales and rounds it to bf16.  The order of those adds
  * varies from run to run, so dQ may differ in its last bit between runs
- * (dK and dV do not); attn_bwd_deterministic gives reproducible bits.  At
- * D = 64 (and in attn_bwd_deterministic) dQ has a kernel of its own that
- * recomputes S and dP per query block.  Three kernels are queued on
+ * (dK and dV do not); attn_bwd_deterministic gives reproducible bits (there
+ * dQ has a kernel of its own that recomputes S and dP per query block).
+ * Three kernels are queued on
  * `stream`; the workspace must not be shared with concurrent calls.  Errors
  * as attn_fwd, plus ATTN_ERR_INVALID_ARG for a null dout / dq / dk / dv /
  * workspace or a too small workspace, and ATTN_ERR_MISALIGNED for a workspace
@@ -227,7 +227,7 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
 /*
  * attn_bwd with bit-reproducible results: dQ by its own kernel, which
  * recomputes S and dP per query block (two more GEMMs per block pair than
- * attn_bwd at D = 128), with no atomic adds.  Arguments, workspace and
+ * attn_bwd), with no atomic adds.  Arguments, workspace and
  * errors as attn_bwd.
  */
 attn_status_t attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
