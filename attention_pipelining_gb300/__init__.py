@@ -39,7 +39,7 @@ EXPORTS = ["attn_fwd", "attn_fwd_host", "attn_status_string", "attn_device_statu
            "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc",
            "attn_splitkv_noalloc_capacity", "attn_bwd", "attn_bwd_deterministic",
-           "attn_bwd_workspace_bytes",
+           "attn_bwd_workspace_bytes", "attn_bwd_timeout_test",
            "attn_bwd_host", "chunk_scan_fwd", "chunk_scan_fwd_host"]
 
 
@@ -106,6 +106,9 @@ def _load():
     lib.attn_bwd.restype = ci
     lib.attn_bwd_deterministic.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
     lib.attn_bwd_deterministic.restype = ci
+    lib.attn_bwd_timeout_test.argtypes = [vp] * 10 + [ctypes.c_size_t] + [ci] * 7 + [cf, ci,
+                                          ctypes.c_ulonglong, vp]
+    lib.attn_bwd_timeout_test.restype = ci
     lib.attn_bwd_host.argtypes = [vp] * 19 + [ctypes.c_size_t] + [ci] * 7 + [cf, vp]
     lib.attn_bwd_host.restype = ci
     lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
@@ -351,6 +354,27 @@ def fwd_timeout_test(q, k, v, causal: bool, scale: float, drop_block: int,
                                          float(scale), int(drop_block), int(wait_budget_ns),
                                          _stream_handle(stream)), "attn_fwd_timeout_test")
     return o, lse
+
+
+def bwd_timeout_test(q, k, v, o, lse, dout, causal: bool, scale: float, drop_item: int,
+                     wait_budget_ns: int = 20_000_000, stream=None):
+    """Test hook: runs attn_bwd with one "P^T, dS^T stored" signal withheld
+    at work item ``drop_item`` of every dK/dV CTA, so the issuer's bounded
+    wait runs out (see attn_testing.h).  Returns (dq, dk, dv); the device
+    status word then reads ATTN_ERR_TIMEOUT."""
+    import torch
+    _check_inputs(q, k, v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    ws = torch.empty(bwd_workspace_bytes(B, Hq, Hkv, Sq, D), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(_load().attn_bwd_timeout_test(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                                         dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                                         B, Hq, Hkv, Sq, Skv, D, int(bool(causal)), float(scale),
+                                         int(drop_item), int(wait_budget_ns),
+                                         _stream_handle(stream)), "attn_bwd_timeout_test")
+    return dq, dk, dv
 
 
 def fwd_tail_timeout_test(q, k, v, causal: bool, scale: float,

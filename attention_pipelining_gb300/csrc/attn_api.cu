@@ -298,7 +298,8 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               void* workspace, size_t workspace_bytes, int B, int H_q, int H_kv,
                               int S_q, int S_kv, int D, int causal, float scale,
-                              bool deterministic, attn_stream_t stream) {
+                              bool deterministic, attn_stream_t stream, int drop_item = -1,
+                              unsigned long long timeout_ns = kDefaultTimeoutNs) {
   attn_status_t st = bwd_validate(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
                                   B, H_q, H_kv, S_q, S_kv, D, causal, scale);
   if (st != ATTN_OK) return st;
@@ -329,7 +330,8 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   p.groups = B * H_kv;
   p.scale = scale;
   p.scale_log2 = scale_log2_of(scale);
-  p.timeout_ns = kDefaultTimeoutNs;
+  p.timeout_ns = timeout_ns;
+  p.fault_drop_item = drop_item;
   if (launch_attn_bwd(p, D, o, dout, lse, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
@@ -824,6 +826,19 @@ attn_status_t attn_fwd_tail_timeout_test(const void* q, const void* k, const voi
     return ATTN_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H_q, H_kv, S_q, S_kv, D, causal, scale, nullptr, 0, 0, -1,
                   wait_budget_ns, stream, 1);
+}
+
+attn_status_t attn_bwd_timeout_test(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, void* workspace, size_t workspace_bytes, int B,
+                                    int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                                    float scale, int drop_item, unsigned long long wait_budget_ns,
+                                    attn_stream_t stream) {
+  if (drop_item < 0) return ATTN_ERR_INVALID_ARG;
+  if (wait_budget_ns < 1000000ull || wait_budget_ns > kDefaultTimeoutNs)
+    return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv,
+                  S_q, S_kv, D, causal, scale, false, stream, drop_item, wait_budget_ns);
 }
 
 int attn_fwd_tail_pairs(int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal) {

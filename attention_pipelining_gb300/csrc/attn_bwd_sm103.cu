@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
         }
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&ps_ready[h]);
+        if (!(w == 0 && h == 0 && n == p.fault_drop_item)) mbar_arrive(&ps_ready[h]);
       }
       ++n;
     }

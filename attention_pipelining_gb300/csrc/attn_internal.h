@@ -97,6 +97,11 @@ struct BwdParams {
   int R, Rp, groups;
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  // Test of the timeout path: when >= 0, the first elementwise warpgroup of
+  // the dK/dV kernel does not signal "P^T, dS^T stored" for half 0 of this
+  // work item (query block) of each CTA, so the issuer's bounded wait runs
+  // out.  -1 in normal use.
+  int fault_drop_item;
 };
 
 // Queues the backward on `stream`: with p.dq_acc set (D = 128) prep (which

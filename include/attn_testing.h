@@ -28,6 +28,17 @@
  * `wait_budget_ns` must lie in [1 ms, 2 s].  Outputs are unspecified.
  * For tests only.
  *
+ * attn_bwd_timeout_test runs attn_bwd (same arguments and buffers; the
+ * path that computes dQ inside the dK/dV kernel) with one difference: in
+ * every dK/dV CTA that reaches work item `drop_item` (its query blocks with
+ * work, counted from 0 in the order it walks them), the first elementwise
+ * warpgroup does not signal that the item's first half block of P^T and
+ * dS^T is stored, so the tensor-core issuer's wait for it runs out after
+ * `wait_budget_ns`.  Every role of the CTA unwinds (the dQ read-out warps
+ * included), the status word reads ATTN_ERR_TIMEOUT and the gradients are
+ * unspecified.  `drop_item` must be >= 0 and `wait_budget_ns` in [1 ms,
+ * 2 s] (else ATTN_ERR_INVALID_ARG).  For tests only.
+ *
  * attn_fwd_tail_pairs returns how many tiles attn_fwd splits across CTA
  * pairs for these sizes on the current device (0 when the tail is not
  * split), or -1 for invalid sizes or a device that cannot be queried.
@@ -51,6 +62,13 @@ attn_status_t attn_fwd_tail_timeout_test(const void *q, const void *k, const voi
                                          float *lse, int B, int H_q, int H_kv, int S_q, int S_kv,
                                          int D, int causal, float scale,
                                          unsigned long long wait_budget_ns, attn_stream_t stream);
+
+attn_status_t attn_bwd_timeout_test(const void *q, const void *k, const void *v, const void *o,
+                                    const float *lse, const void *dout, void *dq, void *dk,
+                                    void *dv, void *workspace, size_t workspace_bytes, int B,
+                                    int H_q, int H_kv, int S_q, int S_kv, int D, int causal,
+                                    float scale, int drop_item, unsigned long long wait_budget_ns,
+                                    attn_stream_t stream);
 
 int attn_fwd_tail_pairs(int B, int H_q, int H_kv, int S_q, int S_kv, int D, int causal);
 
