@@ -316,6 +316,28 @@ def calibrate_oracle(q, k, v, w, target_s: float):
     return max(1, int(target_s / per_row))
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU
+    baseline's record."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(q, k, v, w, target_s: float = 12.0) -> dict:
     import oracle
     n = calibrate_oracle(q, k, v, w, target_s)
@@ -325,6 +347,7 @@ def cpu_baseline(q, k, v, w, target_s: float = 12.0) -> dict:
         "value": row_flops(w, rows) / dt / 1e12,
         "unit": "TFLOP/s",
         "cores": oracle.num_threads(),
+        "cpu_model": host_cpu_model(),
         "kind": "oracle",
         "sample": f"{len(rows)} of {w.B * w.H_q * w.S_q} output rows of {w.name} "
                   f"(random rows, each over its full visible key range), fp64, {dt:.1f} s",
@@ -362,7 +385,7 @@ def run_reference(args, w):
         "config": {"workload": w.name, **{kk: vv for kk, vv in w.as_dict().items() if kk != "name"},
                    "sample_rows_per_step": n},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-                         "kind": "oracle",
+                         "cpu_model": host_cpu_model(), "kind": "oracle",
                          "sample": f"{n} random output rows of {w.name} per step, fp64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -680,6 +703,7 @@ def cpu_baseline_bwd(q, k, v, dout, w, target_s: float = 12.0) -> dict:
         n = min(w.B * w.H_q * w.S_q, max(n * 2, int(n * target_s / max(dt, 1e-3) / 2)))
     flops = 2.5 * row_flops(w, rows)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.default().num_threads(),
+            "cpu_model": host_cpu_model(),
             "kind": "oracle",
             "sample": f"dQ of {len(rows)} random query rows of {w.name} (each over its full "
                       f"visible key range), fp64, {dt:.1f} s"}
@@ -822,7 +846,8 @@ def cpu_baseline_chunk_scan(w, target_s: float = 12.0) -> dict:
     m = (rows // w.H) % w.Q                      # row within its chunk
     flops = float(2.0 * w.P * (m + 1).sum())
     return {"value": flops / dt_s / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.default().num_threads(), "kind": "oracle",
+            "cores": oracle.default().num_threads(), "cpu_model": host_cpu_model(),
+            "kind": "oracle",
             "sample": f"{len(rows)} random output rows of one batch item of {w.name}, fp64, "
                       f"{dt_s:.1f} s"}
 
