@@ -69,6 +69,9 @@ SHAPES = [
     (1, 3, 1, 77, 150, 64, False),      # three heads per group, tiny S_q
     (1, 1, 1, 513, 129, 128, True),     # S_kv < S_q, ragged tails
     (2, 2, 2, 640, 640, 64, True),
+    (1, 8, 1, 40, 96, 128, True),       # eight heads per group, one ragged key block
+    (2, 1, 1, 1, 33, 64, False),        # one query row: the second half block holds none
+    (1, 4, 4, 64, 64, 128, True),       # exactly one half block of rows per head
 ]
 
 
