@@ -402,9 +402,35 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
   // diagonal anyway)
   const int rot = (kFuse && !p.causal) ? kvb % n_qb : 0;
   auto qb_at = [&](int i) { return i + rot < n_qb ? i + rot : i + rot - n_qb; };
-  // query blocks with work, counted once here (every role walks the same list)
+  // The query blocks with work (items n = 0 .. n_work - 1), walked by every
+  // role in the same order.  With the causal mask and S_q a multiple of 128
+  // no block spans two heads, and block pb of a head sees keys kv0 .. when
+  // its last position pb * 128 + 127 >= kv0, i.e. pb >= kvb: the items are
+  // those blocks of each head in turn, found without a scan (a scan's
+  // division per skipped block cost a short CTA tens of microseconds).
+  // Otherwise (a ragged S_q) the blocks are scanned with qblock_sees.
+  const bool by_head = p.causal && (p.S_q % kRows == 0);
+  const int nqh = by_head ? p.S_q / kRows : 1;             // position blocks per head
+  const int per_head = by_head ? (nqh > kvb ? nqh - kvb : 0) : 0;
   int n_work = 0;
-  for (int qb = 0; qb < n_qb; ++qb) n_work += qblock_sees(p, qb * kRows, kv0) ? 1 : 0;
+  if (!p.causal) {
+    n_work = n_qb;
+  } else if (by_head) {
+    n_work = (p.R / p.S_q) * per_head;
+  } else {
+    for (int qb = 0; qb < n_qb; ++qb) n_work += qblock_sees(p, qb * kRows, kv0) ? 1 : 0;
+  }
+  // first row of item n's query block; `cursor` is the caller's scan
+  // position (the ragged causal case only; items are asked for in order)
+  auto item_r0 = [&](int n, int& cursor) -> int {
+    if (!p.causal) return qb_at(n) * kRows;
+    if (by_head) {
+      const int h = n / per_head;
+      return (h * nqh + kvb + (n - h * per_head)) * kRows;
+    }
+    while (cursor < n_qb - 1 && !qblock_sees(p, cursor * kRows, kv0)) ++cursor;
+    return (cursor++) * kRows;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -470,10 +496,9 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
         }
       }
     }
-    int n = 0;
-    for (int i = 0; i < n_qb && ok; ++i) {
-      const int r0 = qb_at(i) * kRows;
-      if (!qblock_sees(p, r0, kv0)) continue;
+    int cursor = 0;
+    for (int n = 0; n < n_work && ok; ++n) {
+      const int r0 = item_r0(n, cursor);
       const int s = n % C::kQStages;
       // masking: rows past R, keys past S_kv, and (causal) keys after a row's
       // position; a block needs none when every row sees every key
@@ -590,7 +615,6 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
         tc_fence_before_sync();
         if (!(w == 0 && h == 0 && n == p.fault_drop_item)) mbar_arrive(&ps_ready[h]);
       }
-      ++n;
     }
     // ---------------------------------------------------------- epilogue
     // warpgroup w writes columns [D/2 w, D/2 (w + 1)) of dV and dK
@@ -726,9 +750,9 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
       tma_load_tile<D>(sK, &p.tm_k, kv_full, kv0, zkv, pol_kv);
       tma_load_tile<D>(sV, &p.tm_v, kv_full, kv0, zkv, pol_kv);
     }
-    for (int i = 0; i < n_qb && ok; ++i) {
-      const int r0 = qb_at(i) * kRows;
-      if (!qblock_sees(p, r0, kv0)) continue;
+    int cursor = 0;
+    for (int n = 0; n < n_work && ok; ++n) {
+      const int r0 = item_r0(n, cursor);
       const int s = issued % C::kQStages;
       const int round = issued / C::kQStages;
       if (round > 0 && !warp_wait_b(&q_empty[s], (round - 1) & 1, sAbort, budget)) {
@@ -769,10 +793,9 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
     int nh = 0;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
-    int n = 0;
-    for (int i = 0; i < n_qb && ok; ++i) {
-      const int r0 = qb_at(i) * kRows;
-      if (!qblock_sees(p, r0, kv0)) continue;
+    int cursor = 0;
+    for (int n = 0; n < n_work && ok; ++n) {
+      const int r0 = item_r0(n, cursor);
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         if constexpr (D == 64) {
@@ -827,7 +850,6 @@ __global__ void __launch_bounds__(kFuse ? kThreadsFused : kThreadsB, 1)
           ++nh;
         }
       }
-      ++n;
     }
     // every bulk reduction has read its buffer and reached global memory
     if (D == 64 && threadIdx.x == 12 * 32) tma_store_wait_all();
