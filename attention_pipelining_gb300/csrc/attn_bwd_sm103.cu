@@ -9,27 +9,33 @@
 // 3.2 (Flash Attention backward on Blackwell: loads, tensor-core GEMMs and
 // the elementwise work in separate warp groups).
 //
-// Three kernels:
-//   prep   D_i and the base-2 LSE per row, into a padded per-group layout;
-//   dK/dV  one CTA per (row group, 128 keys): over the group's query blocks,
-//          S^T = K Q^T and dP^T = V dO^T on the tensor core, P^T and dS^T by
-//          two elementwise warpgroups (64 queries each), then dV += P^T dO and
-//          dK += dS^T Q accumulate in tensor memory;
-//   dQ     one CTA per (row group, 128 query rows): over the key blocks,
-//          S = Q K^T and dP = dO V^T, dS by the elementwise warpgroups (64
-//          keys each), dQ += dS K in tensor memory.
+// Two paths of three kernels each.  The default one (attn_bwd):
+//   prep     D_i and the base-2 LSE per row, into a padded per-group
+//            layout, and zeros for an fp32 dQ accumulator;
+//   dK/dV    one CTA per (row group, 128 keys): over the group's query
+//            blocks, S^T = K Q^T and dP^T = V dO^T on the tensor core, P^T
+//            and dS^T by two elementwise warpgroups (64 queries each), then
+//            dV += P^T dO and dK += dS^T Q accumulate in tensor memory, and
+//            dQ^T = K^T dS^T per half block, which a fourth warpgroup reads
+//            out and adds into the accumulator in L2 (kFuse);
+//   convert  dq = bf16(scale * accumulator).
+// The deterministic one (attn_bwd_deterministic) runs prep, dK/dV without
+// dQ, and
+//   dQ       one CTA per (row group, 128 query rows): over the key blocks,
+//            S = Q K^T and dP = dO V^T, dS by the elementwise warpgroups (64
+//            keys each), dQ += dS K in tensor memory.
 // P needs no running max in the backward (the forward's LSE normalises it),
-// so the elementwise work splits over columns with no exchange.  Every GEMM
-// has the forward's shapes (M = 128, N = 128 or D, K = D or 128).
+// so the elementwise work splits over columns with no exchange.
 //
 // Each 128 x 128 block runs as two halves of 64 columns, so the elementwise
 // warps work on one half while the tensor core computes the other.
 //
-// 384 threads: warps 0-7 elementwise (warpgroup w takes columns 32w..32w+31
-// of each half, thread = TMEM lane = the tile's row), warp 8 tensor-core
-// issuer and warp 9 TMA producer (warp-wide, one elected lane issues),
-// warps 10-11 idle.  Every wait is bounded; a timeout raises a
-// CTA-wide abort flag and the device status word records ATTN_ERR_TIMEOUT.
+// 384 threads (512 with the fused dQ): warps 0-7 elementwise (warpgroup w
+// takes columns 32w..32w+31 of each half, thread = TMEM lane = the tile's
+// row), warp 8 tensor-core issuer and warp 9 TMA producer (warp-wide, one
+// elected lane issues), warps 10-11 idle, warps 12-15 the dQ read-out.
+// Every wait is bounded; a timeout raises a CTA-wide abort flag and the
+// device status word records ATTN_ERR_TIMEOUT.
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -62,6 +68,21 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, uin
 }
 
 __device__ __forceinline__ float u2f_b(uint32_t x) { return __uint_as_float(x); }
+
+// Adds x to the fp32 at `addr` in global memory, performed in L2 (no
+// return value; relaxed, device scope).
+__device__ __forceinline__ void red_add_f32(float* addr, float x) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
+}
+
+// Adds `bytes` of fp32 from shared memory into global memory element by
+// element (performed in L2), tracked by the issuing thread's bulk groups like
+// a store.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+               ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
 
 // The work of a 128 x 128 block is done in two halves h = 0, 1 of 64
 // columns, so the elementwise warpgroups work on one half while the tensor

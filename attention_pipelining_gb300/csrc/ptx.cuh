@@ -300,21 +300,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// Adds x to the fp32 at `addr` in global memory, performed in L2 (no
-// return value; relaxed, device scope).
-__device__ __forceinline__ void red_add_f32(float* addr, float x) {
-  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(x) : "memory");
-}
-
-// Adds `bytes` of fp32 from shared memory into global memory element by
-// element (performed in L2), tracked by the issuing thread's bulk groups like
-// a store.  Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-               ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
