@@ -200,3 +200,35 @@ def test_chunk_scan_host_entry_rejects_before_queuing(lib):
     assert f(*([A] * 5), *([A] * 5), 1, 300, 4, 1, 64, 256, None) == 1  # L not a multiple of Q
     assert f(*([A] * 5), *([A] * 5), 1, 256, 4, 1, 128, 256, None) == 2  # P = 128
     assert f(*([A] * 5), A, A, A, A + 8, A, *dims) == 3                 # misaligned x
+
+
+def test_bwd_workspace_bytes(lib):
+    """4 (D + 2) bytes per query row, rows padded to a multiple of 128 per
+    (batch, kv-head) group: the per-row vectors and the fp32 dQ accumulator."""
+    R = (8 // 2) * 300                      # rows of a group
+    Rp = (R + 127) // 128 * 128
+    for D in (64, 128):
+        assert lib.attn_bwd_workspace_bytes(2, 8, 2, 300, D) == (D + 2) * 2 * 2 * Rp * 4
+    assert lib.attn_bwd_workspace_bytes(2, 8, 2, 300, 96) == 0
+    assert lib.attn_bwd_workspace_bytes(2, 8, 3, 300, 128) == 0
+    assert lib.attn_bwd_workspace_bytes(0, 8, 2, 300, 128) == 0
+
+
+def test_bwd_entries_reject_before_launch(lib):
+    """attn_bwd_deterministic and the backward's timeout hook share
+    attn_bwd's checks; every call here fails them (fake device addresses,
+    never dereferenced)."""
+    ws_bytes = lib.attn_bwd_workspace_bytes(1, 4, 2, 128, 128)
+    dims = [1, 4, 2, 128, 128, 128, 0, ctypes.c_float(0.1)]
+    bufs = [A] * 9
+    no_dout = [A] * 9
+    no_dout[5] = None
+    assert lib.attn_bwd_deterministic(*no_dout, A, ws_bytes, *dims, None) == 1
+    assert lib.attn_bwd_deterministic(*bufs, A, ws_bytes - 1, *dims, None) == 1
+    assert lib.attn_bwd_deterministic(*bufs, A + 16, ws_bytes, *dims, None) == 3
+    bad_d = [1, 4, 2, 128, 128, 96, 0, ctypes.c_float(0.1)]
+    assert lib.attn_bwd_deterministic(*bufs, A, ws_bytes, *bad_d, None) == 2
+    assert lib.attn_bwd_timeout_test(*bufs, A, ws_bytes, *dims, -1, 20_000_000, None) == 1
+    assert lib.attn_bwd_timeout_test(*bufs, A, ws_bytes, *dims, 1, 10, None) == 1
+    assert lib.attn_bwd_timeout_test(*bufs, A, ws_bytes, *dims, 1, 10**10, None) == 1
+    assert lib.attn_bwd_timeout_test(*bufs, A, ws_bytes, *bad_d, 1, 20_000_000, None) == 2
