@@ -72,6 +72,11 @@ SHAPES = [
     (1, 8, 1, 40, 96, 128, True),       # eight heads per group, one ragged key block
     (2, 1, 1, 1, 33, 64, False),        # one query row: the second half block holds none
     (1, 4, 4, 64, 64, 128, True),       # exactly one half block of rows per head
+    # causal with S_q a multiple of 128 (visible query blocks computed per
+    # head): keys past the last position (no query block sees key block 2),
+    # and more positions than keys
+    (1, 2, 1, 256, 384, 128, True),
+    (1, 4, 2, 384, 256, 64, True),
 ]
 
 
